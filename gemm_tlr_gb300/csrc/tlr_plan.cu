@@ -1,0 +1,1630 @@
+// Host side of the Tile-Low-Rank GEMM library: descriptor validation, operand
+// views, the rank-metadata planner, descriptor-table building and launches.
+//
+//   C <- alpha op(A) op(B) + beta C   ("Tile-Low-Rank GEMM: Designing Storage
+//   Around the Contraction", opening section)
+//
+// Plan (same page, "Association order and workspace"): from ranks alone,
+//   - rho_i / gamma_j (rank sums) give the final-stage costs of the two
+//     association orders, F_R = sum_i 2 d_i W_J rho_i (U (S Z^T), one product
+//     per tile row) and F_L = sum_j 2 d_j H_I gamma_j ((U S) Z^T, one per tile
+//     column);
+//   - C is split into rectangles of output tiles that fit the workspace:
+//     widest feasible block of tile columns first, then the longest runs of tile
+//     rows; each rectangle holds the full reduction over k and takes the cheaper
+//     feasible order; rectangles run in sequence over one arena.
+// The left order is evaluated as the right order of the transposed product
+// C^T = op(B)^T op(A)^T with a transposed store of the output tile, so both
+// orders share one kernel path.
+//
+// Per rectangle three launches of the task kernel (section "One product, three
+// stages"):
+//   L1  Stage 1 S_k = V_{:,k}^T W_{k,:} per contraction tile k (fused over i
+//       and j), plus P_i = D_ii W_{i,:} (first half of D_A O_B) and the k=j block
+//       V_ij^T D_jj of T_i (O_A D_B), both from "TLR Matrix Multiplication",
+//       section "The easy terms";
+//   L2  Stage 2 T_i[k-block, j-block] = S_ikj Z_kj^T, fused over i (rows of one
+//       product scatter into the terminal matrices of several tile rows);
+//   L3  Stage 3 C[i, J] = alpha (U_i T_i + P_ij Z_ij^T | D_ii D_ii) + beta C:
+//       the sum over k is the tensor-core K-loop over the packed row panel U_i,
+//       and the dense-diagonal terms are one more K segment of the same
+//       accumulator, so every element of C is read and written once.
+// One-TLR-operand products (dense B) skip Stage 2: L1 writes T_i rows
+// V_{:,k}^T B_k directly, and L3 adds the segment D_ii B_i.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <functional>
+#include <map>
+#include <new>
+#include <string>
+#include <set>
+#include <tuple>
+#include <vector>
+
+#include "tlr_gemm.h"
+#include "tlr_tables.h"
+
+namespace tlr {
+cudaError_t launch_task_gemm(bool tf32, const Params &p, int grid, cudaStream_t stream);
+cudaError_t launch_round_tf32(const float *const *src, float *const *dst, const int64_t *count, int n,
+                              int grid, cudaStream_t stream);
+cudaError_t launch_scale_c(float *C, int64_t ldc, int64_t m, int64_t n, float beta, int grid,
+                           cudaStream_t stream);
+cudaError_t launch_unsatisfied_wait(const Params &p, cudaStream_t stream);
+}  // namespace tlr
+
+using namespace tlr;
+
+namespace {
+
+constexpr int kKindStage1 = 0, kKindStage2 = 1, kKindStage3 = 2, kKindRound = 3, kKindScale = 4;
+constexpr int kNumKinds = 5;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t align_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// ------------------------------------------------------------------ views
+struct View {            // column-major matrix in device memory (elements)
+  uint64_t addr = 0;
+  int64_t rows = 0, cols = 0, ld = 0;
+};
+
+View sub_cols(const View &v, int64_t c0, int64_t c1, int es) {
+  View s = v;
+  s.addr = v.addr + static_cast<uint64_t>(c0 * v.ld * es);
+  s.cols = c1 - c0;
+  return s;
+}
+
+struct Part {            // contiguous run of one panel: tiles [t0, t1) of the panel index
+  View v;                // d x (columns of the run)
+  int t0 = 0, t1 = 0;
+  int64_t col0 = 0;      // column of the run's first tile within the whole panel
+};
+
+// Stored TLR matrix (before op).
+struct Stored {
+  int ntr = 0, ntc = 0, m = 0;
+  int64_t b = 0, brem = 0;
+  bool boundary = false, diag_dense = false;
+  std::vector<int64_t> rd, cd;
+  std::vector<int32_t> rank;          // ntr*ntc, 0 on dense tiles
+  std::vector<View> outer, inner;     // per low-rank tile
+  std::vector<View> diag;             // per dense diagonal tile
+  std::vector<std::vector<Part>> rowp, colp;
+  std::vector<std::vector<int64_t>> rpos, cpos;   // tile column inside its row / col panel
+  std::vector<int64_t> ucol, vcol;    // packed column offset of each low-rank tile in its buffer
+};
+
+// Logical operand op(X): either a TLR grid or a dense matrix.
+struct LOp {
+  bool dense = false;
+  int nr = 0, nc = 0;
+  std::vector<int64_t> rd, cd, ro, co;
+  std::vector<int32_t> rank;
+  std::vector<uint8_t> dtile;          // dense tile (diagonal) flag
+  std::vector<View> outer, inner;      // op(X)_ik = outer inner^T
+  std::vector<View> diag;              // stored dense tile behind op(X)_ii
+  bool diag_trans = false;             // op(X)_ii = stored^T
+  std::vector<std::vector<Part>> rowp, colp;
+  std::vector<std::vector<int64_t>> rpos, cpos;
+  View dv;                             // dense: stored matrix
+  bool dtrans = false;                 // dense: op = T
+  int32_t r(int i, int k) const { return rank[static_cast<size_t>(i) * nc + k]; }
+  bool dt(int i, int k) const { return dtile[static_cast<size_t>(i) * nc + k] != 0; }
+};
+
+struct Operand {                       // validated descriptor plus device base addresses
+  tlr_operand_t d;
+  Stored s;
+  int64_t u_elems = 0, v_elems = 0, d_elems = 0, buU = 0, buV = 0, bvU = 0, bvV = 0, g_elems = 0;
+};
+
+int elem_size(int dtype) { return dtype == TLR_BF16 ? 2 : 4; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Compute stored geometry, packed offsets and the element count of each buffer.
+tlr_status_t describe(const tlr_operand_t &d, Operand &o, bool check_pointers) {
+  o.d = d;
+  if (d.dtype != TLR_F32 && d.dtype != TLR_BF16) return TLR_STATUS_INVALID_ARG;
+  if (d.rows <= 0 || d.cols <= 0) return TLR_STATUS_INVALID_ARG;
+  const int es = elem_size(d.dtype);
+  const int amod = 16 / es;
+  if (d.kind == TLR_KIND_DENSE) {
+    if (d.ld < d.rows) return TLR_STATUS_INVALID_ARG;
+    if ((d.ld * es) % 16) return TLR_STATUS_ALIGNMENT;
+    if (check_pointers) {
+      if (!d.data) return TLR_STATUS_INVALID_ARG;
+      if (!aligned16(d.data)) return TLR_STATUS_ALIGNMENT;
+    }
+    return TLR_STATUS_OK;
+  }
+  if (d.kind != TLR_KIND_TLR) return TLR_STATUS_INVALID_ARG;
+  if (d.b <= 0 || !d.ranks) return TLR_STATUS_INVALID_ARG;
+  Stored &s = o.s;
+  s.b = d.b;
+  s.diag_dense = d.diag_dense != 0;
+  s.ntr = static_cast<int>(ceil_div(d.rows, d.b));
+  s.ntc = static_cast<int>(ceil_div(d.cols, d.b));
+  s.boundary = (d.rows % d.b) != 0 || (d.cols % d.b) != 0;
+  if (s.diag_dense && d.rows != d.cols) return TLR_STATUS_INVALID_ARG;
+  if (s.boundary && !s.diag_dense) return TLR_STATUS_UNSUPPORTED;
+  s.m = s.boundary ? static_cast<int>(d.rows / d.b) : -1;
+  s.brem = s.boundary ? d.rows - static_cast<int64_t>(s.m) * d.b : 0;
+  if (s.boundary && s.m < 1) return TLR_STATUS_UNSUPPORTED;
+  for (int i = 0; i < s.ntr; ++i) s.rd.push_back(std::min<int64_t>(d.b, d.rows - i * d.b));
+  for (int k = 0; k < s.ntc; ++k) s.cd.push_back(std::min<int64_t>(d.b, d.cols - k * d.b));
+  for (int64_t x : s.rd) if (x % amod) return TLR_STATUS_ALIGNMENT;
+  for (int64_t x : s.cd) if (x % amod) return TLR_STATUS_ALIGNMENT;
+  const size_t nt = static_cast<size_t>(s.ntr) * s.ntc;
+  s.rank.assign(nt, 0);
+  for (int i = 0; i < s.ntr; ++i)
+    for (int k = 0; k < s.ntc; ++k) {
+      if (s.diag_dense && i == k) continue;
+      const int32_t r = d.ranks[static_cast<size_t>(i) * s.ntc + k];
+      if (r < 0 || r > s.rd[i] || r > s.cd[k]) return TLR_STATUS_INVALID_ARG;
+      s.rank[static_cast<size_t>(i) * s.ntc + k] = r;
+    }
+  auto R = [&](int i, int k) { return static_cast<int64_t>(s.rank[static_cast<size_t>(i) * s.ntc + k]); };
+  auto lowrank = [&](int i, int k) { return !(s.diag_dense && i == k); };
+  const int nr = s.boundary ? s.m : s.ntr, nc = s.boundary ? s.m : s.ntc;
+  // packed column offsets (in factor columns)
+  std::vector<int64_t> ucol(nt, -1), vcol(nt, -1);
+  int64_t c = 0;
+  for (int i = 0; i < nr; ++i)
+    for (int k = 0; k < nc; ++k)
+      if (lowrank(i, k)) { ucol[static_cast<size_t>(i) * s.ntc + k] = c; c += R(i, k); }
+  const int64_t ucols = c;
+  c = 0;
+  for (int k = 0; k < nc; ++k)
+    for (int i = 0; i < nr; ++i)
+      if (lowrank(i, k)) { vcol[static_cast<size_t>(i) * s.ntc + k] = c; c += R(i, k); }
+  int64_t bu_cols = 0, bv_cols = 0;
+  if (s.boundary) {
+    for (int i = 0; i < s.m; ++i) { ucol[static_cast<size_t>(i) * s.ntc + s.m] = bu_cols; vcol[static_cast<size_t>(i) * s.ntc + s.m] = bu_cols; bu_cols += R(i, s.m); }
+    for (int j = 0; j < s.m; ++j) { ucol[static_cast<size_t>(s.m) * s.ntc + j] = bv_cols; vcol[static_cast<size_t>(s.m) * s.ntc + j] = bv_cols; bv_cols += R(s.m, j); }
+  }
+  o.u_elems = d.b * ucols;
+  o.v_elems = d.b * ucols;
+  o.d_elems = s.diag_dense ? static_cast<int64_t>(d.b) * d.b * nr : 0;
+  o.buU = d.b * bu_cols;
+  o.buV = s.brem * bu_cols;
+  o.bvU = s.brem * bv_cols;
+  o.bvV = d.b * bv_cols;
+  o.g_elems = s.boundary ? s.brem * s.brem : 0;
+  // optional caller offsets must agree with the prefix sums
+  for (int i = 0; i < s.ntr; ++i)
+    for (int k = 0; k < s.ntc; ++k) {
+      if (!lowrank(i, k)) continue;
+      const size_t t = static_cast<size_t>(i) * s.ntc + k;
+      if (d.u_offsets && d.u_offsets[t] != s.rd[i] * ucol[t]) return TLR_STATUS_INVALID_ARG;
+      if (d.v_offsets && d.v_offsets[t] != s.cd[k] * vcol[t]) return TLR_STATUS_INVALID_ARG;
+    }
+  if (check_pointers) {
+    if ((ucols > 0) && (!d.U || !d.V)) return TLR_STATUS_INVALID_ARG;
+    if (o.d_elems > 0 && !d.D) return TLR_STATUS_INVALID_ARG;
+    if (bu_cols > 0 && (!d.bu_U || !d.bu_V)) return TLR_STATUS_INVALID_ARG;
+    if (bv_cols > 0 && (!d.bv_U || !d.bv_V)) return TLR_STATUS_INVALID_ARG;
+    if (s.boundary && !d.gamma) return TLR_STATUS_INVALID_ARG;
+    for (const void *p : {d.U, d.V, d.D, d.bu_U, d.bu_V, d.bv_U, d.bv_V, d.gamma})
+      if (p && !aligned16(p)) return TLR_STATUS_ALIGNMENT;
+  }
+  s.rpos.assign(s.ntr, std::vector<int64_t>(s.ntc, -1));
+  s.cpos.assign(s.ntc, std::vector<int64_t>(s.ntr, -1));
+  s.ucol = ucol;
+  s.vcol = vcol;
+  return TLR_STATUS_OK;
+}
+
+// Attach device addresses (possibly of rounded copies) to the stored views and
+// build the row / column panels.
+void bind(Operand &o, uint64_t U, uint64_t V, uint64_t D, uint64_t buU, uint64_t buV, uint64_t bvU,
+          uint64_t bvV, uint64_t G) {
+  Stored &s = o.s;
+  const int es = elem_size(o.d.dtype);
+  const int64_t b = s.b;
+  const size_t nt = static_cast<size_t>(s.ntr) * s.ntc;
+  const std::vector<int64_t> &ucol = s.ucol, &vcol = s.vcol;
+  s.outer.assign(nt, View{});
+  s.inner.assign(nt, View{});
+  auto lowrank = [&](int i, int k) { return !(s.diag_dense && i == k); };
+  for (int i = 0; i < s.ntr; ++i)
+    for (int k = 0; k < s.ntc; ++k) {
+      const size_t t = static_cast<size_t>(i) * s.ntc + k;
+      if (!lowrank(i, k)) { s.outer[t] = View{}; s.inner[t] = View{}; continue; }
+      const int64_t di = s.rd[i], dk = s.cd[k], r = s.rank[t];
+      uint64_t ub = U, vb = V;
+      if (s.boundary && k == s.m && i < s.m) { ub = buU; vb = buV; }
+      else if (s.boundary && i == s.m && k < s.m) { ub = bvU; vb = bvV; }
+      s.outer[t] = View{ub + static_cast<uint64_t>(di * ucol[t] * es), di, r, di};
+      s.inner[t] = View{vb + static_cast<uint64_t>(dk * vcol[t] * es), dk, r, dk};
+    }
+  s.diag.assign(s.ntr, View{});
+  if (s.diag_dense)
+    for (int i = 0; i < s.ntr; ++i) {
+      if (s.boundary && i == s.m) s.diag[i] = View{G, s.brem, s.brem, s.brem};
+      else s.diag[i] = View{D + static_cast<uint64_t>(b * b * i * es), b, b, b};
+    }
+  // panels: a part is a run of consecutive tiles that share one buffer
+  s.rowp.assign(s.ntr, {});
+  s.colp.assign(s.ntc, {});
+  for (int i = 0; i < s.ntr; ++i) {
+    int64_t pos = 0;
+    for (int k = 0; k < s.ntc; ++k) {
+      if (!lowrank(i, k)) continue;
+      const size_t t = static_cast<size_t>(i) * s.ntc + k;
+      const View &v = s.outer[t];
+      s.rpos[i][k] = pos;
+      std::vector<Part> &P = s.rowp[i];
+      const bool contiguous = !P.empty() &&
+                              P.back().v.addr + static_cast<uint64_t>(P.back().v.cols * P.back().v.ld * es) == v.addr &&
+                              P.back().v.ld == v.ld;
+      if (contiguous) { P.back().v.cols += v.cols; P.back().t1 = k + 1; }
+      else P.push_back(Part{View{v.addr, v.rows, v.cols, v.ld}, k, k + 1, pos});
+      pos += v.cols;
+    }
+  }
+  for (int k = 0; k < s.ntc; ++k) {
+    int64_t pos = 0;
+    for (int i = 0; i < s.ntr; ++i) {
+      if (!lowrank(i, k)) continue;
+      const size_t t = static_cast<size_t>(i) * s.ntc + k;
+      const View &v = s.inner[t];
+      s.cpos[k][i] = pos;
+      std::vector<Part> &P = s.colp[k];
+      const bool contiguous = !P.empty() &&
+                              P.back().v.addr + static_cast<uint64_t>(P.back().v.cols * P.back().v.ld * es) == v.addr &&
+                              P.back().v.ld == v.ld;
+      if (contiguous) { P.back().v.cols += v.cols; P.back().t1 = i + 1; }
+      else P.push_back(Part{View{v.addr, v.rows, v.cols, v.ld}, i, i + 1, pos});
+      pos += v.cols;
+    }
+  }
+}
+
+// op(X) as a logical operand. Transposition swaps the factor families and the
+// tile coordinates ("Tile-Low-Rank GEMM: Designing Storage Around the
+// Contraction", section "Where fusion stops", paragraph "Transposes").
+LOp logical(const Operand &o, bool trans, int64_t pseudo_b) {
+  LOp L;
+  if (o.d.kind == TLR_KIND_DENSE) {
+    L.dense = true;
+    L.dv = View{reinterpret_cast<uint64_t>(o.d.data), o.d.rows, o.d.cols, o.d.ld};
+    L.dtrans = trans;
+    const int64_t R = trans ? o.d.cols : o.d.rows, Cc = trans ? o.d.rows : o.d.cols;
+    for (int64_t x = 0; x < R; x += pseudo_b) L.rd.push_back(std::min(pseudo_b, R - x));
+    for (int64_t x = 0; x < Cc; x += pseudo_b) L.cd.push_back(std::min(pseudo_b, Cc - x));
+  } else {
+    const Stored &s = o.s;
+    L.rd = trans ? s.cd : s.rd;
+    L.cd = trans ? s.rd : s.cd;
+    L.nr = trans ? s.ntc : s.ntr;
+    L.nc = trans ? s.ntr : s.ntc;
+    const size_t nt = static_cast<size_t>(L.nr) * L.nc;
+    L.rank.assign(nt, 0);
+    L.dtile.assign(nt, 0);
+    L.outer.assign(nt, View{});
+    L.inner.assign(nt, View{});
+    for (int i = 0; i < L.nr; ++i)
+      for (int k = 0; k < L.nc; ++k) {
+        const int si = trans ? k : i, sk = trans ? i : k;
+        const size_t st = static_cast<size_t>(si) * s.ntc + sk, lt = static_cast<size_t>(i) * L.nc + k;
+        L.rank[lt] = s.rank[st];
+        L.dtile[lt] = (s.diag_dense && si == sk) ? 1 : 0;
+        L.outer[lt] = trans ? s.inner[st] : s.outer[st];
+        L.inner[lt] = trans ? s.outer[st] : s.inner[st];
+      }
+    L.diag = s.diag;
+    L.diag_trans = trans;
+    L.rowp = trans ? s.colp : s.rowp;
+    L.colp = trans ? s.rowp : s.colp;
+    L.rpos = trans ? s.cpos : s.rpos;
+    L.cpos = trans ? s.rpos : s.cpos;
+  }
+  L.nr = static_cast<int>(L.rd.size());
+  L.nc = static_cast<int>(L.cd.size());
+  L.ro.assign(L.nr + 1, 0);
+  L.co.assign(L.nc + 1, 0);
+  for (int i = 0; i < L.nr; ++i) L.ro[i + 1] = L.ro[i] + L.rd[i];
+  for (int k = 0; k < L.nc; ++k) L.co[k + 1] = L.co[k] + L.cd[k];
+  return L;
+}
+
+// Parts of a panel restricted to tiles [t0, t1): (sub-view, first tile, row offset in the result).
+struct RPart {
+  View v;
+  std::vector<std::pair<int, int64_t>> tiles;   // (tile, column inside v)
+  std::vector<int64_t> width;                   // rank of each listed tile
+};
+
+std::vector<RPart> restrict_panel(const std::vector<Part> &parts, const std::vector<int64_t> &pos,
+                                  int t0, int t1, const std::function<int64_t(int)> &rank_of, int es) {
+  std::vector<RPart> out;
+  for (const Part &p : parts) {
+    const int a = std::max(p.t0, t0), e = std::min(p.t1, t1);
+    if (a >= e) continue;
+    RPart rp;
+    int64_t c0 = -1, c1 = -1;
+    for (int t = a; t < e; ++t) {
+      if (pos[t] < 0) continue;
+      const int64_t r = rank_of(t);
+      const int64_t local = pos[t] - p.col0;
+      if (c0 < 0) c0 = local;
+      c1 = local + r;
+      rp.tiles.push_back({t, local});
+      rp.width.push_back(r);
+    }
+    if (c0 < 0 || c1 <= c0) continue;
+    rp.v = sub_cols(p.v, c0, c1, es);
+    for (auto &tl : rp.tiles) tl.second -= c0;
+    out.push_back(rp);
+  }
+  return out;
+}
+
+// ------------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+struct Rect {
+  int i0, i1, j0, j1;
+  bool left;
+};
+
+struct Launch {
+  int kind;
+  int64_t t0, t1;
+};
+
+// ------------------------------------------------------------------ builder
+struct Builder {
+  const LOp &X;
+  const LOp &Y;
+  int es;
+  bool tf32;
+  int bn;
+  bool trans_out;
+  uint64_t ws;                          // arena base for this rectangle
+  std::vector<CUtensorMap> *maps;
+  std::map<std::tuple<uint64_t, int64_t, int64_t, int64_t, int>, int> *map_index;
+  std::vector<Task> *tasks;
+  std::vector<Seg> *segs;
+  std::vector<Piece> *pieces;
+  std::vector<Out> *outs;
+  tlr_status_t status = TLR_STATUS_OK;
+  double fl_s1 = 0, fl_s2 = 0, fl_s3 = 0, fl_dense = 0, fl_final = 0;
+  bool dry = false;                     // validate only: no tensor maps are encoded
+  std::vector<std::pair<View, int>> *views = nullptr;   // every map's view and majorness
+
+  int map_of(const View &v, bool mn) {
+    auto key = std::make_tuple(v.addr, v.rows, v.cols, v.ld, mn ? 1 : 0);
+    auto it = map_index->find(key);
+    if (it != map_index->end()) return it->second;
+    CUtensorMap m;
+    memset(&m, 0, sizeof m);
+    if (views) views->push_back({v, mn ? 1 : 0});
+    if (dry) {
+      const int idx = static_cast<int>(maps->size());
+      maps->push_back(m);
+      (*map_index)[key] = idx;
+      return idx;
+    }
+    const int ch = 128 / es;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(v.rows), static_cast<cuuint64_t>(v.cols)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(v.ld * es)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(ch), static_cast<cuuint32_t>(mn ? ch : 64)};
+    cuuint32_t estr[2] = {1, 1};
+    auto fn = encode_fn();
+    if (!fn || v.rows <= 0 || v.cols <= 0) { status = TLR_STATUS_CUDA_ERROR; return 0; }
+    CUresult r = fn(&m, es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                    reinterpret_cast<void *>(v.addr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) { status = TLR_STATUS_CUDA_ERROR; return 0; }
+    const int idx = static_cast<int>(maps->size());
+    maps->push_back(m);
+    (*map_index)[key] = idx;
+    return idx;
+  }
+
+  int out_ws(uint64_t ptr, int64_t ld) {
+    Out o;
+    o.ptr = reinterpret_cast<void *>(ptr);
+    o.ld = ld;
+    o.kind = tf32 ? kOutTF32 : kOutBF16;
+    o.trans = 0;
+    outs->push_back(o);
+    return static_cast<int>(outs->size()) - 1;
+  }
+  int out_c() {
+    Out o;
+    o.ptr = nullptr;
+    o.ld = 0;
+    o.kind = kOutC;
+    o.trans = trans_out ? 1 : 0;
+    outs->push_back(o);
+    return static_cast<int>(outs->size()) - 1;
+  }
+  void emit(int out, int64_t row0, int64_t col0, int64_t rows, int64_t cols, const std::vector<Seg> &sg,
+            const std::vector<Piece> &pc) {
+    Task t;
+    memset(&t, 0, sizeof t);
+    t.seg0 = static_cast<int32_t>(segs->size());
+    t.nseg = static_cast<int32_t>(sg.size());
+    t.out = out;
+    t.rows = static_cast<int32_t>(rows);
+    t.cols = static_cast<int32_t>(cols);
+    t.piece0 = static_cast<int32_t>(pieces->size());
+    t.npiece = static_cast<int32_t>(pc.size());
+    t.row0 = row0;
+    t.col0 = col0;
+    segs->insert(segs->end(), sg.begin(), sg.end());
+    pieces->insert(pieces->end(), pc.begin(), pc.end());
+    tasks->push_back(t);
+  }
+  static Seg seg(int am, int bm, bool amn, bool bmn, int64_t a_mn0, int64_t b_mn0, int64_t k_len) {
+    Seg s;
+    s.a_map = am;
+    s.b_map = bm;
+    s.a_x = static_cast<int32_t>(amn ? a_mn0 : 0);
+    s.a_y = static_cast<int32_t>(amn ? 0 : a_mn0);
+    s.b_x = static_cast<int32_t>(bmn ? b_mn0 : 0);
+    s.b_y = static_cast<int32_t>(bmn ? 0 : b_mn0);
+    s.k_len = static_cast<int32_t>(k_len);
+    s.flags = (amn ? kSegAMN : 0u) | (bmn ? kSegBMN : 0u);
+    return s;
+  }
+};
+
+// Workspace layout of one rectangle (right order on X * Y).
+struct RectLayout {
+  int i0, i1, j0, j1;
+  int64_t WJ = 0;
+  std::vector<int64_t> colT;                 // per j in [j0, j1]: column inside T / the C block
+  std::vector<int64_t> Soff, Sld, Srows;     // per k
+  std::vector<std::vector<int64_t>> Scol;    // per k, per j: column of block j in S_k (-1: none)
+  std::vector<int64_t> R;                    // per i: first T row
+  std::vector<std::vector<int64_t>> Toff;    // per i, per part: first T row of the part
+  int64_t Tld = 0, Toffset = 0;
+  std::vector<int64_t> Poff;                 // per i
+  std::vector<std::vector<int64_t>> Pcol;    // per i, per j
+  int64_t bytes = 0;
+};
+
+RectLayout layout_rect(const LOp &X, const LOp &Y, int i0, int i1, int j0, int j1, int es) {
+  RectLayout L;
+  L.i0 = i0; L.i1 = i1; L.j0 = j0; L.j1 = j1;
+  L.colT.assign(j1 - j0 + 1, 0);
+  for (int j = j0; j < j1; ++j) L.colT[j - j0 + 1] = L.colT[j - j0] + Y.cd[j];
+  L.WJ = L.colT.back();
+  int64_t off = 0;
+  const int nk = X.nc;
+  L.Soff.assign(nk, -1); L.Sld.assign(nk, 0); L.Srows.assign(nk, 0); L.Scol.assign(nk, {});
+  if (!Y.dense) {
+    for (int k = 0; k < nk; ++k) {
+      int64_t sig = 0;
+      for (int i = i0; i < i1; ++i) if (!X.dt(i, k)) sig += X.r(i, k);
+      L.Srows[k] = sig;
+      L.Scol[k].assign(j1 - j0, -1);
+      int64_t g = 0;
+      for (int j = j0; j < j1; ++j)
+        if (!Y.dt(k, j) && Y.r(k, j) > 0) { L.Scol[k][j - j0] = g; g += Y.r(k, j); }
+      if (sig == 0 || g == 0) continue;
+      L.Sld[k] = align_up(sig, 8);
+      L.Soff[k] = off;
+      off = align_up(off + L.Sld[k] * g * es, 256);
+    }
+  }
+  // T: rows of each part of each tile row padded to 8 (16-byte aligned bases)
+  L.R.assign(X.nr, 0);
+  L.Toff.assign(X.nr, {});
+  int64_t rows = 0;
+  for (int i = i0; i < i1; ++i) {
+    L.R[i] = rows;
+    for (const Part &p : X.rowp[i]) {
+      L.Toff[i].push_back(rows);
+      rows += align_up(p.v.cols, 8);
+    }
+  }
+  L.Tld = align_up(std::max<int64_t>(rows, 8), 8);
+  L.Toffset = off;
+  off = align_up(off + L.Tld * L.WJ * es, 256);
+  // P_i = D_ii W_{i,J}
+  L.Poff.assign(X.nr, -1);
+  L.Pcol.assign(X.nr, {});
+  if (!Y.dense) {
+    for (int i = i0; i < i1; ++i) {
+      if (!(i < X.nc && X.dt(i, i))) continue;
+      L.Pcol[i].assign(j1 - j0, -1);
+      int64_t g = 0;
+      for (int j = j0; j < j1; ++j)
+        if (!Y.dt(i, j) && Y.r(i, j) > 0) { L.Pcol[i][j - j0] = g; g += Y.r(i, j); }
+      if (g == 0) continue;
+      L.Poff[i] = off;
+      off = align_up(off + X.rd[i] * g * es, 256);
+    }
+  }
+  L.bytes = off;
+  return L;
+}
+
+// Final-stage cost of the right order on X * Y over a rectangle.
+double final_cost(const LOp &X, int i0, int i1, int64_t WJ) {
+  double f = 0;
+  for (int i = i0; i < i1; ++i) {
+    int64_t rho = 0;
+    for (int k = 0; k < X.nc; ++k) if (!X.dt(i, k)) rho += X.r(i, k);
+    f += 2.0 * static_cast<double>(X.rd[i]) * static_cast<double>(WJ) * static_cast<double>(rho);
+  }
+  return f;
+}
+
+std::vector<Piece> pieces_for(const RPart &rp, int64_t row_base_in_space, int64_t w0, int64_t rows,
+                              const std::function<int64_t(int)> &dst_of) {
+  // rp's tiles occupy rows [row_base + local, +width) of the product's row space
+  std::vector<Piece> pc;
+  for (size_t q = 0; q < rp.tiles.size(); ++q) {
+    const int64_t s = row_base_in_space + rp.tiles[q].second, e = s + rp.width[q];
+    const int64_t a = std::max(s, w0), b = std::min(e, w0 + rows);
+    if (a >= b) continue;
+    Piece p;
+    p.src0 = static_cast<int32_t>(a - w0);
+    p.len = static_cast<int32_t>(b - a);
+    p.dst0 = dst_of(rp.tiles[q].first) + (a - s);
+    pc.push_back(p);
+  }
+  return pc;
+}
+
+// Build the tasks of one rectangle into the three launch lists.
+void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vector<Task> &l2,
+                std::vector<Task> &l3, std::vector<Seg> &segs, std::vector<Piece> &pieces) {
+  const LOp &X = B.X;
+  const LOp &Y = B.Y;
+  const int es = B.es, bn = B.bn;
+  const int i0 = L.i0, i1 = L.i1, j0 = L.j0, j1 = L.j1;
+  const uint64_t T = B.ws + static_cast<uint64_t>(L.Toffset);
+  const int outT = B.out_ws(T, L.Tld);
+  // T row of tile (i, k) of op(X)
+  auto trow = [&](int i, int k) -> int64_t {
+    const auto &parts = X.rowp[i];
+    for (size_t pi = 0; pi < parts.size(); ++pi)
+      if (k >= parts[pi].t0 && k < parts[pi].t1)
+        return L.Toff[i][pi] + (X.rpos[i][k] - parts[pi].col0);
+    return -1;
+  };
+  auto rank_col = [&](int k) { return [&X, k](int i) { return static_cast<int64_t>(X.r(i, k)); }; };
+
+  // ---------------- L1: Stage 1, P, k=j blocks (or the dense-B product)
+  B.tasks = &l1;
+  for (int k = 0; k < X.nc; ++k) {
+    std::vector<RPart> Ap = restrict_panel(X.colp[k], X.cpos[k], i0, i1, rank_col(k), es);
+    if (Ap.empty()) continue;
+    if (Y.dense) {
+      // rows k of op(B), columns of the rectangle
+      View yk;
+      bool ymn = Y.dtrans;
+      const int64_t c0 = Y.co[j0];
+      if (!Y.dtrans) yk = View{Y.dv.addr + static_cast<uint64_t>((Y.ro[k] + c0 * Y.dv.ld) * es), Y.rd[k], L.WJ, Y.dv.ld};
+      else yk = View{Y.dv.addr + static_cast<uint64_t>((c0 + Y.ro[k] * Y.dv.ld) * es), L.WJ, Y.rd[k], Y.dv.ld};
+      const int bm = B.map_of(yk, ymn);
+      int64_t base = 0;
+      for (const RPart &ap : Ap) {
+        const int am = B.map_of(ap.v, false);
+        for (int64_t mt = 0; mt < ceil_div(ap.v.cols, kBM); ++mt)
+          for (int64_t nt = 0; nt < ceil_div(L.WJ, bn); ++nt) {
+            const int64_t rows = std::min<int64_t>(kBM, ap.v.cols - mt * kBM);
+            auto pc = pieces_for(ap, 0, mt * kBM, rows, [&](int i) { return trow(i, k); });
+            B.emit(outT, 0, nt * bn, rows, std::min<int64_t>(bn, L.WJ - nt * bn),
+                   {Builder::seg(am, bm, false, ymn, mt * kBM, nt * bn, X.cd[k])}, pc);
+          }
+        B.fl_s1 += 2.0 * ap.v.cols * static_cast<double>(L.WJ) * X.cd[k];
+        base += ap.v.cols;
+      }
+      continue;
+    }
+    // Stage 1: S_k = V_{:,k}^T W_{k,:}
+    if (L.Soff[k] >= 0) {
+      const uint64_t S = B.ws + static_cast<uint64_t>(L.Soff[k]);
+      const int outS = B.out_ws(S, L.Sld[k]);
+      std::vector<RPart> Bp = restrict_panel(Y.rowp[k], Y.rpos[k], j0, j1,
+                                             [&Y, k](int j) { return static_cast<int64_t>(Y.r(k, j)); }, es);
+      int64_t ra = 0;
+      for (const RPart &ap : Ap) {
+        const int am = B.map_of(ap.v, false);
+        int64_t cb = 0;
+        for (const RPart &bp : Bp) {
+          const int bm = B.map_of(bp.v, false);
+          for (int64_t mt = 0; mt < ceil_div(ap.v.cols, kBM); ++mt)
+            for (int64_t nt = 0; nt < ceil_div(bp.v.cols, bn); ++nt)
+              B.emit(outS, ra + mt * kBM, cb + nt * bn, std::min<int64_t>(kBM, ap.v.cols - mt * kBM),
+                     std::min<int64_t>(bn, bp.v.cols - nt * bn),
+                     {Builder::seg(am, bm, false, false, mt * kBM, nt * bn, X.cd[k])}, {});
+          B.fl_s1 += 2.0 * ap.v.cols * static_cast<double>(bp.v.cols) * X.cd[k];
+          cb += bp.v.cols;
+        }
+        ra += ap.v.cols;
+      }
+    }
+    // k = j block with a dense tile of op(B): T_i[k-block, k-block] = V_ik^T D_kk
+    if (k >= j0 && k < j1 && k < Y.nr && Y.dt(k, k)) {
+      const bool ymn = Y.diag_trans;
+      const int bm = B.map_of(Y.diag[k], ymn);
+      int64_t ra = 0;
+      for (const RPart &ap : Ap) {
+        const int am = B.map_of(ap.v, false);
+        for (int64_t mt = 0; mt < ceil_div(ap.v.cols, kBM); ++mt)
+          for (int64_t nt = 0; nt < ceil_div(Y.cd[k], bn); ++nt) {
+            const int64_t rows = std::min<int64_t>(kBM, ap.v.cols - mt * kBM);
+            auto pc = pieces_for(ap, 0, mt * kBM, rows, [&](int i) { return trow(i, k); });
+            B.emit(outT, 0, L.colT[k - j0] + nt * bn, rows, std::min<int64_t>(bn, Y.cd[k] - nt * bn),
+                   {Builder::seg(am, bm, false, ymn, mt * kBM, nt * bn, Y.rd[k])}, pc);
+          }
+        B.fl_dense += 2.0 * ap.v.cols * static_cast<double>(Y.cd[k]) * Y.rd[k];
+        ra += ap.v.cols;
+      }
+    }
+  }
+  // P_i = D_ii W_{i,J}
+  if (!Y.dense)
+    for (int i = i0; i < i1; ++i) {
+      if (L.Poff[i] < 0) continue;
+      const uint64_t P = B.ws + static_cast<uint64_t>(L.Poff[i]);
+      const int outP = B.out_ws(P, X.rd[i]);
+      const bool amn = !X.diag_trans;
+      const int am = B.map_of(X.diag[i], amn);
+      std::vector<RPart> Bp = restrict_panel(Y.rowp[i], Y.rpos[i], j0, j1,
+                                             [&Y, i](int j) { return static_cast<int64_t>(Y.r(i, j)); }, es);
+      int64_t cb = 0;
+      for (const RPart &bp : Bp) {
+        const int bm = B.map_of(bp.v, false);
+        for (int64_t mt = 0; mt < ceil_div(X.rd[i], kBM); ++mt)
+          for (int64_t nt = 0; nt < ceil_div(bp.v.cols, bn); ++nt)
+            B.emit(outP, mt * kBM, cb + nt * bn, std::min<int64_t>(kBM, X.rd[i] - mt * kBM),
+                   std::min<int64_t>(bn, bp.v.cols - nt * bn),
+                   {Builder::seg(am, bm, amn, false, mt * kBM, nt * bn, X.cd[i])}, {});
+        B.fl_dense += 2.0 * X.rd[i] * static_cast<double>(bp.v.cols) * X.cd[i];
+        cb += bp.v.cols;
+      }
+    }
+
+  // ---------------- L2: Stage 2, T_i[k, j] = S_ikj Z_kj^T fused over i
+  B.tasks = &l2;
+  if (!Y.dense)
+    for (int k = 0; k < X.nc; ++k) {
+      if (L.Srows[k] == 0) continue;
+      std::vector<RPart> Ap = restrict_panel(X.colp[k], X.cpos[k], i0, i1, rank_col(k), es);
+      // the S_k row space is the concatenation of Ap
+      std::vector<int64_t> base;
+      int64_t acc = 0;
+      for (const RPart &ap : Ap) { base.push_back(acc); acc += ap.v.cols; }
+      const int64_t sig = L.Srows[k];
+      for (int j = j0; j < j1; ++j) {
+        if (Y.dt(k, j)) continue;                       // handled in L1
+        const int64_t r = Y.r(k, j);
+        int am = -1, bm = -1;
+        if (r > 0) {
+          const View sv{B.ws + static_cast<uint64_t>(L.Soff[k] + L.Scol[k][j - j0] * L.Sld[k] * es), sig, r, L.Sld[k]};
+          am = B.map_of(sv, true);
+          bm = B.map_of(Y.inner[static_cast<size_t>(k) * Y.nc + j], true);
+          B.fl_s2 += 2.0 * sig * static_cast<double>(Y.cd[j]) * r;
+        }
+        for (int64_t mt = 0; mt < ceil_div(sig, kBM); ++mt) {
+          const int64_t rows = std::min<int64_t>(kBM, sig - mt * kBM);
+          std::vector<Piece> pc;
+          for (size_t q = 0; q < Ap.size(); ++q) {
+            auto pp = pieces_for(Ap[q], base[q], mt * kBM, rows, [&](int i) { return trow(i, k); });
+            pc.insert(pc.end(), pp.begin(), pp.end());
+          }
+          for (int64_t nt = 0; nt < ceil_div(Y.cd[j], bn); ++nt) {
+            std::vector<Seg> sg;
+            if (r > 0) sg.push_back(Builder::seg(am, bm, true, true, mt * kBM, nt * bn, r));
+            B.emit(outT, 0, L.colT[j - j0] + nt * bn, rows, std::min<int64_t>(bn, Y.cd[j] - nt * bn), sg, pc);
+          }
+        }
+      }
+    }
+
+  // ---------------- L3: Stage 3, C[i, J] = alpha (U_i T_i + dense segment) + beta C
+  B.tasks = &l3;
+  const int outC = B.out_c();
+  for (int i = i0; i < i1; ++i) {
+    const auto &parts = X.rowp[i];
+    std::vector<int> am(parts.size()), bm(parts.size());
+    int64_t rho = 0;
+    for (size_t pi = 0; pi < parts.size(); ++pi) {
+      am[pi] = B.map_of(parts[pi].v, true);
+      const View tv{T + static_cast<uint64_t>(L.Toff[i][pi] * es), parts[pi].v.cols, L.WJ, L.Tld};
+      bm[pi] = B.map_of(tv, false);
+      rho += parts[pi].v.cols;
+    }
+    B.fl_s3 += 2.0 * X.rd[i] * static_cast<double>(L.WJ) * rho;
+    B.fl_final += 2.0 * X.rd[i] * static_cast<double>(L.WJ) * rho;
+    const bool xdiag = i < X.nc && X.dt(i, i);
+    int dm = -1;
+    const bool dmn = !X.diag_trans;
+    if (xdiag) dm = B.map_of(X.diag[i], dmn);
+    for (int j = j0; j < j1; ++j) {
+      // the dense-tile segment of this output block
+      int sm = -1, zm = -1;
+      bool smn = false, zmn = false;
+      int64_t klen = 0;
+      if (xdiag) {
+        if (Y.dense) {
+          View yi;
+          zmn = Y.dtrans;
+          if (!Y.dtrans) yi = View{Y.dv.addr + static_cast<uint64_t>((Y.ro[i] + Y.co[j] * Y.dv.ld) * es), Y.rd[i], Y.cd[j], Y.dv.ld};
+          else yi = View{Y.dv.addr + static_cast<uint64_t>((Y.co[j] + Y.ro[i] * Y.dv.ld) * es), Y.cd[j], Y.rd[i], Y.dv.ld};
+          sm = dm; smn = dmn; zm = B.map_of(yi, zmn); klen = X.cd[i];
+        } else if (j == i && Y.dt(i, i)) {
+          sm = dm; smn = dmn; zmn = Y.diag_trans; zm = B.map_of(Y.diag[i], zmn); klen = X.cd[i];
+        } else if (!Y.dt(i, j) && Y.r(i, j) > 0) {
+          const int64_t r = Y.r(i, j);
+          const View pv{B.ws + static_cast<uint64_t>(L.Poff[i] + L.Pcol[i][j - j0] * X.rd[i] * es), X.rd[i], r, X.rd[i]};
+          sm = B.map_of(pv, true); smn = true;
+          zm = B.map_of(Y.inner[static_cast<size_t>(i) * Y.nc + j], true); zmn = true;
+          klen = r;
+        }
+        if (klen > 0) B.fl_dense += 2.0 * X.rd[i] * static_cast<double>(Y.cd[j]) * klen;
+      }
+      for (int64_t nt = 0; nt < ceil_div(Y.cd[j], bn); ++nt)
+        for (int64_t mt = 0; mt < ceil_div(X.rd[i], kBM); ++mt) {
+          std::vector<Seg> sg;
+          for (size_t pi = 0; pi < parts.size(); ++pi)
+            if (parts[pi].v.cols > 0)
+              sg.push_back(Builder::seg(am[pi], bm[pi], true, false, mt * kBM, L.colT[j - j0] + nt * bn,
+                                        parts[pi].v.cols));
+          if (klen > 0) sg.push_back(Builder::seg(sm, zm, smn, zmn, mt * kBM, nt * bn, klen));
+          B.emit(outC, X.ro[i] + mt * kBM, Y.co[j] + nt * bn, std::min<int64_t>(kBM, X.rd[i] - mt * kBM),
+                 std::min<int64_t>(bn, Y.cd[j] - nt * bn), sg, {});
+        }
+    }
+  }
+  (void)segs;
+  (void)pieces;
+}
+
+// Sort a launch's tasks by decreasing K so the persistent CTAs finish together.
+void sort_by_work(std::vector<Task> &v, const std::vector<Seg> &segs) {
+  std::stable_sort(v.begin(), v.end(), [&](const Task &a, const Task &b) {
+    int64_t ka = 0, kb = 0;
+    for (int s = 0; s < a.nseg; ++s) ka += segs[a.seg0 + s].k_len;
+    for (int s = 0; s < b.nseg; ++s) kb += segs[b.seg0 + s].k_len;
+    return ka > kb;
+  });
+}
+
+int device_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ handle / plan
+struct tlr_handle_s {
+  cudaStream_t stream = nullptr;
+  unsigned int *d_err = nullptr;
+  bool timing = false;
+  std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> ev_used;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev_free;
+  double ms[kNumKinds] = {0, 0, 0, 0, 0};
+  int64_t count[kNumKinds] = {0, 0, 0, 0, 0};
+  unsigned long long wait_limit_ns = 2000000000ull;
+};
+
+struct tlr_plan_s {
+  tlr_handle_t h = nullptr;
+  bool tf32 = false;
+  int bn = 256;
+  int64_t Cm = 0, Cn = 0;                 // dimensions of C
+  void *d_tables = nullptr;
+  const void *d_maps = nullptr;
+  const Task *d_tasks = nullptr;
+  const Seg *d_segs = nullptr;
+  const Piece *d_pieces = nullptr;
+  const Out *d_outs = nullptr;
+  std::vector<Launch> launches;
+  std::vector<const float *> round_src;
+  std::vector<float *> round_dst;
+  std::vector<int64_t> round_n;
+  tlr_plan_info_t info{};
+};
+
+namespace {
+
+struct ProblemViews {
+  Operand A, B;
+  bool dense_left = false, dense_right = false;
+  int dtype = TLR_F32;
+  int64_t Cm = 0, Cn = 0, K = 0;
+  int64_t pseudo_b = 0;
+};
+
+tlr_status_t prepare(tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A, const tlr_operand_t *B,
+                     ProblemViews &pv, bool check_pointers) {
+  if (!A || !B) return TLR_STATUS_INVALID_ARG;
+  if ((opA != TLR_OP_N && opA != TLR_OP_T) || (opB != TLR_OP_N && opB != TLR_OP_T)) return TLR_STATUS_INVALID_ARG;
+  tlr_status_t st = describe(*A, pv.A, check_pointers);
+  if (st) return st;
+  st = describe(*B, pv.B, check_pointers);
+  if (st) return st;
+  if (A->dtype != B->dtype) return TLR_STATUS_UNSUPPORTED;
+  pv.dtype = A->dtype;
+  pv.dense_left = A->kind == TLR_KIND_DENSE;
+  pv.dense_right = B->kind == TLR_KIND_DENSE;
+  if (pv.dense_left && pv.dense_right) return TLR_STATUS_UNSUPPORTED;
+  pv.Cm = opA == TLR_OP_T ? A->cols : A->rows;
+  pv.K = opA == TLR_OP_T ? A->rows : A->cols;
+  const int64_t Kb = opB == TLR_OP_T ? B->cols : B->rows;
+  pv.Cn = opB == TLR_OP_T ? B->rows : B->cols;
+  if (pv.K != Kb) return TLR_STATUS_INVALID_ARG;
+  // contraction tiles must line up
+  const tlr_operand_t *T = pv.dense_left ? B : A;
+  pv.pseudo_b = T->b;
+  if (!pv.dense_left && !pv.dense_right && A->b != B->b) return TLR_STATUS_UNSUPPORTED;
+  return TLR_STATUS_OK;
+}
+
+// Base addresses used by the kernels (originals, or tf32-rounded copies in the workspace).
+struct Bases { uint64_t a[8]; };
+
+void collect_round(const Operand &o, bool tf32, uint64_t ws, int64_t &off, std::vector<const float *> &src,
+                   std::vector<float *> &dst, std::vector<int64_t> &cnt, Bases &out) {
+  const tlr_operand_t &d = o.d;
+  const void *ptrs[8] = {d.U, d.V, d.D, d.bu_U, d.bu_V, d.bv_U, d.bv_V, d.gamma};
+  const int64_t n[8] = {o.u_elems, o.v_elems, o.d_elems, o.buU, o.buV, o.bvU, o.bvV, o.g_elems};
+  if (d.kind == TLR_KIND_DENSE) {
+    const int64_t ne = d.ld * d.cols;
+    if (tf32) {
+      out.a[0] = ws ? ws + static_cast<uint64_t>(off) : 0;
+      if (ws) { src.push_back(static_cast<const float *>(d.data)); dst.push_back(reinterpret_cast<float *>(out.a[0])); cnt.push_back(ne); }
+      off = align_up(off + ne * 4, 256);
+    } else {
+      out.a[0] = reinterpret_cast<uint64_t>(d.data);
+    }
+    return;
+  }
+  for (int b = 0; b < 8; ++b) {
+    if (!tf32 || n[b] == 0 || !ptrs[b]) { out.a[b] = reinterpret_cast<uint64_t>(ptrs[b]); continue; }
+    out.a[b] = ws ? ws + static_cast<uint64_t>(off) : 0;
+    if (ws) { src.push_back(static_cast<const float *>(ptrs[b])); dst.push_back(reinterpret_cast<float *>(out.a[b])); cnt.push_back(n[b]); }
+    off = align_up(off + n[b] * 4, 256);
+  }
+}
+
+struct PlanCore {
+  ProblemViews pv;
+  LOp XR, YR;     // right order:  op(A) * op(B)
+  LOp XL, YL;     // left order:   op(B)^T * op(A)^T  (transposed output)
+  bool can_right = true, can_left = true;
+  int64_t fixed = 0;   // workspace taken by rounded input copies
+  int nI = 0, nJ = 0;  // tile grid of C
+  std::vector<int64_t> Crd, Ccd;
+};
+
+void bind_operand(Operand &o, const Bases &b) {
+  if (o.d.kind == TLR_KIND_DENSE) { o.d.data = reinterpret_cast<const void *>(b.a[0]); return; }
+  bind(o, b.a[0], b.a[1], b.a[2], b.a[3], b.a[4], b.a[5], b.a[6], b.a[7]);
+}
+
+tlr_status_t core_init(PlanCore &pc, tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A,
+                       const tlr_operand_t *B, bool check_pointers, uint64_t ws,
+                       std::vector<const float *> *rsrc, std::vector<float *> *rdst, std::vector<int64_t> *rn) {
+  tlr_status_t st = prepare(opA, opB, A, B, pc.pv, check_pointers);
+  if (st) return st;
+  const bool tf32 = pc.pv.dtype == TLR_F32;
+  std::vector<const float *> s;
+  std::vector<float *> d;
+  std::vector<int64_t> n;
+  Bases ba{}, bb{};
+  int64_t off = 0;
+  collect_round(pc.pv.A, tf32, ws, off, s, d, n, ba);
+  collect_round(pc.pv.B, tf32, ws, off, s, d, n, bb);
+  pc.fixed = off;
+  if (rsrc) { *rsrc = s; *rdst = d; *rn = n; }
+  bind_operand(pc.pv.A, ba);
+  bind_operand(pc.pv.B, bb);
+  const bool tA = opA == TLR_OP_T, tB = opB == TLR_OP_T;
+  const int64_t pb = pc.pv.pseudo_b;
+  pc.can_right = !pc.pv.dense_left;
+  pc.can_left = !pc.pv.dense_right;
+  if (pc.can_right) { pc.XR = logical(pc.pv.A, tA, pb); pc.YR = logical(pc.pv.B, tB, pb); }
+  if (pc.can_left) { pc.XL = logical(pc.pv.B, !tB, pb); pc.YL = logical(pc.pv.A, !tA, pb); }
+  const LOp &X = pc.can_right ? pc.XR : pc.YL;   // op(A) geometry
+  const LOp &Y = pc.can_right ? pc.YR : pc.XL;   // op(B)^T geometry when left-only
+  if (pc.can_right) { pc.Crd = pc.XR.rd; pc.Ccd = pc.YR.cd; }
+  else { pc.Crd = pc.YL.cd; pc.Ccd = pc.XL.rd; }
+  (void)X; (void)Y;
+  pc.nI = static_cast<int>(pc.Crd.size());
+  pc.nJ = static_cast<int>(pc.Ccd.size());
+  return TLR_STATUS_OK;
+}
+
+// Workspace bytes of rectangle (rows [i0,i1), cols [j0,j1) of C) under an order.
+int64_t rect_bytes(const PlanCore &pc, int i0, int i1, int j0, int j1, bool left, int es) {
+  if (!left) return layout_rect(pc.XR, pc.YR, i0, i1, j0, j1, es).bytes;
+  return layout_rect(pc.XL, pc.YL, j0, j1, i0, i1, es).bytes;
+}
+
+double rect_cost(const PlanCore &pc, int i0, int i1, int j0, int j1, bool left) {
+  if (!left) {
+    int64_t W = 0;
+    for (int j = j0; j < j1; ++j) W += pc.Ccd[j];
+    return final_cost(pc.XR, i0, i1, W);
+  }
+  int64_t H = 0;
+  for (int i = i0; i < i1; ++i) H += pc.Crd[i];
+  return final_cost(pc.XL, j0, j1, H);
+}
+
+// Order for a rectangle: cheaper feasible one (tie: right); -1 if none fits.
+int choose(const PlanCore &pc, int i0, int i1, int j0, int j1, int64_t arena, tlr_order_t force, int es) {
+  const bool r_ok = pc.can_right && force != TLR_ORDER_LEFT && rect_bytes(pc, i0, i1, j0, j1, false, es) <= arena;
+  const bool l_ok = pc.can_left && force != TLR_ORDER_RIGHT && rect_bytes(pc, i0, i1, j0, j1, true, es) <= arena;
+  if (r_ok && l_ok) return rect_cost(pc, i0, i1, j0, j1, true) < rect_cost(pc, i0, i1, j0, j1, false) ? 1 : 0;
+  if (r_ok) return 0;
+  if (l_ok) return 1;
+  return -1;
+}
+
+// Rectangles for a budget: widest feasible block of tile columns, then the
+// longest runs of tile rows that fit.
+bool split(const PlanCore &pc, int64_t budget, tlr_order_t force, int es, std::vector<Rect> &rects) {
+  rects.clear();
+  const int64_t arena = budget - pc.fixed;
+  if (arena < 0) return false;
+  int w = pc.nJ;
+  for (; w >= 1; --w) {
+    bool ok = true;
+    for (int j0 = 0; ok && j0 < pc.nJ; j0 += w)
+      for (int i = 0; ok && i < pc.nI; ++i)
+        if (choose(pc, i, i + 1, j0, std::min(pc.nJ, j0 + w), arena, force, es) < 0) ok = false;
+    if (ok) break;
+  }
+  if (w < 1) return false;
+  for (int j0 = 0; j0 < pc.nJ; j0 += w) {
+    const int j1 = std::min(pc.nJ, j0 + w);
+    int i0 = 0;
+    while (i0 < pc.nI) {
+      int i1 = i0 + 1;
+      while (i1 < pc.nI && choose(pc, i0, i1 + 1, j0, j1, arena, force, es) >= 0) ++i1;
+      const int o = choose(pc, i0, i1, j0, j1, arena, force, es);
+      rects.push_back(Rect{i0, i1, j0, j1, o == 1});
+      i0 = i1;
+    }
+  }
+  return true;
+}
+
+int64_t max_rect_bytes(const PlanCore &pc, const std::vector<Rect> &rects, int es) {
+  int64_t m = 0;
+  for (const Rect &r : rects) m = std::max(m, rect_bytes(pc, r.i0, r.i1, r.j0, r.j1, r.left, es));
+  return m;
+}
+
+// Output tile width: the smallest multiple of 64 covering a tile of C, at most 256.
+int choose_bn(const PlanCore &pc) {
+  int64_t bmax = 0;
+  for (int64_t x : pc.Ccd) bmax = std::max(bmax, x);
+  for (int64_t x : pc.Crd) bmax = std::max(bmax, x);
+  return static_cast<int>(std::min<int64_t>(kMaxBN, align_up(std::max<int64_t>(bmax, 64), 64)));
+}
+
+struct Tables {
+  int bn = 256;
+  std::vector<CUtensorMap> maps;
+  std::map<std::tuple<uint64_t, int64_t, int64_t, int64_t, int>, int> map_index;
+  std::vector<Task> all;
+  std::vector<Seg> segs;
+  std::vector<Piece> pieces;
+  std::vector<Out> outs;
+  std::vector<Launch> launches;
+  std::vector<std::pair<View, int>> views;
+  std::vector<int> task_rect;               // rectangle of each task
+  std::vector<RectLayout> layouts;          // per rectangle (in the order it was built)
+  std::vector<uint8_t> rect_left;
+  tlr_plan_info_t info{};
+};
+
+tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, uint64_t ws, bool dry, Tables &tb) {
+  const int es = elem_size(pc.pv.dtype);
+  const bool tf32 = pc.pv.dtype == TLR_F32;
+  const uint64_t arena = ws + static_cast<uint64_t>(pc.fixed);
+  tlr_plan_info_t &info = tb.info;
+  memset(&info, 0, sizeof info);
+  for (size_t ri = 0; ri < rects.size(); ++ri) {
+    const Rect &r = rects[ri];
+    const LOp &X = r.left ? pc.XL : pc.XR;
+    const LOp &Y = r.left ? pc.YL : pc.YR;
+    const int i0 = r.left ? r.j0 : r.i0, i1 = r.left ? r.j1 : r.i1;
+    const int j0 = r.left ? r.i0 : r.j0, j1 = r.left ? r.i1 : r.j1;
+    RectLayout L = layout_rect(X, Y, i0, i1, j0, j1, es);
+    Builder B{X, Y, es, tf32, tb.bn, r.left, arena, &tb.maps, &tb.map_index, nullptr, &tb.segs, &tb.pieces, &tb.outs};
+    B.dry = dry;
+    B.views = &tb.views;
+    std::vector<Task> l1, l2, l3;
+    build_rect(B, L, l1, l2, l3, tb.segs, tb.pieces);
+    if (B.status) return B.status;
+    sort_by_work(l1, tb.segs);
+    sort_by_work(l2, tb.segs);
+    const std::vector<Task> *lists[3] = {&l1, &l2, &l3};
+    const int kinds[3] = {kKindStage1, kKindStage2, kKindStage3};
+    for (int q = 0; q < 3; ++q) {
+      if (lists[q]->empty()) continue;
+      const int64_t t0 = static_cast<int64_t>(tb.all.size());
+      tb.all.insert(tb.all.end(), lists[q]->begin(), lists[q]->end());
+      tb.task_rect.insert(tb.task_rect.end(), lists[q]->size(), static_cast<int>(ri));
+      tb.launches.push_back(Launch{kinds[q], t0, static_cast<int64_t>(tb.all.size())});
+    }
+    tb.layouts.push_back(L);
+    tb.rect_left.push_back(r.left ? 1 : 0);
+    info.runs += 1;
+    if (r.left) info.runs_left += 1; else info.runs_right += 1;
+    info.flops_stage1 += B.fl_s1;
+    info.flops_stage2 += B.fl_s2;
+    info.flops_stage3 += B.fl_s3;
+    info.flops_dense_terms += B.fl_dense;
+    if (pc.can_right) info.flops_right_final += rect_cost(pc, r.i0, r.i1, r.j0, r.j1, false);
+    if (pc.can_left) info.flops_left_final += rect_cost(pc, r.i0, r.i1, r.j0, r.j1, true);
+  }
+  info.flops_executed = info.flops_stage1 + info.flops_stage2 + info.flops_stage3 + info.flops_dense_terms;
+  info.tasks = static_cast<int64_t>(tb.all.size());
+  return TLR_STATUS_OK;
+}
+
+// ------------------------------------------------------------------ table validation
+// Host-side proof that a plan's launches stay inside their buffers: every
+// tensor-map view lies in one input buffer or the workspace, every segment's K
+// range fits its views, every task writes inside its output, the tiles of C are
+// covered exactly once, and in each rectangle the T rows Stage 3 reads are
+// written exactly once by the earlier launches.
+struct Region { uint64_t base; int64_t bytes; };
+
+bool inside(const std::vector<Region> &regs, uint64_t a, int64_t n) {
+  for (const Region &r : regs)
+    if (a >= r.base && a + static_cast<uint64_t>(n) <= r.base + static_cast<uint64_t>(r.bytes)) return true;
+  return false;
+}
+
+std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, int64_t ws_bytes) {
+  const int es = elem_size(pc.pv.dtype);
+  std::vector<Region> regs;
+  regs.push_back(Region{ws, ws_bytes});
+  for (const Operand *o : {&pc.pv.A, &pc.pv.B}) {
+    if (o->d.kind == TLR_KIND_DENSE) { regs.push_back(Region{reinterpret_cast<uint64_t>(o->d.data), o->d.ld * o->d.cols * es}); continue; }
+    const Stored &s = o->s;
+    for (size_t t = 0; t < s.outer.size(); ++t) {
+      if (s.outer[t].cols > 0) regs.push_back(Region{s.outer[t].addr, s.outer[t].ld * s.outer[t].cols * es});
+      if (s.inner[t].cols > 0) regs.push_back(Region{s.inner[t].addr, s.inner[t].ld * s.inner[t].cols * es});
+    }
+    for (const Part &p : std::vector<Part>()) (void)p;
+    for (const auto &P : s.rowp) for (const Part &p : P) regs.push_back(Region{p.v.addr, p.v.ld * p.v.cols * es});
+    for (const auto &P : s.colp) for (const Part &p : P) regs.push_back(Region{p.v.addr, p.v.ld * p.v.cols * es});
+    for (const View &v : s.diag) if (v.rows > 0) regs.push_back(Region{v.addr, v.ld * v.cols * es});
+  }
+  char buf[256];
+  for (size_t m = 0; m < tb.views.size(); ++m) {
+    const View &v = tb.views[m].first;
+    if (v.rows <= 0 || v.cols <= 0 || v.ld < v.rows || (v.ld * es) % 16 || (v.addr & 15u)) {
+      snprintf(buf, sizeof buf, "map %zu: bad view rows=%lld cols=%lld ld=%lld", m, (long long)v.rows, (long long)v.cols, (long long)v.ld);
+      return buf;
+    }
+    const int64_t span = ((v.cols - 1) * v.ld + v.rows) * es;
+    if (!inside(regs, v.addr, span)) { snprintf(buf, sizeof buf, "map %zu: view outside every buffer", m); return buf; }
+  }
+  const int64_t Cm = pc.pv.Cm, Cn = pc.pv.Cn;
+  std::set<std::pair<int64_t, int64_t>> ctiles;
+  double carea = 0;
+  for (size_t ti = 0; ti < tb.all.size(); ++ti) {
+    const Task &t = tb.all[ti];
+    if (t.rows < 1 || t.rows > kBM || t.cols < 1 || t.cols > tb.bn) { snprintf(buf, sizeof buf, "task %zu: bad extent", ti); return buf; }
+    for (int q = 0; q < t.nseg; ++q) {
+      const Seg &g = tb.segs[t.seg0 + q];
+      if (g.k_len <= 0 || g.a_map < 0 || g.b_map < 0 || g.a_map >= (int)tb.views.size() || g.b_map >= (int)tb.views.size()) {
+        snprintf(buf, sizeof buf, "task %zu seg %d: bad map or K", ti, q); return buf;
+      }
+      const bool amn = g.flags & kSegAMN, bmn = g.flags & kSegBMN;
+      if (tb.views[g.a_map].second != (amn ? 1 : 0) || tb.views[g.b_map].second != (bmn ? 1 : 0)) {
+        snprintf(buf, sizeof buf, "task %zu seg %d: majorness differs from the map's box", ti, q); return buf;
+      }
+      const View &va = tb.views[g.a_map].first, &vb = tb.views[g.b_map].first;
+      const int64_t aK = amn ? va.cols : va.rows, aMN = amn ? va.rows : va.cols;
+      const int64_t bK = bmn ? vb.cols : vb.rows, bMN = bmn ? vb.rows : vb.cols;
+      const int64_t a0 = amn ? g.a_x : g.a_y, b0 = bmn ? g.b_x : g.b_y;
+      const int64_t ak = amn ? g.a_y : g.a_x, bk = bmn ? g.b_y : g.b_x;
+      if (ak != 0 || bk != 0 || g.k_len > aK || g.k_len > bK) { snprintf(buf, sizeof buf, "task %zu seg %d: K range", ti, q); return buf; }
+      if (a0 < 0 || a0 >= aMN || b0 < 0 || b0 >= bMN) { snprintf(buf, sizeof buf, "task %zu seg %d: tile outside its operand", ti, q); return buf; }
+      if (((amn ? g.a_x : g.a_x) * es) % 16 || ((bmn ? g.b_x : g.b_x) * es) % 16) { snprintf(buf, sizeof buf, "task %zu seg %d: TMA x not 16-byte aligned", ti, q); return buf; }
+    }
+    const Out &o = tb.outs[t.out];
+    if (o.kind == kOutC) {
+      const int64_t R = o.trans ? Cn : Cm, Cc = o.trans ? Cm : Cn;
+      if (t.npiece || t.row0 < 0 || t.col0 < 0 || t.row0 + t.rows > R || t.col0 + t.cols > Cc) {
+        snprintf(buf, sizeof buf, "task %zu: C tile outside C", ti); return buf;
+      }
+      if (!ctiles.insert({o.trans ? t.col0 : t.row0, o.trans ? t.row0 : t.col0}).second) {
+        snprintf(buf, sizeof buf, "task %zu: C tile written twice", ti); return buf;
+      }
+      carea += static_cast<double>(t.rows) * t.cols;
+    } else {
+      const uint64_t base = reinterpret_cast<uint64_t>(o.ptr);
+      int64_t rmin = INT64_MAX, rmax = -1;
+      if (t.npiece == 0) { rmin = t.row0; rmax = t.row0 + t.rows - 1; }
+      for (int q = 0; q < t.npiece; ++q) {
+        const Piece &pe = tb.pieces[t.piece0 + q];
+        if (pe.src0 < 0 || pe.len <= 0 || pe.src0 + pe.len > t.rows) { snprintf(buf, sizeof buf, "task %zu: bad piece", ti); return buf; }
+        rmin = std::min<int64_t>(rmin, pe.dst0);
+        rmax = std::max<int64_t>(rmax, pe.dst0 + pe.len - 1);
+      }
+      if (rmin < 0 || rmax >= o.ld) { snprintf(buf, sizeof buf, "task %zu: row beyond the leading dimension", ti); return buf; }
+      const uint64_t lo = base + static_cast<uint64_t>((rmin + t.col0 * o.ld) * es);
+      const uint64_t hi = base + static_cast<uint64_t>((rmax + (t.col0 + t.cols - 1) * o.ld + 1) * es);
+      if (lo < ws + static_cast<uint64_t>(pc.fixed) || hi > ws + static_cast<uint64_t>(ws_bytes)) {
+        snprintf(buf, sizeof buf, "task %zu: workspace write outside the arena", ti); return buf;
+      }
+    }
+  }
+  if (carea != static_cast<double>(Cm) * static_cast<double>(Cn)) return "tiles of C do not cover C exactly";
+  // T coverage per rectangle
+  for (size_t ri = 0; ri < tb.layouts.size(); ++ri) {
+    const RectLayout &L = tb.layouts[ri];
+    const bool left = tb.rect_left[ri] != 0;
+    const LOp &X = left ? pc.XL : pc.XR;
+    const uint64_t T = ws + static_cast<uint64_t>(pc.fixed + L.Toffset);
+    // column interval -> written row intervals
+    std::map<std::pair<int64_t, int64_t>, std::vector<std::pair<int64_t, int64_t>>> wr;
+    for (size_t ti = 0; ti < tb.all.size(); ++ti) {
+      if (tb.task_rect[ti] != static_cast<int>(ri)) continue;
+      const Task &t = tb.all[ti];
+      const Out &o = tb.outs[t.out];
+      if (o.kind == kOutC || reinterpret_cast<uint64_t>(o.ptr) != T) continue;
+      auto &rows = wr[{t.col0, t.col0 + t.cols}];
+      if (t.npiece == 0) rows.push_back({t.row0, t.row0 + t.rows});
+      for (int q = 0; q < t.npiece; ++q) {
+        const Piece &pe = tb.pieces[t.piece0 + q];
+        rows.push_back({pe.dst0, pe.dst0 + pe.len});
+      }
+    }
+    std::vector<std::pair<int64_t, int64_t>> need;
+    for (int i = L.i0; i < L.i1; ++i)
+      for (size_t pi = 0; pi < X.rowp[i].size(); ++pi)
+        if (X.rowp[i][pi].v.cols > 0) need.push_back({L.Toff[i][pi], L.Toff[i][pi] + X.rowp[i][pi].v.cols});
+    std::sort(need.begin(), need.end());
+    if (need.empty()) continue;
+    int64_t c = 0;
+    for (auto &kv : wr) {
+      if (kv.first.first != c) { snprintf(buf, sizeof buf, "rect %zu: T columns not tiled at %lld", ri, (long long)c); return buf; }
+      c = kv.first.second;
+      auto rows = kv.second;
+      std::sort(rows.begin(), rows.end());
+      if (rows != need) {
+        // merge adjacent written intervals before comparing
+        std::vector<std::pair<int64_t, int64_t>> m;
+        for (auto &x : rows) {
+          if (!m.empty() && m.back().second > x.first) { snprintf(buf, sizeof buf, "rect %zu: T rows written twice", ri); return buf; }
+          if (!m.empty() && m.back().second == x.first) m.back().second = x.second; else m.push_back(x);
+        }
+        std::vector<std::pair<int64_t, int64_t>> n2;
+        for (auto &x : need) {
+          if (!n2.empty() && n2.back().second == x.first) n2.back().second = x.second; else n2.push_back(x);
+        }
+        if (m != n2) { snprintf(buf, sizeof buf, "rect %zu: T rows read by Stage 3 not written exactly once", ri); return buf; }
+      }
+    }
+    if (c != L.WJ) { snprintf(buf, sizeof buf, "rect %zu: T columns end at %lld of %lld", ri, (long long)c, (long long)L.WJ); return buf; }
+  }
+  return std::string();
+}
+
+cudaError_t record_start(tlr_handle_t h, int kind, std::pair<cudaEvent_t, cudaEvent_t> &ev) {
+  if (!h->timing) return cudaSuccess;
+  if (h->ev_free.empty()) {
+    cudaEvent_t a, b;
+    if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) return cudaErrorUnknown;
+    h->ev_free.push_back({a, b});
+  }
+  ev = h->ev_free.back();
+  h->ev_free.pop_back();
+  h->ev_used.push_back({kind, ev});
+  return cudaEventRecord(ev.first, h->stream);
+}
+
+cudaError_t record_stop(tlr_handle_t h, const std::pair<cudaEvent_t, cudaEvent_t> &ev) {
+  if (!h->timing) return cudaSuccess;
+  return cudaEventRecord(ev.second, h->stream);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ exported ABI
+extern "C" {
+
+const char *tlr_status_string(tlr_status_t s) {
+  switch (s) {
+    case TLR_STATUS_OK: return "TLR_STATUS_OK";
+    case TLR_STATUS_INVALID_ARG: return "TLR_STATUS_INVALID_ARG";
+    case TLR_STATUS_ALIGNMENT: return "TLR_STATUS_ALIGNMENT";
+    case TLR_STATUS_WORKSPACE_TOO_SMALL: return "TLR_STATUS_WORKSPACE_TOO_SMALL";
+    case TLR_STATUS_UNSUPPORTED: return "TLR_STATUS_UNSUPPORTED";
+    case TLR_STATUS_CUDA_ERROR: return "TLR_STATUS_CUDA_ERROR";
+    case TLR_STATUS_TIMEOUT: return "TLR_STATUS_TIMEOUT";
+    case TLR_STATUS_NOT_INITIALIZED: return "TLR_STATUS_NOT_INITIALIZED";
+  }
+  return "TLR_STATUS_UNKNOWN";
+}
+
+tlr_status_t tlr_create(tlr_handle_t *handle, void *stream) {
+  if (!handle) return TLR_STATUS_INVALID_ARG;
+  *handle = nullptr;
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || n == 0) { cudaGetLastError(); return TLR_STATUS_NOT_INITIALIZED; }
+  tlr_handle_s *h = new (std::nothrow) tlr_handle_s();
+  if (!h) return TLR_STATUS_INVALID_ARG;
+  h->stream = static_cast<cudaStream_t>(stream);
+  if (cudaMalloc(&h->d_err, 256) != cudaSuccess || cudaMemset(h->d_err, 0, 256) != cudaSuccess) {
+    delete h;
+    return TLR_STATUS_CUDA_ERROR;
+  }
+  *handle = h;
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_destroy(tlr_handle_t h) {
+  if (!h) return TLR_STATUS_INVALID_ARG;
+  cudaStreamSynchronize(h->stream);
+  for (auto &e : h->ev_free) { cudaEventDestroy(e.first); cudaEventDestroy(e.second); }
+  for (auto &e : h->ev_used) { cudaEventDestroy(e.second.first); cudaEventDestroy(e.second.second); }
+  cudaFree(h->d_err);
+  delete h;
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_set_stream(tlr_handle_t h, void *stream) {
+  if (!h) return TLR_STATUS_INVALID_ARG;
+  h->stream = static_cast<cudaStream_t>(stream);
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_analyze(tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A, const tlr_operand_t *B,
+                         tlr_analysis_t *out) {
+  if (!out || !A || !B) return TLR_STATUS_INVALID_ARG;
+  if (A->kind != TLR_KIND_TLR || B->kind != TLR_KIND_TLR) return TLR_STATUS_UNSUPPORTED;
+  PlanCore pc;
+  tlr_status_t st = core_init(pc, opA, opB, A, B, false, 0, nullptr, nullptr, nullptr);
+  if (st) return st;
+  const LOp &X = pc.XR, &Y = pc.YR;
+  out->nt_i = X.nr; out->nt_k = X.nc; out->nt_j = Y.nc;
+  int64_t W = 0, H = 0;
+  for (int j = 0; j < Y.nc; ++j) W += Y.cd[j];
+  for (int i = 0; i < X.nr; ++i) H += X.rd[i];
+  int64_t sr = 0, sg = 0;
+  for (int i = 0; i < X.nr; ++i) {
+    int64_t rho = 0;
+    for (int k = 0; k < X.nc; ++k) if (!X.dt(i, k)) rho += X.r(i, k);
+    if (out->rho) out->rho[i] = rho;
+    if (out->stage3_mnk) { out->stage3_mnk[3 * i] = X.rd[i]; out->stage3_mnk[3 * i + 1] = W; out->stage3_mnk[3 * i + 2] = rho; }
+    sr += rho;
+  }
+  for (int j = 0; j < Y.nc; ++j) {
+    int64_t g = 0;
+    for (int k = 0; k < Y.nr; ++k) if (!Y.dt(k, j)) g += Y.r(k, j);
+    if (out->gamma) out->gamma[j] = g;
+    sg += g;
+  }
+  for (int k = 0; k < X.nc; ++k) {
+    int64_t s = 0, G = 0;
+    for (int i = 0; i < X.nr; ++i) if (!X.dt(i, k)) s += X.r(i, k);
+    for (int j = 0; j < Y.nc; ++j) if (!Y.dt(k, j)) G += Y.r(k, j);
+    if (out->sigma) out->sigma[k] = s;
+    if (out->Gamma) out->Gamma[k] = G;
+    if (out->stage1_mnk) { out->stage1_mnk[3 * k] = s; out->stage1_mnk[3 * k + 1] = G; out->stage1_mnk[3 * k + 2] = X.cd[k]; }
+  }
+  out->F_R = final_cost(X, 0, X.nr, W);
+  out->F_L = final_cost(pc.XL, 0, pc.XL.nr, H);
+  out->order = out->F_L < out->F_R ? TLR_ORDER_LEFT : TLR_ORDER_RIGHT;
+  out->T_right_rows = sr; out->T_right_cols = W;
+  out->T_left_rows = H; out->T_left_cols = sg;
+  int64_t prods = 0;
+  std::set<std::pair<int32_t, int32_t>> shapes;
+  for (int i = 0; i < X.nr; ++i)
+    for (int k = 0; k < X.nc; ++k)
+      for (int j = 0; j < Y.nc; ++j) {
+        if (X.dt(i, k) || Y.dt(k, j)) continue;
+        if (X.r(i, k) <= 0 || Y.r(k, j) <= 0) continue;
+        ++prods;
+        shapes.insert({X.r(i, k), Y.r(k, j)});
+      }
+  out->coupling_products = prods;
+  out->distinct_shapes = static_cast<int64_t>(shapes.size());
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_gemm_workspace_bytes(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A,
+                                      const tlr_operand_t *B, int runs, size_t *bytes) {
+  (void)h;
+  if (!bytes) return TLR_STATUS_INVALID_ARG;
+  PlanCore pc;
+  tlr_status_t st = core_init(pc, opA, opB, A, B, false, 0, nullptr, nullptr, nullptr);
+  if (st) return st;
+  const int es = elem_size(pc.pv.dtype);
+  if (runs <= 0) runs = 1;
+  std::vector<Rect> rects;
+  int64_t whole = INT64_MAX / 4;
+  if (pc.can_right) whole = std::min(whole, rect_bytes(pc, 0, pc.nI, 0, pc.nJ, false, es));
+  if (pc.can_left) whole = std::min(whole, rect_bytes(pc, 0, pc.nI, 0, pc.nJ, true, es));
+  int64_t hi = pc.fixed + whole;
+  if (!split(pc, hi, TLR_ORDER_AUTO, es, rects)) return TLR_STATUS_INVALID_ARG;
+  int64_t lo = pc.fixed;
+  // smallest budget whose split has at most `runs` rectangles
+  while (lo < hi) {
+    const int64_t mid = lo + (hi - lo) / 2;
+    if (split(pc, mid, TLR_ORDER_AUTO, es, rects) && static_cast<int>(rects.size()) <= runs) hi = mid;
+    else lo = mid + 1;
+  }
+  split(pc, hi, TLR_ORDER_AUTO, es, rects);
+  *bytes = static_cast<size_t>(pc.fixed + max_rect_bytes(pc, rects, es));
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A,
+                             const tlr_operand_t *B, void *workspace, size_t workspace_bytes,
+                             tlr_order_t order, tlr_plan_t *plan_out) {
+  if (!h || !plan_out) return TLR_STATUS_INVALID_ARG;
+  *plan_out = nullptr;
+  if (order != TLR_ORDER_AUTO && order != TLR_ORDER_RIGHT && order != TLR_ORDER_LEFT) return TLR_STATUS_INVALID_ARG;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TLR_STATUS_ALIGNMENT;
+  const uint64_t ws = reinterpret_cast<uint64_t>(workspace);
+  PlanCore pc;
+  std::vector<const float *> rs;
+  std::vector<float *> rd;
+  std::vector<int64_t> rn;
+  tlr_status_t st = core_init(pc, opA, opB, A, B, true, ws ? ws : 1, &rs, &rd, &rn);
+  if (st) return st;
+  const int es = elem_size(pc.pv.dtype);
+  const bool tf32 = pc.pv.dtype == TLR_F32;
+  std::vector<Rect> rects;
+  if (!split(pc, static_cast<int64_t>(workspace_bytes), order, es, rects)) return TLR_STATUS_WORKSPACE_TOO_SMALL;
+  const int64_t need = pc.fixed + max_rect_bytes(pc, rects, es);
+  if (need > 0 && !workspace) return TLR_STATUS_INVALID_ARG;
+
+  tlr_plan_s *p = new (std::nothrow) tlr_plan_s();
+  if (!p) return TLR_STATUS_INVALID_ARG;
+  p->h = h;
+  p->tf32 = tf32;
+  p->Cm = pc.pv.Cm;
+  p->Cn = pc.pv.Cn;
+  p->round_src = rs;
+  p->round_dst = rd;
+  p->round_n = rn;
+  p->bn = choose_bn(pc);
+
+  Tables tb;
+  tb.bn = p->bn;
+  st = build_tables(pc, rects, ws, false, tb);
+  if (st) { delete p; return st; }
+  p->launches = tb.launches;
+  p->info = tb.info;
+  tlr_plan_info_t &info = p->info;
+  info.workspace_bytes = static_cast<size_t>(need);
+  info.launches = static_cast<int64_t>(p->launches.size()) + (p->round_n.empty() ? 0 : 1);
+  if (static_cast<size_t>(need) > workspace_bytes) { delete p; return TLR_STATUS_WORKSPACE_TOO_SMALL; }
+  std::vector<CUtensorMap> &maps = tb.maps;
+  std::vector<Task> &all = tb.all;
+  std::vector<Seg> &segs = tb.segs;
+  std::vector<Piece> &pieces = tb.pieces;
+  std::vector<Out> &outs = tb.outs;
+
+  // one device allocation for all tables: maps first (64-byte aligned)
+  const size_t szm = maps.size() * sizeof(CUtensorMap);
+  const size_t szt = align_up(static_cast<int64_t>(all.size() * sizeof(Task)), 256);
+  const size_t szs = align_up(static_cast<int64_t>(segs.size() * sizeof(Seg)), 256);
+  const size_t szp = align_up(static_cast<int64_t>(pieces.size() * sizeof(Piece)), 256);
+  const size_t szo = align_up(static_cast<int64_t>(outs.size() * sizeof(Out)), 256);
+  const size_t om = 0, ot = align_up(static_cast<int64_t>(szm), 256), os = ot + szt, op = os + szs, oo = op + szp;
+  const size_t total = oo + szo + 256;
+  std::vector<uint8_t> host(total, 0);
+  if (szm) memcpy(host.data() + om, maps.data(), szm);
+  if (!all.empty()) memcpy(host.data() + ot, all.data(), all.size() * sizeof(Task));
+  if (!segs.empty()) memcpy(host.data() + os, segs.data(), segs.size() * sizeof(Seg));
+  if (!pieces.empty()) memcpy(host.data() + op, pieces.data(), pieces.size() * sizeof(Piece));
+  if (!outs.empty()) memcpy(host.data() + oo, outs.data(), outs.size() * sizeof(Out));
+  if (cudaMallocAsync(&p->d_tables, total, h->stream) != cudaSuccess) { cudaGetLastError(); delete p; return TLR_STATUS_CUDA_ERROR; }
+  if (cudaMemcpyAsync(p->d_tables, host.data(), total, cudaMemcpyHostToDevice, h->stream) != cudaSuccess ||
+      cudaStreamSynchronize(h->stream) != cudaSuccess) {
+    cudaFreeAsync(p->d_tables, h->stream);
+    delete p;
+    return TLR_STATUS_CUDA_ERROR;
+  }
+  uint8_t *dt = static_cast<uint8_t *>(p->d_tables);
+  p->d_maps = dt + om;
+  p->d_tasks = reinterpret_cast<const Task *>(dt + ot);
+  p->d_segs = reinterpret_cast<const Seg *>(dt + os);
+  p->d_pieces = reinterpret_cast<const Piece *>(dt + op);
+  p->d_outs = reinterpret_cast<const Out *>(dt + oo);
+  *plan_out = p;
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_debug_check_plan(tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A, const tlr_operand_t *B,
+                                  size_t workspace_bytes, tlr_order_t order, tlr_plan_info_t *info,
+                                  char *msg, size_t msg_len) {
+  if (msg && msg_len) msg[0] = 0;
+  const uint64_t ws = 0x100000000000ull;   // a stand-in address: nothing is dereferenced
+  PlanCore pc;
+  tlr_status_t st = core_init(pc, opA, opB, A, B, true, ws, nullptr, nullptr, nullptr);
+  if (st) return st;
+  const int es = elem_size(pc.pv.dtype);
+  std::vector<Rect> rects;
+  if (!split(pc, static_cast<int64_t>(workspace_bytes), order, es, rects)) return TLR_STATUS_WORKSPACE_TOO_SMALL;
+  Tables tb;
+  tb.bn = choose_bn(pc);
+  st = build_tables(pc, rects, ws, true, tb);
+  if (st) return st;
+  const int64_t need = pc.fixed + max_rect_bytes(pc, rects, es);
+  tb.info.workspace_bytes = static_cast<size_t>(need);
+  tb.info.launches = static_cast<int64_t>(tb.launches.size());
+  if (info) *info = tb.info;
+  const std::string why = validate_tables(pc, tb, ws, std::max<int64_t>(need, static_cast<int64_t>(workspace_bytes)));
+  if (!why.empty()) {
+    if (msg && msg_len) { strncpy(msg, why.c_str(), msg_len - 1); msg[msg_len - 1] = 0; }
+    return TLR_STATUS_INVALID_ARG;
+  }
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_plan_info(tlr_plan_t plan, tlr_plan_info_t *info) {
+  if (!plan || !info) return TLR_STATUS_INVALID_ARG;
+  *info = plan->info;
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_plan_execute(tlr_plan_t p, float alpha, float beta, float *C, int64_t ldc) {
+  if (!p || !C) return TLR_STATUS_INVALID_ARG;
+  if (ldc < p->Cm || (ldc % 4)) return ldc < p->Cm ? TLR_STATUS_INVALID_ARG : TLR_STATUS_ALIGNMENT;
+  if (!aligned16(C)) return TLR_STATUS_ALIGNMENT;
+  tlr_handle_t h = p->h;
+  const int sms = device_sms();
+  std::pair<cudaEvent_t, cudaEvent_t> ev;
+  if (alpha == 0.f) {
+    if (record_start(h, kKindScale, ev) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+    cudaError_t e = launch_scale_c(C, ldc, p->Cm, p->Cn, beta, 4 * sms, h->stream);
+    if (e != cudaSuccess || record_stop(h, ev) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+    return TLR_STATUS_OK;
+  }
+  if (!p->round_n.empty()) {
+    if (record_start(h, kKindRound, ev) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+    cudaError_t e = launch_round_tf32(p->round_src.data(), p->round_dst.data(), p->round_n.data(),
+                                      static_cast<int>(p->round_n.size()), 4 * sms, h->stream);
+    if (e != cudaSuccess || record_stop(h, ev) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+  }
+  Params prm;
+  memset(&prm, 0, sizeof prm);
+  prm.maps = p->d_maps;
+  prm.segs = p->d_segs;
+  prm.pieces = p->d_pieces;
+  prm.outs = p->d_outs;
+  prm.C = C;
+  prm.ldc = ldc;
+  prm.alpha = alpha;
+  prm.beta = beta;
+  prm.bn = p->bn;
+  prm.err = h->d_err;
+  prm.wait_limit_ns = h->wait_limit_ns;
+  for (const Launch &l : p->launches) {
+    prm.tasks = p->d_tasks + l.t0;
+    prm.ntasks = static_cast<int32_t>(l.t1 - l.t0);
+    const int grid = static_cast<int>(std::min<int64_t>(sms, l.t1 - l.t0));
+    if (record_start(h, l.kind, ev) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+    if (launch_task_gemm(p->tf32, prm, grid, h->stream) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+    if (record_stop(h, ev) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+  }
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_plan_destroy(tlr_plan_t p) {
+  if (!p) return TLR_STATUS_INVALID_ARG;
+  if (p->d_tables) cudaFreeAsync(p->d_tables, p->h->stream);
+  delete p;
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_gemm(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, float alpha, const tlr_operand_t *A,
+                      const tlr_operand_t *B, float beta, float *C, int64_t ldc, void *workspace,
+                      size_t workspace_bytes) {
+  tlr_plan_t p = nullptr;
+  tlr_status_t st = tlr_plan_create(h, opA, opB, A, B, workspace, workspace_bytes, TLR_ORDER_AUTO, &p);
+  if (st) return st;
+  st = tlr_plan_execute(p, alpha, beta, C, ldc);
+  tlr_plan_destroy(p);
+  return st;
+}
+
+tlr_status_t tlr_get_device_status(tlr_handle_t h) {
+  if (!h) return TLR_STATUS_INVALID_ARG;
+  if (cudaStreamSynchronize(h->stream) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+  unsigned int err = 0;
+  if (cudaMemcpy(&err, h->d_err, sizeof err, cudaMemcpyDeviceToHost) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+  if (err) {
+    cudaMemset(h->d_err, 0, sizeof err);
+    return TLR_STATUS_TIMEOUT;
+  }
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_set_timing(tlr_handle_t h, int enabled) {
+  if (!h) return TLR_STATUS_INVALID_ARG;
+  h->timing = enabled != 0;
+  return TLR_STATUS_OK;
+}
+
+static tlr_status_t collect_timing(tlr_handle_t h) {
+  if (h->ev_used.empty()) return TLR_STATUS_OK;
+  if (cudaStreamSynchronize(h->stream) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+  for (auto &u : h->ev_used) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, u.second.first, u.second.second) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+    h->ms[u.first] += ms;
+    h->count[u.first] += 1;
+    h->ev_free.push_back(u.second);
+  }
+  h->ev_used.clear();
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_get_timing(tlr_handle_t h, int kind, double *ms, int64_t *launches) {
+  if (!h || kind < 0 || kind >= kNumKinds) return TLR_STATUS_INVALID_ARG;
+  tlr_status_t st = collect_timing(h);
+  if (st) return st;
+  if (ms) *ms = h->ms[kind];
+  if (launches) *launches = h->count[kind];
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_reset_timing(tlr_handle_t h) {
+  if (!h) return TLR_STATUS_INVALID_ARG;
+  tlr_status_t st = collect_timing(h);
+  for (int k = 0; k < kNumKinds; ++k) { h->ms[k] = 0; h->count[k] = 0; }
+  return st;
+}
+
+tlr_status_t tlr_set_wait_limit_us(tlr_handle_t h, int64_t limit_us) {
+  if (!h || limit_us <= 0) return TLR_STATUS_INVALID_ARG;
+  h->wait_limit_ns = static_cast<unsigned long long>(limit_us) * 1000ull;
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_debug_unsatisfied_wait(tlr_handle_t h) {
+  if (!h) return TLR_STATUS_INVALID_ARG;
+  Params prm;
+  memset(&prm, 0, sizeof prm);
+  prm.err = h->d_err;
+  prm.wait_limit_ns = h->wait_limit_ns;
+  if (launch_unsatisfied_wait(prm, h->stream) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+  return TLR_STATUS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// Device-side descriptor tables shared by the host planner (tlr_plan.cu) and
+// the tcgen05 kernel (tlr_kernels.cu). Everything here is plain data: the
+// planner fills these arrays once per plan and uploads them; each kernel launch
+// walks a contiguous range of tasks.
+//
+// A task is one 128 x BN output tile of one product. Its accumulator is the
+// sum over a short list of K segments; each segment is one operand pair read
+// through two TMA tensor maps with exact extents (so ragged ranks are
+// zero-filled by the copy engine, never padded in memory). This is how the sum
+// over contraction tiles k runs inside one tensor-core K-loop ("Tile-Low-Rank
+// GEMM: Designing Storage Around the Contraction", section "One product, three
+// stages", Stage 3) and how the dense-diagonal terms of "TLR Matrix
+// Multiplication", section "Regular TLR GEMM", join the same accumulator so C is
+// written once.
+#pragma once
+#include <stdint.h>
+
+namespace tlr {
+
+constexpr int kBM = 128;            // rows of an output tile (MMA M)
+constexpr int kMaxBN = 256;         // widest output tile (MMA N)
+constexpr int kStages = 4;          // shared-memory pipeline depth
+constexpr int kSmemA = kBM * 128;   // one stage of A: 128 rows x 128 bytes
+constexpr int kSmemB = kMaxBN * 128;
+constexpr int kStageBytes = kSmemA + kSmemB;
+constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kTmemCols = 512;      // two accumulators of up to 256 fp32 columns
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+
+enum : uint32_t {
+  kSegAMN = 1u,   // A operand MN-major (rows of its view are M); else K-major
+  kSegBMN = 2u,   // B operand MN-major (rows of its view are N); else K-major
+};
+
+// One K segment of a task. TMA coordinates are those of the first box; the
+// kernel steps x/y by the box size along MN and by BK along K.
+struct alignas(16) Seg {
+  int32_t a_map, b_map;   // indices into the tensor-map table
+  int32_t a_x, a_y;       // MN-major: (mn0, k0); K-major: (k0, mn0)
+  int32_t b_x, b_y;
+  int32_t k_len;          // logical K of this segment (elements, > 0)
+  uint32_t flags;
+};
+
+// Row pieces: output-tile rows [src0, src0+len) go to output rows dst0.. .
+struct alignas(16) Piece {
+  int32_t src0, len;
+  int64_t dst0;
+};
+
+enum : int32_t {
+  kOutC = 0,        // fp32 C: alpha * acc + beta * C (C unread when beta == 0)
+  kOutBF16 = 1,     // workspace, bf16 round-to-nearest-even
+  kOutTF32 = 2,     // workspace, fp32 rounded to nearest tf32
+};
+
+struct alignas(16) Out {
+  void *ptr;        // NULL for kOutC: the launch's C pointer is used
+  int64_t ld;       // ignored for kOutC (the launch's ldc)
+  int32_t kind;
+  int32_t trans;    // 1: element (r, c) of the tile goes to ptr[c + r * ld]
+};
+
+struct alignas(16) Task {
+  int32_t seg0, nseg;     // segments [seg0, seg0 + nseg); nseg == 0 writes zeros (beta * C)
+  int32_t out;            // index into the output table
+  int32_t rows, cols;     // valid part of the tile (<= kBM, <= BN)
+  int32_t piece0, npiece; // row pieces; npiece == 0: output row = row0 + r
+  int32_t pad_;
+  int64_t row0, col0;     // output coordinates of the tile origin
+};
+
+struct Params {
+  const void *maps;       // CUtensorMap[], 64-byte aligned, device memory
+  const Task *tasks;
+  const Seg *segs;
+  const Piece *pieces;
+  const Out *outs;
+  float *C;
+  int64_t ldc;
+  float alpha, beta;
+  int32_t ntasks;
+  int32_t bn;             // output tile width (multiple of 64, <= kMaxBN)
+  unsigned int *err;      // device error word (bounded waits that ran out)
+  unsigned long long wait_limit_ns;
+};
+
+}  // namespace tlr

@@ -1,0 +1,151 @@
+"""Device memory for operands and C, and the C-ABI descriptors that point at it.
+
+PyTorch provides the device allocations, pinned host staging and streams; the
+library's kernels do every step of the product.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import numpy as np
+
+from . import _abi
+
+_BUFS = ("U", "V", "D", "bu_U", "bu_V", "bv_U", "bv_V", "gamma")
+
+
+def _as_torch(a: np.ndarray, dtype: str):
+    import torch
+    if dtype == "bf16":
+        bits = (np.ascontiguousarray(a, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+
+
+def host_descriptor(X) -> tuple:
+    """Descriptor with ranks only (no device pointers): for tlr_analyze and sizing."""
+    d = _abi.tlr_operand_t()
+    keep = []
+    d.dtype = _abi.TLR_BF16 if X.dtype == "bf16" else _abi.TLR_F32
+    d.rows, d.cols = X.rows, X.cols
+    if X.kind == "dense":
+        d.kind, d.ld = _abi.TLR_KIND_DENSE, X.rows
+        return d, keep
+    r = np.ascontiguousarray(X.ranks, dtype=np.int32)
+    keep.append(r)
+    d.kind, d.b, d.diag_dense, d.ranks = _abi.TLR_KIND_TLR, X.b, int(bool(X.diag_dense)), r.ctypes.data
+    return d, keep
+
+
+class DeviceOperand:
+    """Device copy of a generator matrix (TLR or dense) plus its descriptor.
+
+    With ``pinned=True`` a pinned host copy is kept so that ``upload`` can
+    re-send the inputs host-to-device on a stream (end-to-end timing).
+    """
+
+    def __init__(self, X, device="cuda", pinned: bool = False):
+        import torch
+        self.X = X
+        self.host = {}
+        self.dev = {}
+        d, keep = host_descriptor(X)
+        self._keep = keep
+        names = ("data",) if X.kind == "dense" else _BUFS
+        for name in names:
+            a = X.data if name == "data" else getattr(X, name)
+            if a is None or a.size == 0:
+                continue
+            h = _as_torch(a, X.dtype)
+            if pinned:
+                h = h.pin_memory()
+            self.host[name] = h
+            self.dev[name] = h.to(device, non_blocking=False)
+            setattr(d, name, self.dev[name].data_ptr())
+        self.desc = d
+        self.nbytes = sum(t.numel() * t.element_size() for t in self.dev.values())
+
+    def upload(self, stream=None) -> int:
+        """Copy the pinned host inputs to the device buffers; returns bytes copied."""
+        n = 0
+        for name, h in self.host.items():
+            self.dev[name].copy_(h, non_blocking=True)
+            n += h.numel() * h.element_size()
+        return n
+
+
+class DeviceProblem:
+    """A ``tlr_inputs.Problem`` resident on the device, with C and a workspace."""
+
+    def __init__(self, p, device="cuda", pinned: bool = False, workspace_bytes: Optional[int] = None,
+                 fill_c_nan: bool = True):
+        import torch
+        self.p = p
+        self.A = DeviceOperand(p.A, device, pinned)
+        self.B = DeviceOperand(p.B, device, pinned)
+        self.opA = _abi.TLR_OP_T if p.opA == "T" else _abi.TLR_OP_N
+        self.opB = _abi.TLR_OP_T if p.opB == "T" else _abi.TLR_OP_N
+        self.ldc = p.m
+        if p.C is not None:
+            self.C0_host = torch.from_numpy(np.ascontiguousarray(p.C, dtype=np.float32))
+            if pinned:
+                self.C0_host = self.C0_host.pin_memory()
+            self.C0 = self.C0_host.to(device)
+        else:
+            self.C0_host = None
+            self.C0 = None
+        self.C = torch.empty(p.m * p.n, dtype=torch.float32, device=device)
+        self.reset_c(fill_c_nan)
+        self.handle = None
+        self.plan = None
+        self.ws = None
+        self.ws_bytes = workspace_bytes
+
+    def reset_c(self, fill_nan: bool = True):
+        if self.C0 is not None:
+            self.C.copy_(self.C0)
+        else:
+            self.C.fill_(float("nan") if fill_nan else 0.0)
+
+    def make_plan(self, handle: int, budget: Optional[int] = None, order: int = _abi.TLR_ORDER_AUTO):
+        import torch
+        need_full = _abi.tlr_gemm_workspace_bytes(handle, self.opA, self.opB, self.A.desc, self.B.desc, 1)
+        if budget is None:
+            budget = self.p.budget if self.p.budget is not None else need_full
+        self.ws_bytes = int(budget)
+        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=self.C.device)
+        self.handle = handle
+        self.plan = _abi.tlr_plan_create(handle, self.opA, self.opB, self.A.desc, self.B.desc,
+                                         self.ws.data_ptr(), self.ws_bytes, order)
+        return self.plan
+
+    def run(self):
+        _abi.tlr_plan_execute(self.plan, self.p.alpha, self.p.beta, self.C.data_ptr(), self.ldc)
+
+    def info(self) -> dict:
+        return _abi.tlr_plan_info(self.plan)
+
+    def result(self) -> np.ndarray:
+        """C as a (m, n) float64 numpy array."""
+        return self.C.double().cpu().numpy().reshape(self.p.n, self.p.m).T
+
+    def close(self):
+        if self.plan:
+            _abi.tlr_plan_destroy(self.plan)
+            self.plan = None
+
+
+def fake_descriptor(X, base: int) -> tuple:
+    """Descriptor whose buffers sit at stand-in addresses (for host-only checks)."""
+    d, keep = host_descriptor(X)
+    addr = base
+    names = ("data",) if X.kind == "dense" else _BUFS
+    for name in names:
+        a = X.data if name == "data" else getattr(X, name)
+        if a is None or a.size == 0:
+            continue
+        setattr(d, name, addr)
+        es = 2 if X.dtype == "bf16" else 4
+        addr += ((a.size * es + 4095) // 4096) * 4096
+    return d, keep
