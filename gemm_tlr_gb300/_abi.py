@@ -51,7 +51,7 @@ class tlr_plan_info_t(ctypes.Structure):
         ("flops_stage2", ctypes.c_double), ("flops_stage3", ctypes.c_double),
         ("flops_dense_terms", ctypes.c_double), ("flops_right_final", ctypes.c_double),
         ("flops_left_final", ctypes.c_double), ("workspace_bytes", ctypes.c_size_t),
-        ("tasks", ctypes.c_int64),
+        ("tasks", ctypes.c_int64), ("flops_launch", ctypes.c_double * 3),
     ]
 
 
@@ -177,10 +177,16 @@ def tlr_plan_create(h: int, opA: int, opB: int, A: tlr_operand_t, B: tlr_operand
     return p.value
 
 
+def _info_dict(i) -> dict:
+    d = {f: getattr(i, f) for f, _ in tlr_plan_info_t._fields_}
+    d["flops_launch"] = list(i.flops_launch)
+    return d
+
+
 def tlr_plan_info(p: int) -> dict:
     i = tlr_plan_info_t()
     check(lib().tlr_plan_info(_P(p), ctypes.byref(i)), "tlr_plan_info")
-    return {f: getattr(i, f) for f, _ in tlr_plan_info_t._fields_}
+    return _info_dict(i)
 
 
 def tlr_plan_execute(p: int, alpha: float, beta: float, C: int, ldc: int) -> None:
@@ -230,4 +236,4 @@ def tlr_debug_check_plan(opA: int, opB: int, A: tlr_operand_t, B: tlr_operand_t,
     msg = ctypes.create_string_buffer(512)
     st = lib().tlr_debug_check_plan(opA, opB, ctypes.byref(A), ctypes.byref(B), ws_bytes, order,
                                     ctypes.byref(info), msg, 512)
-    return st, msg.value.decode(), {f: getattr(info, f) for f, _ in tlr_plan_info_t._fields_}
+    return st, msg.value.decode(), _info_dict(info)

@@ -438,6 +438,35 @@ __global__ void round_tf32_kernel(const __grid_constant__ RoundJob job) {
   }
 }
 
+// Transposed, tf32-rounded copies of input views (TF32 tensor cores read
+// K-major operands only). 256 threads: a 32 x 32 tile through shared memory,
+// coalesced reads along the source's columns and writes along the copy's.
+__global__ void transpose_round_kernel(const TJob *__restrict__ jobs, int njobs, int64_t ntiles) {
+  __shared__ float tile[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    int lo = 0, hi = njobs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (jobs[mid].tile0 <= t) lo = mid; else hi = mid - 1;
+    }
+    const TJob J = jobs[lo];
+    const int64_t local = t - J.tile0;
+    const int64_t tr = (J.rows + 31) / 32;
+    const int64_t r0 = (local % tr) * 32, c0 = (local / tr) * 32;
+    for (int yy = ty; yy < 32; yy += 8) {
+      const int64_t r = r0 + tx, c = c0 + yy;
+      tile[yy][tx] = (r < J.rows && c < J.cols) ? J.src[r + c * J.src_ld] : 0.f;
+    }
+    __syncthreads();
+    for (int yy = ty; yy < 32; yy += 8) {
+      const int64_t c = c0 + tx, r = r0 + yy;
+      if (r < J.rows && c < J.cols) J.dst[c + r * J.dst_ld] = round_tf32(tile[tx][yy]);
+    }
+    __syncthreads();
+  }
+}
+
 // C <- beta * C (beta == 0: C <- 0 without reading C), column-major m x n.
 __global__ void scale_c_kernel(float *C, int64_t ldc, int64_t m, int64_t n, float beta) {
   const int64_t total = m * n;
@@ -495,6 +524,12 @@ cudaError_t launch_round_tf32(const float *const *src, float *const *dst, const 
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_transpose_round(const TJob *jobs, int njobs, int64_t ntiles, int grid, cudaStream_t stream) {
+  if (njobs <= 0 || ntiles <= 0) return cudaSuccess;
+  transpose_round_kernel<<<grid, 256, 0, stream>>>(jobs, njobs, ntiles);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_scale_c(float *C, int64_t ldc, int64_t m, int64_t n, float beta, int grid,

@@ -57,6 +57,7 @@ cudaError_t launch_round_tf32(const float *const *src, float *const *dst, const 
                               int grid, cudaStream_t stream);
 cudaError_t launch_scale_c(float *C, int64_t ldc, int64_t m, int64_t n, float beta, int grid,
                            cudaStream_t stream);
+cudaError_t launch_transpose_round(const TJob *jobs, int njobs, int64_t ntiles, int grid, cudaStream_t stream);
 cudaError_t launch_unsatisfied_wait(const Params &p, cudaStream_t stream);
 }  // namespace tlr
 
@@ -395,6 +396,14 @@ struct Launch {
 };
 
 // ------------------------------------------------------------------ builder
+using ViewKey = std::tuple<uint64_t, int64_t, int64_t, int64_t>;
+ViewKey vkey(const View &v) { return std::make_tuple(v.addr, v.rows, v.cols, v.ld); }
+
+struct ORef {           // an operand as the kernel reads it: tensor map + majorness
+  int map = 0;
+  bool mn = false;
+};
+
 struct Builder {
   const LOp &X;
   const LOp &Y;
@@ -410,9 +419,14 @@ struct Builder {
   std::vector<Piece> *pieces;
   std::vector<Out> *outs;
   tlr_status_t status = TLR_STATUS_OK;
-  double fl_s1 = 0, fl_s2 = 0, fl_s3 = 0, fl_dense = 0, fl_final = 0;
+  double fl_s1 = 0, fl_s2 = 0, fl_s3 = 0, fl_dense = 0;
+  double fl_launch[3] = {0, 0, 0};      // the same FLOPs by launch class
   bool dry = false;                     // validate only: no tensor maps are encoded
   std::vector<std::pair<View, int>> *views = nullptr;   // every map's view and majorness
+  // TF32 operands are read K-major only: a caller view that would be read
+  // MN-major is replaced by its transposed copy (made by the pre-pass).
+  const std::map<ViewKey, View> *tcopy = nullptr;
+  std::set<ViewKey> *need_copy = nullptr;               // collection pass: record, do not build
 
   int map_of(const View &v, bool mn) {
     auto key = std::make_tuple(v.addr, v.rows, v.cols, v.ld, mn ? 1 : 0);
@@ -421,7 +435,7 @@ struct Builder {
     CUtensorMap m;
     memset(&m, 0, sizeof m);
     if (views) views->push_back({v, mn ? 1 : 0});
-    if (dry) {
+    if (dry || need_copy) {
       const int idx = static_cast<int>(maps->size());
       maps->push_back(m);
       (*map_index)[key] = idx;
@@ -443,6 +457,31 @@ struct Builder {
     maps->push_back(m);
     (*map_index)[key] = idx;
     return idx;
+  }
+
+  // A caller-owned (input) view read with the given majorness.
+  ORef input(const View &v, bool mn) {
+    if (tf32 && mn) {
+      if (need_copy) { need_copy->insert(vkey(v)); return ORef{map_of(v, true), true}; }
+      auto it = tcopy ? tcopy->find(vkey(v)) : std::map<ViewKey, View>::const_iterator();
+      if (!tcopy || it == tcopy->end()) { status = TLR_STATUS_UNSUPPORTED; return ORef{}; }
+      return ORef{map_of(it->second, false), false};
+    }
+    return ORef{map_of(v, mn), mn};
+  }
+  // A workspace view (always produced K-major for the stage that reads it).
+  ORef work(const View &v) { return ORef{map_of(v, false), false}; }
+
+  // Rows [kk0, kk0+kl) x columns [n0, n0+nl) of a dense op(Y) as a B operand.
+  ORef dense_block(int64_t kk0, int64_t kl, int64_t n0, int64_t nl) {
+    const View &d = Y.dv;
+    if (!Y.dtrans) return input(View{d.addr + static_cast<uint64_t>((kk0 + n0 * d.ld) * es), kl, nl, d.ld}, false);
+    if (!tf32) return input(View{d.addr + static_cast<uint64_t>((n0 + kk0 * d.ld) * es), nl, kl, d.ld}, true);
+    if (need_copy) { need_copy->insert(vkey(d)); return ORef{0, false}; }
+    auto it = tcopy ? tcopy->find(vkey(d)) : std::map<ViewKey, View>::const_iterator();
+    if (!tcopy || it == tcopy->end()) { status = TLR_STATUS_UNSUPPORTED; return ORef{}; }
+    const View &c = it->second;   // stored^T: rows = stored cols (K), cols = stored rows (N)
+    return ORef{map_of(View{c.addr + static_cast<uint64_t>((kk0 + n0 * c.ld) * es), kl, nl, c.ld}, false), false};
   }
 
   int out_ws(uint64_t ptr, int64_t ld) {
@@ -480,32 +519,36 @@ struct Builder {
     pieces->insert(pieces->end(), pc.begin(), pc.end());
     tasks->push_back(t);
   }
-  static Seg seg(int am, int bm, bool amn, bool bmn, int64_t a_mn0, int64_t b_mn0, int64_t k_len) {
+  static Seg seg(ORef a, ORef b, int64_t a_mn0, int64_t b_mn0, int64_t k_len) {
     Seg s;
-    s.a_map = am;
-    s.b_map = bm;
-    s.a_x = static_cast<int32_t>(amn ? a_mn0 : 0);
-    s.a_y = static_cast<int32_t>(amn ? 0 : a_mn0);
-    s.b_x = static_cast<int32_t>(bmn ? b_mn0 : 0);
-    s.b_y = static_cast<int32_t>(bmn ? 0 : b_mn0);
+    s.a_map = a.map;
+    s.b_map = b.map;
+    s.a_x = static_cast<int32_t>(a.mn ? a_mn0 : 0);
+    s.a_y = static_cast<int32_t>(a.mn ? 0 : a_mn0);
+    s.b_x = static_cast<int32_t>(b.mn ? b_mn0 : 0);
+    s.b_y = static_cast<int32_t>(b.mn ? 0 : b_mn0);
     s.k_len = static_cast<int32_t>(k_len);
-    s.flags = (amn ? kSegAMN : 0u) | (bmn ? kSegBMN : 0u);
+    s.flags = (a.mn ? kSegAMN : 0u) | (b.mn ? kSegBMN : 0u);
     return s;
   }
 };
 
 // Workspace layout of one rectangle (right order on X * Y).
+//   S_k^T   (Gamma_k(J) padded) x sigma_k(I): Stage-1 output, the column block of
+//           tile j starts on a 16-byte boundary so Stage 2 reads it K-major;
+//   T       rows of T_i (parts padded to 8) x W_J columns, column-major;
+//   P_i^T   (Gamma_i(J) padded) x d_i: (D_ii W_{i,J})^T, blocks aligned like S.
 struct RectLayout {
   int i0, i1, j0, j1;
   int64_t WJ = 0;
   std::vector<int64_t> colT;                 // per j in [j0, j1]: column inside T / the C block
-  std::vector<int64_t> Soff, Sld, Srows;     // per k
-  std::vector<std::vector<int64_t>> Scol;    // per k, per j: column of block j in S_k (-1: none)
+  std::vector<int64_t> Soff, Sld, Ssig;      // per k (Soff < 0: no S_k)
+  std::vector<std::vector<int64_t>> Srow;    // per k, per j: first row of block j in S_k^T
   std::vector<int64_t> R;                    // per i: first T row
   std::vector<std::vector<int64_t>> Toff;    // per i, per part: first T row of the part
   int64_t Tld = 0, Toffset = 0;
-  std::vector<int64_t> Poff;                 // per i
-  std::vector<std::vector<int64_t>> Pcol;    // per i, per j
+  std::vector<int64_t> Poff, Pld;            // per i
+  std::vector<std::vector<int64_t>> Prow;    // per i, per j
   int64_t bytes = 0;
 };
 
@@ -517,23 +560,22 @@ RectLayout layout_rect(const LOp &X, const LOp &Y, int i0, int i1, int j0, int j
   L.WJ = L.colT.back();
   int64_t off = 0;
   const int nk = X.nc;
-  L.Soff.assign(nk, -1); L.Sld.assign(nk, 0); L.Srows.assign(nk, 0); L.Scol.assign(nk, {});
+  L.Soff.assign(nk, -1); L.Sld.assign(nk, 0); L.Ssig.assign(nk, 0); L.Srow.assign(nk, {});
   if (!Y.dense) {
     for (int k = 0; k < nk; ++k) {
       int64_t sig = 0;
       for (int i = i0; i < i1; ++i) if (!X.dt(i, k)) sig += X.r(i, k);
-      L.Srows[k] = sig;
-      L.Scol[k].assign(j1 - j0, -1);
+      L.Ssig[k] = sig;
+      L.Srow[k].assign(j1 - j0, -1);
       int64_t g = 0;
       for (int j = j0; j < j1; ++j)
-        if (!Y.dt(k, j) && Y.r(k, j) > 0) { L.Scol[k][j - j0] = g; g += Y.r(k, j); }
+        if (!Y.dt(k, j) && Y.r(k, j) > 0) { L.Srow[k][j - j0] = g; g += align_up(Y.r(k, j), 8); }
       if (sig == 0 || g == 0) continue;
-      L.Sld[k] = align_up(sig, 8);
+      L.Sld[k] = g;
       L.Soff[k] = off;
-      off = align_up(off + L.Sld[k] * g * es, 256);
+      off = align_up(off + g * sig * es, 256);
     }
   }
-  // T: rows of each part of each tile row padded to 8 (16-byte aligned bases)
   L.R.assign(X.nr, 0);
   L.Toff.assign(X.nr, {});
   int64_t rows = 0;
@@ -547,19 +589,20 @@ RectLayout layout_rect(const LOp &X, const LOp &Y, int i0, int i1, int j0, int j
   L.Tld = align_up(std::max<int64_t>(rows, 8), 8);
   L.Toffset = off;
   off = align_up(off + L.Tld * L.WJ * es, 256);
-  // P_i = D_ii W_{i,J}
   L.Poff.assign(X.nr, -1);
-  L.Pcol.assign(X.nr, {});
+  L.Pld.assign(X.nr, 0);
+  L.Prow.assign(X.nr, {});
   if (!Y.dense) {
     for (int i = i0; i < i1; ++i) {
       if (!(i < X.nc && X.dt(i, i))) continue;
-      L.Pcol[i].assign(j1 - j0, -1);
+      L.Prow[i].assign(j1 - j0, -1);
       int64_t g = 0;
       for (int j = j0; j < j1; ++j)
-        if (!Y.dt(i, j) && Y.r(i, j) > 0) { L.Pcol[i][j - j0] = g; g += Y.r(i, j); }
+        if (!Y.dt(i, j) && Y.r(i, j) > 0) { L.Prow[i][j - j0] = g; g += align_up(Y.r(i, j), 8); }
       if (g == 0) continue;
+      L.Pld[i] = g;
       L.Poff[i] = off;
-      off = align_up(off + X.rd[i] * g * es, 256);
+      off = align_up(off + g * X.rd[i] * es, 256);
     }
   }
   L.bytes = off;
@@ -577,12 +620,14 @@ double final_cost(const LOp &X, int i0, int i1, int64_t WJ) {
   return f;
 }
 
-std::vector<Piece> pieces_for(const RPart &rp, int64_t row_base_in_space, int64_t w0, int64_t rows,
+// Row pieces of an output tile whose rows [w0, w0+rows) of a product's row
+// space run over the tiles of `rp` (placed at row_base): each tile's rows go
+// to dst_of(tile).
+std::vector<Piece> pieces_for(const RPart &rp, int64_t row_base, int64_t w0, int64_t rows,
                               const std::function<int64_t(int)> &dst_of) {
-  // rp's tiles occupy rows [row_base + local, +width) of the product's row space
   std::vector<Piece> pc;
   for (size_t q = 0; q < rp.tiles.size(); ++q) {
-    const int64_t s = row_base_in_space + rp.tiles[q].second, e = s + rp.width[q];
+    const int64_t s = row_base + rp.tiles[q].second, e = s + rp.width[q];
     const int64_t a = std::max(s, w0), b = std::min(e, w0 + rows);
     if (a >= b) continue;
     Piece p;
@@ -596,7 +641,7 @@ std::vector<Piece> pieces_for(const RPart &rp, int64_t row_base_in_space, int64_
 
 // Build the tasks of one rectangle into the three launch lists.
 void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vector<Task> &l2,
-                std::vector<Task> &l3, std::vector<Seg> &segs, std::vector<Piece> &pieces) {
+                std::vector<Task> &l3) {
   const LOp &X = B.X;
   const LOp &Y = B.Y;
   const int es = B.es, bn = B.bn;
@@ -611,120 +656,109 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
         return L.Toff[i][pi] + (X.rpos[i][k] - parts[pi].col0);
     return -1;
   };
-  auto rank_col = [&](int k) { return [&X, k](int i) { return static_cast<int64_t>(X.r(i, k)); }; };
+  auto xcol = [&X](int k) { return [&X, k](int i) { return static_cast<int64_t>(X.r(i, k)); }; };
+  auto yrow = [&Y](int k) { return [&Y, k](int j) { return static_cast<int64_t>(Y.r(k, j)); }; };
 
   // ---------------- L1: Stage 1, P, k=j blocks (or the dense-B product)
   B.tasks = &l1;
   for (int k = 0; k < X.nc; ++k) {
-    std::vector<RPart> Ap = restrict_panel(X.colp[k], X.cpos[k], i0, i1, rank_col(k), es);
+    std::vector<RPart> Ap = restrict_panel(X.colp[k], X.cpos[k], i0, i1, xcol(k), es);
     if (Ap.empty()) continue;
     if (Y.dense) {
-      // rows k of op(B), columns of the rectangle
-      View yk;
-      bool ymn = Y.dtrans;
-      const int64_t c0 = Y.co[j0];
-      if (!Y.dtrans) yk = View{Y.dv.addr + static_cast<uint64_t>((Y.ro[k] + c0 * Y.dv.ld) * es), Y.rd[k], L.WJ, Y.dv.ld};
-      else yk = View{Y.dv.addr + static_cast<uint64_t>((c0 + Y.ro[k] * Y.dv.ld) * es), L.WJ, Y.rd[k], Y.dv.ld};
-      const int bm = B.map_of(yk, ymn);
-      int64_t base = 0;
+      // T_i rows of block k: V_{:,k}^T B_k over the rectangle's columns
+      const ORef bm = B.dense_block(Y.ro[k], Y.rd[k], Y.co[j0], L.WJ);
       for (const RPart &ap : Ap) {
-        const int am = B.map_of(ap.v, false);
-        for (int64_t mt = 0; mt < ceil_div(ap.v.cols, kBM); ++mt)
-          for (int64_t nt = 0; nt < ceil_div(L.WJ, bn); ++nt) {
-            const int64_t rows = std::min<int64_t>(kBM, ap.v.cols - mt * kBM);
-            auto pc = pieces_for(ap, 0, mt * kBM, rows, [&](int i) { return trow(i, k); });
+        const ORef am = B.input(ap.v, false);
+        for (int64_t mt = 0; mt < ceil_div(ap.v.cols, kBM); ++mt) {
+          const int64_t rows = std::min<int64_t>(kBM, ap.v.cols - mt * kBM);
+          auto pc = pieces_for(ap, 0, mt * kBM, rows, [&](int i) { return trow(i, k); });
+          for (int64_t nt = 0; nt < ceil_div(L.WJ, bn); ++nt)
             B.emit(outT, 0, nt * bn, rows, std::min<int64_t>(bn, L.WJ - nt * bn),
-                   {Builder::seg(am, bm, false, ymn, mt * kBM, nt * bn, X.cd[k])}, pc);
-          }
+                   {Builder::seg(am, bm, mt * kBM, nt * bn, X.cd[k])}, pc);
+        }
         B.fl_s1 += 2.0 * ap.v.cols * static_cast<double>(L.WJ) * X.cd[k];
-        base += ap.v.cols;
       }
       continue;
     }
-    // Stage 1: S_k = V_{:,k}^T W_{k,:}
+    // Stage 1, written transposed: S_k^T = W_{k,J}^T V_{k,I}
     if (L.Soff[k] >= 0) {
       const uint64_t S = B.ws + static_cast<uint64_t>(L.Soff[k]);
       const int outS = B.out_ws(S, L.Sld[k]);
-      std::vector<RPart> Bp = restrict_panel(Y.rowp[k], Y.rpos[k], j0, j1,
-                                             [&Y, k](int j) { return static_cast<int64_t>(Y.r(k, j)); }, es);
-      int64_t ra = 0;
-      for (const RPart &ap : Ap) {
-        const int am = B.map_of(ap.v, false);
-        int64_t cb = 0;
-        for (const RPart &bp : Bp) {
-          const int bm = B.map_of(bp.v, false);
-          for (int64_t mt = 0; mt < ceil_div(ap.v.cols, kBM); ++mt)
-            for (int64_t nt = 0; nt < ceil_div(bp.v.cols, bn); ++nt)
-              B.emit(outS, ra + mt * kBM, cb + nt * bn, std::min<int64_t>(kBM, ap.v.cols - mt * kBM),
-                     std::min<int64_t>(bn, bp.v.cols - nt * bn),
-                     {Builder::seg(am, bm, false, false, mt * kBM, nt * bn, X.cd[k])}, {});
-          B.fl_s1 += 2.0 * ap.v.cols * static_cast<double>(bp.v.cols) * X.cd[k];
-          cb += bp.v.cols;
+      std::vector<RPart> Bp = restrict_panel(Y.rowp[k], Y.rpos[k], j0, j1, yrow(k), es);
+      for (const RPart &bp : Bp) {
+        const ORef am = B.input(bp.v, false);
+        for (int64_t mt = 0; mt < ceil_div(bp.v.cols, kBM); ++mt) {
+          const int64_t rows = std::min<int64_t>(kBM, bp.v.cols - mt * kBM);
+          auto pc = pieces_for(bp, 0, mt * kBM, rows, [&](int j) { return L.Srow[k][j - j0]; });
+          int64_t ra = 0;
+          for (const RPart &ap : Ap) {
+            const ORef bm = B.input(ap.v, false);
+            for (int64_t nt = 0; nt < ceil_div(ap.v.cols, bn); ++nt)
+              B.emit(outS, 0, ra + nt * bn, rows, std::min<int64_t>(bn, ap.v.cols - nt * bn),
+                     {Builder::seg(am, bm, mt * kBM, nt * bn, X.cd[k])}, pc);
+            ra += ap.v.cols;
+          }
         }
-        ra += ap.v.cols;
+        for (const RPart &ap : Ap) B.fl_s1 += 2.0 * ap.v.cols * static_cast<double>(bp.v.cols) * X.cd[k];
       }
     }
     // k = j block with a dense tile of op(B): T_i[k-block, k-block] = V_ik^T D_kk
     if (k >= j0 && k < j1 && k < Y.nr && Y.dt(k, k)) {
-      const bool ymn = Y.diag_trans;
-      const int bm = B.map_of(Y.diag[k], ymn);
-      int64_t ra = 0;
+      const ORef bm = B.input(Y.diag[k], Y.diag_trans);
       for (const RPart &ap : Ap) {
-        const int am = B.map_of(ap.v, false);
-        for (int64_t mt = 0; mt < ceil_div(ap.v.cols, kBM); ++mt)
-          for (int64_t nt = 0; nt < ceil_div(Y.cd[k], bn); ++nt) {
-            const int64_t rows = std::min<int64_t>(kBM, ap.v.cols - mt * kBM);
-            auto pc = pieces_for(ap, 0, mt * kBM, rows, [&](int i) { return trow(i, k); });
+        const ORef am = B.input(ap.v, false);
+        for (int64_t mt = 0; mt < ceil_div(ap.v.cols, kBM); ++mt) {
+          const int64_t rows = std::min<int64_t>(kBM, ap.v.cols - mt * kBM);
+          auto pc = pieces_for(ap, 0, mt * kBM, rows, [&](int i) { return trow(i, k); });
+          for (int64_t nt = 0; nt < ceil_div(Y.cd[k], bn); ++nt)
             B.emit(outT, 0, L.colT[k - j0] + nt * bn, rows, std::min<int64_t>(bn, Y.cd[k] - nt * bn),
-                   {Builder::seg(am, bm, false, ymn, mt * kBM, nt * bn, Y.rd[k])}, pc);
-          }
+                   {Builder::seg(am, bm, mt * kBM, nt * bn, Y.rd[k])}, pc);
+        }
         B.fl_dense += 2.0 * ap.v.cols * static_cast<double>(Y.cd[k]) * Y.rd[k];
-        ra += ap.v.cols;
       }
     }
   }
-  // P_i = D_ii W_{i,J}
+  // P_i^T = (D_ii W_{i,J})^T = W_{i,J}^T D_ii^T, written transposed like S
   if (!Y.dense)
     for (int i = i0; i < i1; ++i) {
       if (L.Poff[i] < 0) continue;
       const uint64_t P = B.ws + static_cast<uint64_t>(L.Poff[i]);
-      const int outP = B.out_ws(P, X.rd[i]);
-      const bool amn = !X.diag_trans;
-      const int am = B.map_of(X.diag[i], amn);
-      std::vector<RPart> Bp = restrict_panel(Y.rowp[i], Y.rpos[i], j0, j1,
-                                             [&Y, i](int j) { return static_cast<int64_t>(Y.r(i, j)); }, es);
-      int64_t cb = 0;
+      const int outP = B.out_ws(P, L.Pld[i]);
+      // B operand (kk, n) = op(X)_ii[n, kk]: MN-major on the stored tile unless op(X)_ii is stored^T
+      const ORef dm = B.input(X.diag[i], !X.diag_trans);
+      std::vector<RPart> Bp = restrict_panel(Y.rowp[i], Y.rpos[i], j0, j1, yrow(i), es);
       for (const RPart &bp : Bp) {
-        const int bm = B.map_of(bp.v, false);
-        for (int64_t mt = 0; mt < ceil_div(X.rd[i], kBM); ++mt)
-          for (int64_t nt = 0; nt < ceil_div(bp.v.cols, bn); ++nt)
-            B.emit(outP, mt * kBM, cb + nt * bn, std::min<int64_t>(kBM, X.rd[i] - mt * kBM),
-                   std::min<int64_t>(bn, bp.v.cols - nt * bn),
-                   {Builder::seg(am, bm, amn, false, mt * kBM, nt * bn, X.cd[i])}, {});
+        const ORef am = B.input(bp.v, false);
+        for (int64_t mt = 0; mt < ceil_div(bp.v.cols, kBM); ++mt) {
+          const int64_t rows = std::min<int64_t>(kBM, bp.v.cols - mt * kBM);
+          auto pc = pieces_for(bp, 0, mt * kBM, rows, [&](int j) { return L.Prow[i][j - j0]; });
+          for (int64_t nt = 0; nt < ceil_div(X.rd[i], bn); ++nt)
+            B.emit(outP, 0, nt * bn, rows, std::min<int64_t>(bn, X.rd[i] - nt * bn),
+                   {Builder::seg(am, dm, mt * kBM, nt * bn, X.cd[i])}, pc);
+        }
         B.fl_dense += 2.0 * X.rd[i] * static_cast<double>(bp.v.cols) * X.cd[i];
-        cb += bp.v.cols;
       }
     }
 
+  B.fl_launch[0] += B.fl_s1 + B.fl_dense;
+  const double before2 = B.fl_s2;
   // ---------------- L2: Stage 2, T_i[k, j] = S_ikj Z_kj^T fused over i
   B.tasks = &l2;
   if (!Y.dense)
     for (int k = 0; k < X.nc; ++k) {
-      if (L.Srows[k] == 0) continue;
-      std::vector<RPart> Ap = restrict_panel(X.colp[k], X.cpos[k], i0, i1, rank_col(k), es);
-      // the S_k row space is the concatenation of Ap
+      const int64_t sig = L.Ssig[k];
+      if (sig == 0) continue;
+      std::vector<RPart> Ap = restrict_panel(X.colp[k], X.cpos[k], i0, i1, xcol(k), es);
       std::vector<int64_t> base;
       int64_t acc = 0;
       for (const RPart &ap : Ap) { base.push_back(acc); acc += ap.v.cols; }
-      const int64_t sig = L.Srows[k];
       for (int j = j0; j < j1; ++j) {
         if (Y.dt(k, j)) continue;                       // handled in L1
         const int64_t r = Y.r(k, j);
-        int am = -1, bm = -1;
+        ORef am, bm;
         if (r > 0) {
-          const View sv{B.ws + static_cast<uint64_t>(L.Soff[k] + L.Scol[k][j - j0] * L.Sld[k] * es), sig, r, L.Sld[k]};
-          am = B.map_of(sv, true);
-          bm = B.map_of(Y.inner[static_cast<size_t>(k) * Y.nc + j], true);
+          am = B.work(View{B.ws + static_cast<uint64_t>(L.Soff[k] + L.Srow[k][j - j0] * es), r, sig, L.Sld[k]});
+          bm = B.input(Y.inner[static_cast<size_t>(k) * Y.nc + j], true);
           B.fl_s2 += 2.0 * sig * static_cast<double>(Y.cd[j]) * r;
         }
         for (int64_t mt = 0; mt < ceil_div(sig, kBM); ++mt) {
@@ -736,52 +770,44 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
           }
           for (int64_t nt = 0; nt < ceil_div(Y.cd[j], bn); ++nt) {
             std::vector<Seg> sg;
-            if (r > 0) sg.push_back(Builder::seg(am, bm, true, true, mt * kBM, nt * bn, r));
+            if (r > 0) sg.push_back(Builder::seg(am, bm, mt * kBM, nt * bn, r));
             B.emit(outT, 0, L.colT[j - j0] + nt * bn, rows, std::min<int64_t>(bn, Y.cd[j] - nt * bn), sg, pc);
           }
         }
       }
     }
 
+  B.fl_launch[1] += B.fl_s2 - before2;
+  const double before3 = B.fl_s3 + B.fl_dense;
   // ---------------- L3: Stage 3, C[i, J] = alpha (U_i T_i + dense segment) + beta C
   B.tasks = &l3;
   const int outC = B.out_c();
   for (int i = i0; i < i1; ++i) {
     const auto &parts = X.rowp[i];
-    std::vector<int> am(parts.size()), bm(parts.size());
+    std::vector<ORef> am(parts.size()), bm(parts.size());
     int64_t rho = 0;
     for (size_t pi = 0; pi < parts.size(); ++pi) {
-      am[pi] = B.map_of(parts[pi].v, true);
-      const View tv{T + static_cast<uint64_t>(L.Toff[i][pi] * es), parts[pi].v.cols, L.WJ, L.Tld};
-      bm[pi] = B.map_of(tv, false);
+      if (parts[pi].v.cols <= 0) continue;
+      am[pi] = B.input(parts[pi].v, true);
+      bm[pi] = B.work(View{T + static_cast<uint64_t>(L.Toff[i][pi] * es), parts[pi].v.cols, L.WJ, L.Tld});
       rho += parts[pi].v.cols;
     }
     B.fl_s3 += 2.0 * X.rd[i] * static_cast<double>(L.WJ) * rho;
-    B.fl_final += 2.0 * X.rd[i] * static_cast<double>(L.WJ) * rho;
     const bool xdiag = i < X.nc && X.dt(i, i);
-    int dm = -1;
-    const bool dmn = !X.diag_trans;
-    if (xdiag) dm = B.map_of(X.diag[i], dmn);
+    ORef dm;
+    if (xdiag) dm = B.input(X.diag[i], !X.diag_trans);
     for (int j = j0; j < j1; ++j) {
-      // the dense-tile segment of this output block
-      int sm = -1, zm = -1;
-      bool smn = false, zmn = false;
+      ORef sa, sb;
       int64_t klen = 0;
       if (xdiag) {
         if (Y.dense) {
-          View yi;
-          zmn = Y.dtrans;
-          if (!Y.dtrans) yi = View{Y.dv.addr + static_cast<uint64_t>((Y.ro[i] + Y.co[j] * Y.dv.ld) * es), Y.rd[i], Y.cd[j], Y.dv.ld};
-          else yi = View{Y.dv.addr + static_cast<uint64_t>((Y.co[j] + Y.ro[i] * Y.dv.ld) * es), Y.cd[j], Y.rd[i], Y.dv.ld};
-          sm = dm; smn = dmn; zm = B.map_of(yi, zmn); klen = X.cd[i];
+          sa = dm; sb = B.dense_block(Y.ro[i], Y.rd[i], Y.co[j], Y.cd[j]); klen = X.cd[i];
         } else if (j == i && Y.dt(i, i)) {
-          sm = dm; smn = dmn; zmn = Y.diag_trans; zm = B.map_of(Y.diag[i], zmn); klen = X.cd[i];
+          sa = dm; sb = B.input(Y.diag[i], Y.diag_trans); klen = X.cd[i];
         } else if (!Y.dt(i, j) && Y.r(i, j) > 0) {
-          const int64_t r = Y.r(i, j);
-          const View pv{B.ws + static_cast<uint64_t>(L.Poff[i] + L.Pcol[i][j - j0] * X.rd[i] * es), X.rd[i], r, X.rd[i]};
-          sm = B.map_of(pv, true); smn = true;
-          zm = B.map_of(Y.inner[static_cast<size_t>(i) * Y.nc + j], true); zmn = true;
-          klen = r;
+          klen = Y.r(i, j);
+          sa = B.work(View{B.ws + static_cast<uint64_t>(L.Poff[i] + L.Prow[i][j - j0] * es), klen, X.rd[i], L.Pld[i]});
+          sb = B.input(Y.inner[static_cast<size_t>(i) * Y.nc + j], true);
         }
         if (klen > 0) B.fl_dense += 2.0 * X.rd[i] * static_cast<double>(Y.cd[j]) * klen;
       }
@@ -790,16 +816,14 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
           std::vector<Seg> sg;
           for (size_t pi = 0; pi < parts.size(); ++pi)
             if (parts[pi].v.cols > 0)
-              sg.push_back(Builder::seg(am[pi], bm[pi], true, false, mt * kBM, L.colT[j - j0] + nt * bn,
-                                        parts[pi].v.cols));
-          if (klen > 0) sg.push_back(Builder::seg(sm, zm, smn, zmn, mt * kBM, nt * bn, klen));
+              sg.push_back(Builder::seg(am[pi], bm[pi], mt * kBM, L.colT[j - j0] + nt * bn, parts[pi].v.cols));
+          if (klen > 0) sg.push_back(Builder::seg(sa, sb, mt * kBM, nt * bn, klen));
           B.emit(outC, X.ro[i] + mt * kBM, Y.co[j] + nt * bn, std::min<int64_t>(kBM, X.rd[i] - mt * kBM),
                  std::min<int64_t>(bn, Y.cd[j] - nt * bn), sg, {});
         }
     }
   }
-  (void)segs;
-  (void)pieces;
+  B.fl_launch[2] += B.fl_s3 + B.fl_dense - before3;
 }
 
 // Sort a launch's tasks by decreasing K so the persistent CTAs finish together.
@@ -851,6 +875,9 @@ struct tlr_plan_s {
   std::vector<const float *> round_src;
   std::vector<float *> round_dst;
   std::vector<int64_t> round_n;
+  const TJob *d_tjobs = nullptr;
+  int ntjobs = 0;
+  int64_t ttiles = 0;
   tlr_plan_info_t info{};
 };
 
@@ -900,8 +927,8 @@ void collect_round(const Operand &o, bool tf32, uint64_t ws, int64_t &off, std::
   if (d.kind == TLR_KIND_DENSE) {
     const int64_t ne = d.ld * d.cols;
     if (tf32) {
-      out.a[0] = ws ? ws + static_cast<uint64_t>(off) : 0;
-      if (ws) { src.push_back(static_cast<const float *>(d.data)); dst.push_back(reinterpret_cast<float *>(out.a[0])); cnt.push_back(ne); }
+      out.a[0] = ws + static_cast<uint64_t>(off);
+      src.push_back(static_cast<const float *>(d.data)); dst.push_back(reinterpret_cast<float *>(out.a[0])); cnt.push_back(ne);
       off = align_up(off + ne * 4, 256);
     } else {
       out.a[0] = reinterpret_cast<uint64_t>(d.data);
@@ -909,21 +936,32 @@ void collect_round(const Operand &o, bool tf32, uint64_t ws, int64_t &off, std::
     return;
   }
   for (int b = 0; b < 8; ++b) {
-    if (!tf32 || n[b] == 0 || !ptrs[b]) { out.a[b] = reinterpret_cast<uint64_t>(ptrs[b]); continue; }
-    out.a[b] = ws ? ws + static_cast<uint64_t>(off) : 0;
-    if (ws) { src.push_back(static_cast<const float *>(ptrs[b])); dst.push_back(reinterpret_cast<float *>(out.a[b])); cnt.push_back(n[b]); }
+    if (!tf32 || n[b] == 0) { out.a[b] = reinterpret_cast<uint64_t>(ptrs[b]); continue; }
+    // the rounded copy's place is fixed even when sizing without buffers
+    out.a[b] = ws + static_cast<uint64_t>(off);
+    src.push_back(static_cast<const float *>(ptrs[b])); dst.push_back(reinterpret_cast<float *>(out.a[b])); cnt.push_back(n[b]);
     off = align_up(off + n[b] * 4, 256);
   }
 }
+
+struct TJobHost {
+  uint64_t src, dst;
+  int64_t src_ld, dst_ld, rows, cols;
+};
 
 struct PlanCore {
   ProblemViews pv;
   LOp XR, YR;     // right order:  op(A) * op(B)
   LOp XL, YL;     // left order:   op(B)^T * op(A)^T  (transposed output)
   bool can_right = true, can_left = true;
-  int64_t fixed = 0;   // workspace taken by rounded input copies
+  int64_t fixed = 0;   // workspace taken by tf32-rounded and transposed input copies
   int nI = 0, nJ = 0;  // tile grid of C
   std::vector<int64_t> Crd, Ccd;
+  std::vector<const float *> round_src;
+  std::vector<float *> round_dst;
+  std::vector<int64_t> round_n;
+  std::map<ViewKey, View> tcopy;       // input view -> K-major transposed copy
+  std::vector<TJobHost> tjobs;
 };
 
 void bind_operand(Operand &o, const Bases &b) {
@@ -931,21 +969,56 @@ void bind_operand(Operand &o, const Bases &b) {
   bind(o, b.a[0], b.a[1], b.a[2], b.a[3], b.a[4], b.a[5], b.a[6], b.a[7]);
 }
 
+int choose_bn(const PlanCore &pc);
+void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vector<Task> &l2,
+                std::vector<Task> &l3);
+
+// TF32 products read every operand K-major. Find the input views some order
+// would read MN-major (a dry build of the whole of C in each order) and give
+// each a transposed copy after the rounded copies.
+void collect_copies(PlanCore &pc, uint64_t ws) {
+  std::set<ViewKey> need;
+  const int es = elem_size(pc.pv.dtype);
+  for (int order = 0; order < 2; ++order) {
+    const bool left = order == 1;
+    if ((left && !pc.can_left) || (!left && !pc.can_right)) continue;
+    const LOp &X = left ? pc.XL : pc.XR;
+    const LOp &Y = left ? pc.YL : pc.YR;
+    std::vector<CUtensorMap> maps;
+    std::map<std::tuple<uint64_t, int64_t, int64_t, int64_t, int>, int> mi;
+    std::vector<Seg> segs;
+    std::vector<Piece> pieces;
+    std::vector<Out> outs;
+    RectLayout L = layout_rect(X, Y, 0, X.nr, 0, Y.nc, es);
+    Builder B{X, Y, es, true, choose_bn(pc), left, ws, &maps, &mi, nullptr, &segs, &pieces, &outs};
+    B.dry = true;
+    B.need_copy = &need;
+    std::vector<Task> l1, l2, l3;
+    build_rect(B, L, l1, l2, l3);
+  }
+  int64_t off = pc.fixed;
+  for (const ViewKey &k : need) {
+    const uint64_t addr = std::get<0>(k);
+    const int64_t rows = std::get<1>(k), cols = std::get<2>(k), ld = std::get<3>(k);
+    const int64_t dld = align_up(cols, 4);
+    const uint64_t dst = ws + static_cast<uint64_t>(off);
+    pc.tcopy[k] = View{dst, cols, rows, dld};
+    pc.tjobs.push_back(TJobHost{addr, dst, ld, dld, rows, cols});
+    off = align_up(off + dld * rows * 4, 256);
+  }
+  pc.fixed = off;
+}
+
 tlr_status_t core_init(PlanCore &pc, tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A,
-                       const tlr_operand_t *B, bool check_pointers, uint64_t ws,
-                       std::vector<const float *> *rsrc, std::vector<float *> *rdst, std::vector<int64_t> *rn) {
+                       const tlr_operand_t *B, bool check_pointers, uint64_t ws) {
   tlr_status_t st = prepare(opA, opB, A, B, pc.pv, check_pointers);
   if (st) return st;
   const bool tf32 = pc.pv.dtype == TLR_F32;
-  std::vector<const float *> s;
-  std::vector<float *> d;
-  std::vector<int64_t> n;
   Bases ba{}, bb{};
   int64_t off = 0;
-  collect_round(pc.pv.A, tf32, ws, off, s, d, n, ba);
-  collect_round(pc.pv.B, tf32, ws, off, s, d, n, bb);
+  collect_round(pc.pv.A, tf32, ws, off, pc.round_src, pc.round_dst, pc.round_n, ba);
+  collect_round(pc.pv.B, tf32, ws, off, pc.round_src, pc.round_dst, pc.round_n, bb);
   pc.fixed = off;
-  if (rsrc) { *rsrc = s; *rdst = d; *rn = n; }
   bind_operand(pc.pv.A, ba);
   bind_operand(pc.pv.B, bb);
   const bool tA = opA == TLR_OP_T, tB = opB == TLR_OP_T;
@@ -954,13 +1027,11 @@ tlr_status_t core_init(PlanCore &pc, tlr_op_t opA, tlr_op_t opB, const tlr_opera
   pc.can_left = !pc.pv.dense_right;
   if (pc.can_right) { pc.XR = logical(pc.pv.A, tA, pb); pc.YR = logical(pc.pv.B, tB, pb); }
   if (pc.can_left) { pc.XL = logical(pc.pv.B, !tB, pb); pc.YL = logical(pc.pv.A, !tA, pb); }
-  const LOp &X = pc.can_right ? pc.XR : pc.YL;   // op(A) geometry
-  const LOp &Y = pc.can_right ? pc.YR : pc.XL;   // op(B)^T geometry when left-only
   if (pc.can_right) { pc.Crd = pc.XR.rd; pc.Ccd = pc.YR.cd; }
   else { pc.Crd = pc.YL.cd; pc.Ccd = pc.XL.rd; }
-  (void)X; (void)Y;
   pc.nI = static_cast<int>(pc.Crd.size());
   pc.nJ = static_cast<int>(pc.Ccd.size());
+  if (tf32) collect_copies(pc, ws);
   return TLR_STATUS_OK;
 }
 
@@ -1066,8 +1137,9 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, ui
     Builder B{X, Y, es, tf32, tb.bn, r.left, arena, &tb.maps, &tb.map_index, nullptr, &tb.segs, &tb.pieces, &tb.outs};
     B.dry = dry;
     B.views = &tb.views;
+    B.tcopy = &pc.tcopy;
     std::vector<Task> l1, l2, l3;
-    build_rect(B, L, l1, l2, l3, tb.segs, tb.pieces);
+    build_rect(B, L, l1, l2, l3);
     if (B.status) return B.status;
     sort_by_work(l1, tb.segs);
     sort_by_work(l2, tb.segs);
@@ -1088,6 +1160,7 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, ui
     info.flops_stage2 += B.fl_s2;
     info.flops_stage3 += B.fl_s3;
     info.flops_dense_terms += B.fl_dense;
+    for (int q = 0; q < 3; ++q) info.flops_launch[q] += B.fl_launch[q];
     if (pc.can_right) info.flops_right_final += rect_cost(pc, r.i0, r.i1, r.j0, r.j1, false);
     if (pc.can_left) info.flops_left_final += rect_cost(pc, r.i0, r.i1, r.j0, r.j1, true);
   }
@@ -1127,8 +1200,18 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
     for (const View &v : s.diag) if (v.rows > 0) regs.push_back(Region{v.addr, v.ld * v.cols * es});
   }
   char buf[256];
+  const bool tf32 = pc.pv.dtype == TLR_F32;
+  for (size_t q = 0; q < pc.tjobs.size(); ++q) {
+    const TJobHost &j = pc.tjobs[q];
+    if (!inside(regs, j.src, ((j.cols - 1) * j.src_ld + j.rows) * es) ||
+        j.dst < ws || j.dst + static_cast<uint64_t>(j.dst_ld * j.rows * es) > ws + static_cast<uint64_t>(pc.fixed)) {
+      snprintf(buf, sizeof buf, "transposed copy %zu outside its buffers", q);
+      return buf;
+    }
+  }
   for (size_t m = 0; m < tb.views.size(); ++m) {
     const View &v = tb.views[m].first;
+    if (tf32 && tb.views[m].second) { snprintf(buf, sizeof buf, "map %zu: TF32 operand read MN-major", m); return buf; }
     if (v.rows <= 0 || v.cols <= 0 || v.ld < v.rows || (v.ld * es) % 16 || (v.addr & 15u)) {
       snprintf(buf, sizeof buf, "map %zu: bad view rows=%lld cols=%lld ld=%lld", m, (long long)v.rows, (long long)v.cols, (long long)v.ld);
       return buf;
@@ -1314,7 +1397,7 @@ tlr_status_t tlr_analyze(tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A, con
   if (!out || !A || !B) return TLR_STATUS_INVALID_ARG;
   if (A->kind != TLR_KIND_TLR || B->kind != TLR_KIND_TLR) return TLR_STATUS_UNSUPPORTED;
   PlanCore pc;
-  tlr_status_t st = core_init(pc, opA, opB, A, B, false, 0, nullptr, nullptr, nullptr);
+  tlr_status_t st = core_init(pc, opA, opB, A, B, false, 0);
   if (st) return st;
   const LOp &X = pc.XR, &Y = pc.YR;
   out->nt_i = X.nr; out->nt_k = X.nc; out->nt_j = Y.nc;
@@ -1368,7 +1451,7 @@ tlr_status_t tlr_gemm_workspace_bytes(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB
   (void)h;
   if (!bytes) return TLR_STATUS_INVALID_ARG;
   PlanCore pc;
-  tlr_status_t st = core_init(pc, opA, opB, A, B, false, 0, nullptr, nullptr, nullptr);
+  tlr_status_t st = core_init(pc, opA, opB, A, B, false, 0);
   if (st) return st;
   const int es = elem_size(pc.pv.dtype);
   if (runs <= 0) runs = 1;
@@ -1399,10 +1482,7 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TLR_STATUS_ALIGNMENT;
   const uint64_t ws = reinterpret_cast<uint64_t>(workspace);
   PlanCore pc;
-  std::vector<const float *> rs;
-  std::vector<float *> rd;
-  std::vector<int64_t> rn;
-  tlr_status_t st = core_init(pc, opA, opB, A, B, true, ws ? ws : 1, &rs, &rd, &rn);
+  tlr_status_t st = core_init(pc, opA, opB, A, B, true, ws ? ws : 256);
   if (st) return st;
   const int es = elem_size(pc.pv.dtype);
   const bool tf32 = pc.pv.dtype == TLR_F32;
@@ -1417,9 +1497,9 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
   p->tf32 = tf32;
   p->Cm = pc.pv.Cm;
   p->Cn = pc.pv.Cn;
-  p->round_src = rs;
-  p->round_dst = rd;
-  p->round_n = rn;
+  p->round_src = pc.round_src;
+  p->round_dst = pc.round_dst;
+  p->round_n = pc.round_n;
   p->bn = choose_bn(pc);
 
   Tables tb;
@@ -1444,14 +1524,28 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
   const size_t szs = align_up(static_cast<int64_t>(segs.size() * sizeof(Seg)), 256);
   const size_t szp = align_up(static_cast<int64_t>(pieces.size() * sizeof(Piece)), 256);
   const size_t szo = align_up(static_cast<int64_t>(outs.size() * sizeof(Out)), 256);
+  std::vector<TJob> tj;
+  int64_t tiles = 0;
+  for (const TJobHost &j : pc.tjobs) {
+    TJob d;
+    memset(&d, 0, sizeof d);
+    d.src = reinterpret_cast<const float *>(j.src);
+    d.dst = reinterpret_cast<float *>(j.dst);
+    d.src_ld = j.src_ld; d.dst_ld = j.dst_ld; d.rows = j.rows; d.cols = j.cols; d.tile0 = tiles;
+    tiles += ceil_div(j.rows, 32) * ceil_div(j.cols, 32);
+    tj.push_back(d);
+  }
+  const size_t szj = align_up(static_cast<int64_t>(tj.size() * sizeof(TJob)), 256);
   const size_t om = 0, ot = align_up(static_cast<int64_t>(szm), 256), os = ot + szt, op = os + szs, oo = op + szp;
-  const size_t total = oo + szo + 256;
+  const size_t oj = oo + szo;
+  const size_t total = oj + szj + 256;
   std::vector<uint8_t> host(total, 0);
   if (szm) memcpy(host.data() + om, maps.data(), szm);
   if (!all.empty()) memcpy(host.data() + ot, all.data(), all.size() * sizeof(Task));
   if (!segs.empty()) memcpy(host.data() + os, segs.data(), segs.size() * sizeof(Seg));
   if (!pieces.empty()) memcpy(host.data() + op, pieces.data(), pieces.size() * sizeof(Piece));
   if (!outs.empty()) memcpy(host.data() + oo, outs.data(), outs.size() * sizeof(Out));
+  if (!tj.empty()) memcpy(host.data() + oj, tj.data(), tj.size() * sizeof(TJob));
   if (cudaMallocAsync(&p->d_tables, total, h->stream) != cudaSuccess) { cudaGetLastError(); delete p; return TLR_STATUS_CUDA_ERROR; }
   if (cudaMemcpyAsync(p->d_tables, host.data(), total, cudaMemcpyHostToDevice, h->stream) != cudaSuccess ||
       cudaStreamSynchronize(h->stream) != cudaSuccess) {
@@ -1465,6 +1559,9 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
   p->d_segs = reinterpret_cast<const Seg *>(dt + os);
   p->d_pieces = reinterpret_cast<const Piece *>(dt + op);
   p->d_outs = reinterpret_cast<const Out *>(dt + oo);
+  p->d_tjobs = reinterpret_cast<const TJob *>(dt + oj);
+  p->ntjobs = static_cast<int>(tj.size());
+  p->ttiles = tiles;
   *plan_out = p;
   return TLR_STATUS_OK;
 }
@@ -1475,7 +1572,7 @@ tlr_status_t tlr_debug_check_plan(tlr_op_t opA, tlr_op_t opB, const tlr_operand_
   if (msg && msg_len) msg[0] = 0;
   const uint64_t ws = 0x100000000000ull;   // a stand-in address: nothing is dereferenced
   PlanCore pc;
-  tlr_status_t st = core_init(pc, opA, opB, A, B, true, ws, nullptr, nullptr, nullptr);
+  tlr_status_t st = core_init(pc, opA, opB, A, B, true, ws);
   if (st) return st;
   const int es = elem_size(pc.pv.dtype);
   std::vector<Rect> rects;
@@ -1519,6 +1616,9 @@ tlr_status_t tlr_plan_execute(tlr_plan_t p, float alpha, float beta, float *C, i
     if (record_start(h, kKindRound, ev) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
     cudaError_t e = launch_round_tf32(p->round_src.data(), p->round_dst.data(), p->round_n.data(),
                                       static_cast<int>(p->round_n.size()), 4 * sms, h->stream);
+    if (e == cudaSuccess)
+      e = launch_transpose_round(p->d_tjobs, p->ntjobs, p->ttiles,
+                                 static_cast<int>(std::min<int64_t>(p->ttiles, 16 * sms)), h->stream);
     if (e != cudaSuccess || record_stop(h, ev) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
   }
   Params prm;

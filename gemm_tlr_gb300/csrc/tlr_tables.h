@@ -70,6 +70,16 @@ struct alignas(16) Task {
   int64_t row0, col0;     // output coordinates of the tile origin
 };
 
+// One transposed input copy for the TF32 path: dst[c + r * dst_ld] =
+// round_tf32(src[r + c * src_ld]) for r < rows, c < cols; tile0 is the first
+// 32 x 32 tile of this job in the launch's tile numbering.
+struct alignas(16) TJob {
+  const float *src;
+  float *dst;
+  int64_t src_ld, dst_ld, rows, cols, tile0;
+  int64_t pad_;
+};
+
 struct Params {
   const void *maps;       // CUtensorMap[], 64-byte aligned, device memory
   const Task *tasks;

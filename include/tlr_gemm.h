@@ -111,6 +111,8 @@ typedef struct tlr_plan_info {
     double flops_right_final, flops_left_final;  /* F_R and F_L summed over the rectangles */
     size_t workspace_bytes;       /* bytes of the caller's workspace the plan uses */
     int64_t tasks;                /* output tiles over all launches */
+    double flops_launch[3];       /* per execution, by launch class: [0] Stage 1 with the
+                                     dense-tile precomputes, [1] Stage 2, [2] Stage 3 */
 } tlr_plan_info_t;
 
 /* Metadata of a TLR x TLR product computed from ranks alone (no device use).
