@@ -12,11 +12,15 @@
 // "One product, three stages" and "Where fusion stops"; the dense-diagonal
 // terms follow "TLR Matrix Multiplication", section "Regular TLR GEMM").
 //
-// Roles (192 threads, one CTA per SM):
+// Roles (224 threads, one CTA per SM):
 //   warp 0       TMA producer: 4-stage shared-memory ring, 128-byte swizzle
 //   warp 1       tcgen05.mma issuer (M = 128, N = BN, fp32 accumulators in TMEM,
 //                two accumulators so the epilogue of tile t overlaps tile t+1)
-//   warps 2..5   epilogue: tcgen05.ld, alpha/beta, coalesced column-major stores
+//   warp 2       descriptors: stages each task's segments, output descriptor and
+//                per-row destinations in a shared-memory ring, kRing tasks ahead
+//   warps 3..    epilogue, kEpiGroups groups of four warps: tcgen05.ld, alpha/beta,
+//                coalesced column-major stores; group g takes 32-column chunks
+//                g, g + kEpiGroups, ... so more stores are in flight per SM
 // Every mbarrier wait is bounded (globaltimer); on timeout the CTA raises a flag
 // in the device error word, drains its own copies and MMAs, frees TMEM, exits.
 #include <cuda.h>
@@ -183,6 +187,17 @@ __device__ __forceinline__ float round_tf32(float x) {
 }
 
 // ------------------------------------------------------------------ the GEMM
+// One staged task in shared memory (written by the descriptor warp).
+struct Slot {
+  Task task;                 // 48 B
+  Out out;                   // 32 B
+  int32_t pad_[4];
+  Seg segs[kMaxSegs];        // at 96
+  int64_t pad2_[4];
+  int64_t rowdst[kBM];       // at 256: output row of each tile row, -1 when the row is not stored
+};
+static_assert(sizeof(Slot) <= kSlotBytes, "slot size");
+
 template <bool kTF32>
 __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_constant__ Params p) {
   constexpr int kElt = kTF32 ? 4 : 2;
@@ -194,18 +209,23 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *base_ptr = smem_raw + (base - raw);
-  const uint32_t bars = base + kStages * kStageBytes;
+  Slot *ring = reinterpret_cast<Slot *>(base_ptr + kStages * kStageBytes);
+  const uint32_t bars = base + kStages * kStageBytes + kRing * kSlotBytes;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
   auto tfull_bar = [&](int a) { return bars + 8u * (2 * kStages + a); };
   auto tempty_bar = [&](int a) { return bars + 8u * (2 * kStages + 2 + a); };
   const uint32_t drain_bar = bars + 8u * (2 * kStages + 4);
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + kStages * kStageBytes + 8 * (2 * kStages + 5));
+  auto sfull_bar = [&](int r) { return bars + 8u * (2 * kStages + 5 + r); };
+  auto sempty_bar = [&](int r) { return bars + 8u * (2 * kStages + 5 + kRing + r); };
+  uint32_t *tmem_holder =
+      reinterpret_cast<uint32_t *>(base_ptr + kStages * kStageBytes + kRing * kSlotBytes + 8 * (2 * kStages + 5 + 2 * kRing));
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bn = p.bn;
+  const int my_tasks = blockIdx.x < p.ntasks ? (p.ntasks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -214,7 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 128);
+      mbar_init(tempty_bar(a), kEpiThreads);
+    }
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(sfull_bar(r), 1);
+      mbar_init(sempty_bar(r), 2 + 4 * kEpiGroups);   // producer, MMA issuer, every epilogue warp
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -233,17 +257,50 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
   const uint32_t tmem_base = *tmem_holder;
   const char *maps = reinterpret_cast<const char *>(p.maps);
 
-  if (warp == 0) {
+  if (warp == 2) {
+    // ---------------------------------------------------------------- descriptors
+    // Stage task n of this CTA into ring slot n % kRing, up to kRing tasks ahead.
+    for (int n = 0; n < my_tasks; ++n) {
+      const int r = n % kRing;
+      const uint32_t ph = (n / kRing) & 1;
+      bool ok = true;
+      if (lane == 0) ok = wait_bounded(sempty_bar(r), ph ^ 1u, abort_flag, p, 5);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      Slot &sl = ring[r];
+      const Task task = p.tasks[blockIdx.x + static_cast<int64_t>(n) * gridDim.x];
+      if (lane == 0) { sl.task = task; sl.out = p.outs[task.out]; }
+      if (lane < task.nseg) sl.segs[lane] = p.segs[task.seg0 + lane];
+      for (int row = lane; row < kBM; row += 32) {
+        int64_t d = -1;
+        if (row < task.rows) {
+          if (task.npiece == 0) {
+            d = task.row0 + row;
+          } else {
+            for (int pc = 0; pc < task.npiece; ++pc) {
+              const Piece pe = p.pieces[task.piece0 + pc];
+              if (row >= pe.src0 && row < pe.src0 + pe.len) { d = pe.dst0 + (row - pe.src0); break; }
+            }
+          }
+        }
+        sl.rowdst[row] = d;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfull_bar(r));
+    }
+  } else if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_phase_mask = 0;   // per stage: copy issued / its phase
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.ntasks; t += gridDim.x) {
-        const Task task = p.tasks[t];
-        for (int s = 0; ok && s < task.nseg; ++s) {
-          const Seg sg = p.segs[task.seg0 + s];
+      for (int n = 0; ok && n < my_tasks; ++n) {
+        const int r = n % kRing;
+        if (!wait_bounded(sfull_bar(r), (n / kRing) & 1, abort_flag, p, 6)) break;
+        const Slot &sl = ring[r];
+        const int nseg = sl.task.nseg;
+        for (int s = 0; ok && s < nseg; ++s) {
+          const Seg sg = sl.segs[s];
           const void *ma = maps + 128 * static_cast<size_t>(sg.a_map);
           const void *mb = maps + 128 * static_cast<size_t>(sg.b_map);
           const int nkb = (sg.k_len + kBK - 1) / kBK;
@@ -274,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
           }
         }
+        mbar_arrive(sempty_bar(r));
       }
       // Every copy this thread issued must land before the CTA may exit.
       for (int s = 0; s < kStages; ++s)
@@ -287,14 +345,17 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.ntasks; t += gridDim.x) {
-        const Task task = p.tasks[t];
+      for (int n = 0; ok && n < my_tasks; ++n) {
+        const int r = n % kRing;
+        if (!wait_bounded(sfull_bar(r), (n / kRing) & 1, abort_flag, p, 7)) break;
+        const Slot &sl = ring[r];
+        const int nseg = sl.task.nseg;
         if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p, 2)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kMaxBN);
         uint32_t accumulate = 0;
-        for (int s = 0; ok && s < task.nseg; ++s) {
-          const Seg sg = p.segs[task.seg0 + s];
+        for (int s = 0; ok && s < nseg; ++s) {
+          const Seg sg = sl.segs[s];
           const bool a_mn = sg.flags & kSegAMN, b_mn = sg.flags & kSegBMN;
           const uint32_t id = idesc(kTF32, a_mn, b_mn, static_cast<uint32_t>(bn));
           const int nkb = (sg.k_len + kBK - 1) / kBK;
@@ -319,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
           }
         }
+        mbar_arrive(sempty_bar(r));
         if (!ok) break;
         if (accumulate) mma_commit(tfull_bar(acc));
         else mbar_arrive(tfull_bar(acc));
@@ -332,31 +394,26 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;               // TMEM lanes 32q..32q+31 belong to this warp
     const int row = q * 32 + lane;        // accumulator row held by this thread
+    const int grp = (warp - 3) >> 2;      // epilogue group: its share of the column chunks
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < p.ntasks; t += gridDim.x) {
-      const Task task = p.tasks[t];
+    for (int n = 0; n < my_tasks; ++n) {
+      const int r = n % kRing;
+      if (!wait_bounded(sfull_bar(r), (n / kRing) & 1, abort_flag, p, 8)) break;
+      const Slot &sl = ring[r];
+      const int64_t drow = sl.rowdst[row];
+      const bool valid = drow >= 0;
+      const int ncols = sl.task.cols;
+      const bool has_acc = sl.task.nseg > 0;
+      const int64_t col0 = sl.task.col0;
+      const Out o = sl.out;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sempty_bar(r));
       if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p, 4)) break;
       tc_fence_after();
-      const Out o = p.outs[task.out];
-      bool valid = row < task.rows;
-      int64_t drow = task.row0 + row;
-      if (task.npiece > 0) {
-        valid = false;
-        for (int pc = 0; pc < task.npiece; ++pc) {
-          const Piece pe = p.pieces[task.piece0 + pc];
-          if (row >= pe.src0 && row < pe.src0 + pe.len) {
-            drow = pe.dst0 + (row - pe.src0);
-            valid = true;
-            break;
-          }
-        }
-      }
-      const int ncols = task.cols;
-      const bool has_acc = task.nseg > 0;
       const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                               static_cast<uint32_t>(acc * kMaxBN);
-      for (int cc = 0; cc < ncols; cc += 32) {
+      for (int cc = 32 * grp; cc < ncols; cc += 32 * kEpiGroups) {
         float v[32];
         if (has_acc) {
           tmem_ld32(t_addr + cc, v);
@@ -364,16 +421,48 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
-        if (!valid) continue;
         const int nc = ncols - cc < 32 ? ncols - cc : 32;
+        const int64_t c0 = col0 + cc;
+        if (o.kind == kOutC && o.trans) {
+          // Output tile element (r, c) goes to C[c + r * ldc]. Transpose the warp's
+          // 32 x 32 block across lanes (XOR butterfly) so that lane i holds tile
+          // column c0 + i for the warp's 32 rows; every store then writes 32
+          // consecutive floats of one column of C.
+#pragma unroll
+          for (int sh = 16; sh > 0; sh >>= 1) {
+            const bool upper = (lane & sh) != 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (j & sh) continue;
+              const float send = upper ? v[j] : v[j | sh];
+              const float recv = __shfl_xor_sync(0xffffffffu, send, sh);
+              if (upper) v[j] = recv;
+              else v[j | sh] = recv;
+            }
+          }
+          float *C = p.C;
+          const int64_t ld = p.ldc;
+          const bool cok = lane < nc;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int64_t dj = __shfl_sync(0xffffffffu, valid ? drow : int64_t(-1), j);
+            if (cok && dj >= 0) {
+              const int64_t off = (c0 + lane) + dj * ld;
+              float val = p.alpha * v[j];
+              if (p.beta != 0.f) val = fmaf(p.beta, C[off], val);
+              C[off] = val;
+            }
+          }
+          continue;
+        }
+        if (!valid) continue;
         if (o.kind == kOutC) {
           float *C = p.C;
           const int64_t ld = p.ldc;
-          const int64_t c0 = task.col0 + cc;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             if (i < nc) {
-              const int64_t off = o.trans ? (c0 + i) + drow * ld : drow + (c0 + i) * ld;
+              const int64_t off = drow + (c0 + i) * ld;
               float val = p.alpha * v[i];
               if (p.beta != 0.f) val = fmaf(p.beta, C[off], val);
               C[off] = val;
@@ -381,13 +470,11 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
           }
         } else if (o.kind == kOutBF16) {
           __nv_bfloat16 *W = static_cast<__nv_bfloat16 *>(o.ptr);
-          const int64_t c0 = task.col0 + cc;
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (i < nc) W[o.trans ? (c0 + i) + drow * o.ld : drow + (c0 + i) * o.ld] = __float2bfloat16_rn(v[i]);
         } else {
           float *W = static_cast<float *>(o.ptr);
-          const int64_t c0 = task.col0 + cc;
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (i < nc) W[o.trans ? (c0 + i) + drow * o.ld : drow + (c0 + i) * o.ld] = round_tf32(v[i]);

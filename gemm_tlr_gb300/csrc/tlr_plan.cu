@@ -1224,7 +1224,7 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
   double carea = 0;
   for (size_t ti = 0; ti < tb.all.size(); ++ti) {
     const Task &t = tb.all[ti];
-    if (t.rows < 1 || t.rows > kBM || t.cols < 1 || t.cols > tb.bn) { snprintf(buf, sizeof buf, "task %zu: bad extent", ti); return buf; }
+    if (t.rows < 1 || t.rows > kBM || t.cols < 1 || t.cols > tb.bn || t.nseg > kMaxSegs) { snprintf(buf, sizeof buf, "task %zu: bad extent or segment count", ti); return buf; }
     for (int q = 0; q < t.nseg; ++q) {
       const Seg &g = tb.segs[t.seg0 + q];
       if (g.k_len <= 0 || g.a_map < 0 || g.b_map < 0 || g.a_map >= (int)tb.views.size() || g.b_map >= (int)tb.views.size()) {

@@ -23,9 +23,17 @@ constexpr int kStages = 4;          // shared-memory pipeline depth
 constexpr int kSmemA = kBM * 128;   // one stage of A: 128 rows x 128 bytes
 constexpr int kSmemB = kMaxBN * 128;
 constexpr int kStageBytes = kSmemA + kSmemB;
-constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+#ifndef TLR_EPI_GROUPS
+#define TLR_EPI_GROUPS 2
+#endif
+constexpr int kEpiGroups = TLR_EPI_GROUPS;   // epilogue warp groups; each stores every kEpiGroups-th 32-column chunk
+constexpr int kEpiThreads = 128 * kEpiGroups;
+constexpr int kThreads = 96 + kEpiThreads;   // warp 0 TMA, warp 1 MMA, warp 2 descriptors, then the epilogue
 constexpr int kTmemCols = 512;      // two accumulators of up to 256 fp32 columns
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kMaxSegs = 4;         // K segments per task
+constexpr int kRing = 8;            // task descriptors staged ahead in shared memory
+constexpr int kSlotBytes = 1536;    // one staged task: header, segments, per-row destinations
+constexpr int kSmemBytes = kStages * kStageBytes + kRing * kSlotBytes + 1024 /*align*/ + 512 /*barriers*/;
 
 enum : uint32_t {
   kSegAMN = 1u,   // A operand MN-major (rows of its view are M); else K-major
