@@ -470,9 +470,29 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
           }
         } else if (o.kind == kOutBF16) {
           __nv_bfloat16 *W = static_cast<__nv_bfloat16 *>(o.ptr);
+          if (o.trans) {
+            // row-major output: this thread's 32 values are 64 contiguous bytes of one row
+            __nv_bfloat16 *dst = W + drow * o.ld + c0;
+            if (nc == 32) {
+              uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i < nc) W[o.trans ? (c0 + i) + drow * o.ld : drow + (c0 + i) * o.ld] = __float2bfloat16_rn(v[i]);
+              for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                pk[i] = *reinterpret_cast<const uint32_t *>(&h2);
+              }
+              uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < nc) dst[i] = __float2bfloat16_rn(v[i]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nc) W[drow + (c0 + i) * o.ld] = __float2bfloat16_rn(v[i]);
+          }
         } else {
           float *W = static_cast<float *>(o.ptr);
 #pragma unroll

@@ -484,12 +484,12 @@ struct Builder {
     return ORef{map_of(View{c.addr + static_cast<uint64_t>((kk0 + n0 * c.ld) * es), kl, nl, c.ld}, false), false};
   }
 
-  int out_ws(uint64_t ptr, int64_t ld) {
+  int out_ws(uint64_t ptr, int64_t ld, bool trans = false) {
     Out o;
     o.ptr = reinterpret_cast<void *>(ptr);
     o.ld = ld;
     o.kind = tf32 ? kOutTF32 : kOutBF16;
-    o.trans = 0;
+    o.trans = trans ? 1 : 0;
     outs->push_back(o);
     return static_cast<int>(outs->size()) - 1;
   }
@@ -536,7 +536,9 @@ struct Builder {
 // Workspace layout of one rectangle (right order on X * Y).
 //   S_k^T   (Gamma_k(J) padded) x sigma_k(I): Stage-1 output, the column block of
 //           tile j starts on a 16-byte boundary so Stage 2 reads it K-major;
-//   T       rows of T_i (parts padded to 8) x W_J columns, column-major;
+//   T       rows of T_i (parts padded to 8) x W_J columns; row-major for bf16
+//           (a Stage-2 thread writes contiguous runs of one row, Stage 3 reads it
+//           MN-major), column-major for tf32 (TF32 operands are read K-major);
 //   P_i^T   (Gamma_i(J) padded) x d_i: (D_ii W_{i,J})^T, blocks aligned like S.
 struct RectLayout {
   int i0, i1, j0, j1;
@@ -546,7 +548,9 @@ struct RectLayout {
   std::vector<std::vector<int64_t>> Srow;    // per k, per j: first row of block j in S_k^T
   std::vector<int64_t> R;                    // per i: first T row
   std::vector<std::vector<int64_t>> Toff;    // per i, per part: first T row of the part
-  int64_t Tld = 0, Toffset = 0;
+  int64_t Tld = 0, Toffset = 0;              // Tld: leading dimension of T's storage
+  bool Trow = false;                         // T stored row-major (element (r, c) at c + r * Tld)
+  int64_t Trows = 0;
   std::vector<int64_t> Poff, Pld;            // per i
   std::vector<std::vector<int64_t>> Prow;    // per i, per j
   int64_t bytes = 0;
@@ -554,6 +558,7 @@ struct RectLayout {
 
 RectLayout layout_rect(const LOp &X, const LOp &Y, int i0, int i1, int j0, int j1, int es) {
   RectLayout L;
+  L.Trow = es == 2;
   L.i0 = i0; L.i1 = i1; L.j0 = j0; L.j1 = j1;
   L.colT.assign(j1 - j0 + 1, 0);
   for (int j = j0; j < j1; ++j) L.colT[j - j0 + 1] = L.colT[j - j0] + Y.cd[j];
@@ -586,9 +591,15 @@ RectLayout layout_rect(const LOp &X, const LOp &Y, int i0, int i1, int j0, int j
       rows += align_up(p.v.cols, 8);
     }
   }
-  L.Tld = align_up(std::max<int64_t>(rows, 8), 8);
+  L.Trows = align_up(std::max<int64_t>(rows, 8), 8);
   L.Toffset = off;
-  off = align_up(off + L.Tld * L.WJ * es, 256);
+  if (L.Trow) {
+    L.Tld = align_up(L.WJ, 8);
+    off = align_up(off + L.Trows * L.Tld * es, 256);
+  } else {
+    L.Tld = L.Trows;
+    off = align_up(off + L.Tld * L.WJ * es, 256);
+  }
   L.Poff.assign(X.nr, -1);
   L.Pld.assign(X.nr, 0);
   L.Prow.assign(X.nr, {});
@@ -647,7 +658,7 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
   const int es = B.es, bn = B.bn;
   const int i0 = L.i0, i1 = L.i1, j0 = L.j0, j1 = L.j1;
   const uint64_t T = B.ws + static_cast<uint64_t>(L.Toffset);
-  const int outT = B.out_ws(T, L.Tld);
+  const int outT = B.out_ws(T, L.Tld, L.Trow);
   // T row of tile (i, k) of op(X)
   auto trow = [&](int i, int k) -> int64_t {
     const auto &parts = X.rowp[i];
@@ -789,7 +800,10 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
     for (size_t pi = 0; pi < parts.size(); ++pi) {
       if (parts[pi].v.cols <= 0) continue;
       am[pi] = B.input(parts[pi].v, true);
-      bm[pi] = B.work(View{T + static_cast<uint64_t>(L.Toff[i][pi] * es), parts[pi].v.cols, L.WJ, L.Tld});
+      if (L.Trow)   // MN-major B: view rows are T's columns (N), view columns its rows (K)
+        bm[pi] = ORef{B.map_of(View{T + static_cast<uint64_t>(L.Toff[i][pi] * L.Tld * es), L.WJ, parts[pi].v.cols, L.Tld}, true), true};
+      else
+        bm[pi] = B.work(View{T + static_cast<uint64_t>(L.Toff[i][pi] * es), parts[pi].v.cols, L.WJ, L.Tld});
       rho += parts[pi].v.cols;
     }
     B.fl_s3 += 2.0 * X.rd[i] * static_cast<double>(L.WJ) * rho;
@@ -1263,9 +1277,16 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
         rmin = std::min<int64_t>(rmin, pe.dst0);
         rmax = std::max<int64_t>(rmax, pe.dst0 + pe.len - 1);
       }
-      if (rmin < 0 || rmax >= o.ld) { snprintf(buf, sizeof buf, "task %zu: row beyond the leading dimension", ti); return buf; }
-      const uint64_t lo = base + static_cast<uint64_t>((rmin + t.col0 * o.ld) * es);
-      const uint64_t hi = base + static_cast<uint64_t>((rmax + (t.col0 + t.cols - 1) * o.ld + 1) * es);
+      uint64_t lo, hi;
+      if (o.trans) {   // element (r, c) at c + r * ld
+        if (rmin < 0 || t.col0 < 0 || t.col0 + t.cols > o.ld) { snprintf(buf, sizeof buf, "task %zu: column beyond the leading dimension", ti); return buf; }
+        lo = base + static_cast<uint64_t>((t.col0 + rmin * o.ld) * es);
+        hi = base + static_cast<uint64_t>((t.col0 + t.cols + rmax * o.ld) * es);
+      } else {
+        if (rmin < 0 || rmax >= o.ld) { snprintf(buf, sizeof buf, "task %zu: row beyond the leading dimension", ti); return buf; }
+        lo = base + static_cast<uint64_t>((rmin + t.col0 * o.ld) * es);
+        hi = base + static_cast<uint64_t>((rmax + (t.col0 + t.cols - 1) * o.ld + 1) * es);
+      }
       if (lo < ws + static_cast<uint64_t>(pc.fixed) || hi > ws + static_cast<uint64_t>(ws_bytes)) {
         snprintf(buf, sizeof buf, "task %zu: workspace write outside the arena", ti); return buf;
       }
