@@ -97,6 +97,39 @@ __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t 
   return true;
 }
 
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int *p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add(unsigned int *p, unsigned int v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Bounded wait for a dependency counter (written by other CTAs of this launch).
+__device__ __noinline__ bool wait_counter(const unsigned int *c, unsigned int target, volatile int *abort_flag,
+                                          const Params &p) {
+  if (ld_acquire(c) >= target) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire(c) >= target) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > p.wait_limit_ns) {
+        *abort_flag = 1;
+        atomicOr(p.err, 1u | (9u << 4));
+        return false;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int32_t x, int32_t y,
                                             uint32_t bar) {
   asm volatile(
@@ -218,14 +251,14 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
   const uint32_t drain_bar = bars + 8u * (2 * kStages + 4);
   auto sfull_bar = [&](int r) { return bars + 8u * (2 * kStages + 5 + r); };
   auto sempty_bar = [&](int r) { return bars + 8u * (2 * kStages + 5 + kRing + r); };
+  const uint32_t sig_bar = bars + 8u * (2 * kStages + 5 + 2 * kRing);   // epilogue stores published
   uint32_t *tmem_holder =
-      reinterpret_cast<uint32_t *>(base_ptr + kStages * kStageBytes + kRing * kSlotBytes + 8 * (2 * kStages + 5 + 2 * kRing));
+      reinterpret_cast<uint32_t *>(base_ptr + kStages * kStageBytes + kRing * kSlotBytes + 8 * (2 * kStages + 6 + 2 * kRing));
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bn = p.bn;
-  const int my_tasks = blockIdx.x < p.ntasks ? (p.ntasks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -241,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       mbar_init(sempty_bar(r), 2 + 4 * kEpiGroups);   // producer, MMA issuer, every epilogue warp
     }
     mbar_init(drain_bar, 1);
+    mbar_init(sig_bar, kEpiThreads);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -259,15 +293,36 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
 
   if (warp == 2) {
     // ---------------------------------------------------------------- descriptors
-    // Stage task n of this CTA into ring slot n % kRing, up to kRing tasks ahead.
-    for (int n = 0; n < my_tasks; ++n) {
+    // Claim the next ticket, wait for its dependencies, stage it in ring slot
+    // n % kRing (up to kRing tasks ahead of the consumers). A slot whose task
+    // has nseg < 0 tells the consumers that the launch has no more work.
+    for (int n = 0;; ++n) {
       const int r = n % kRing;
       const uint32_t ph = (n / kRing) & 1;
-      bool ok = true;
-      if (lane == 0) ok = wait_bounded(sempty_bar(r), ph ^ 1u, abort_flag, p, 5);
-      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
       Slot &sl = ring[r];
-      const Task task = p.tasks[blockIdx.x + static_cast<int64_t>(n) * gridDim.x];
+      int ok = 1;
+      unsigned int t = 0;
+      if (lane == 0) {
+        ok = wait_bounded(sempty_bar(r), ph ^ 1u, abort_flag, p, 5) ? 1 : 0;
+        if (ok) t = atomicAdd(p.ticket, 1u);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (!ok) break;
+      if (t >= static_cast<unsigned int>(p.ntasks)) {
+        if (lane == 0) {
+          sl.task.nseg = -1;
+          mbar_arrive(sfull_bar(r));
+        }
+        break;
+      }
+      const Task task = p.tasks[t];
+      if (lane == 0) {
+        for (int d = 0; d < 2 && ok; ++d)
+          if (task.dep[d] >= 0) ok = wait_counter(p.counters + task.dep[d], task.dep_target[d], abort_flag, p) ? 1 : 0;
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
       if (lane == 0) { sl.task = task; sl.out = p.outs[task.out]; }
       if (lane < task.nseg) sl.segs[lane] = p.segs[task.seg0 + lane];
       for (int row = lane; row < kBM; row += 32) {
@@ -294,11 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_phase_mask = 0;   // per stage: copy issued / its phase
       bool ok = true;
-      for (int n = 0; ok && n < my_tasks; ++n) {
+      for (int n = 0; ok; ++n) {
         const int r = n % kRing;
         if (!wait_bounded(sfull_bar(r), (n / kRing) & 1, abort_flag, p, 6)) break;
         const Slot &sl = ring[r];
         const int nseg = sl.task.nseg;
+        if (nseg < 0) break;
+        // operands written earlier in this launch by other CTAs are read through TMA
+        if (sl.task.dep[0] >= 0 || sl.task.dep[1] >= 0) fence_proxy_async_global();
         for (int s = 0; ok && s < nseg; ++s) {
           const Seg sg = sl.segs[s];
           const void *ma = maps + 128 * static_cast<size_t>(sg.a_map);
@@ -345,11 +403,12 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int n = 0; ok && n < my_tasks; ++n) {
+      for (int n = 0; ok; ++n) {
         const int r = n % kRing;
         if (!wait_bounded(sfull_bar(r), (n / kRing) & 1, abort_flag, p, 7)) break;
         const Slot &sl = ring[r];
         const int nseg = sl.task.nseg;
+        if (nseg < 0) break;
         if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p, 2)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kMaxBN);
@@ -397,10 +456,14 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
     const int grp = (warp - 3) >> 2;      // epilogue group: its share of the column chunks
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int n = 0; n < my_tasks; ++n) {
+    uint32_t sig_phase = 0;
+    for (int n = 0;; ++n) {
       const int r = n % kRing;
       if (!wait_bounded(sfull_bar(r), (n / kRing) & 1, abort_flag, p, 8)) break;
       const Slot &sl = ring[r];
+      if (sl.task.nseg < 0) break;
+      const int32_t signal = sl.task.signal;
+      const bool signal_writes = sl.task.signal_writes != 0;
       const int64_t drow = sl.rowdst[row];
       const bool valid = drow >= 0;
       const int ncols = sl.task.cols;
@@ -503,6 +566,18 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (signal >= 0) {
+        if (signal_writes) {
+          // publish this thread's stores to TMA readers in other CTAs
+          fence_proxy_async_global();
+          __threadfence();
+        }
+        // every epilogue thread waits for the phase, so none can arrive for a later task early
+        mbar_arrive(sig_bar);
+        if (!wait_bounded(sig_bar, sig_phase, abort_flag, p, 10)) break;
+        if (warp == 3 && lane == 0) red_release_add(p.counters + signal, 1u);
+        sig_phase ^= 1u;
+      }
     }
   }
 

@@ -65,8 +65,8 @@ using namespace tlr;
 
 namespace {
 
-constexpr int kKindStage1 = 0, kKindStage2 = 1, kKindStage3 = 2, kKindRound = 3, kKindScale = 4;
-constexpr int kNumKinds = 5;
+constexpr int kKindStage1 = 0, kKindStage2 = 1, kKindStage3 = 2, kKindRound = 3, kKindScale = 4, kKindTasks = 5;
+constexpr int kNumKinds = 6;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t align_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -427,6 +427,28 @@ struct Builder {
   // MN-major is replaced by its transposed copy (made by the pre-pass).
   const std::map<ViewKey, View> *tcopy = nullptr;
   std::set<ViewKey> *need_copy = nullptr;               // collection pass: record, do not build
+  // Dependency counters of the merged launch (see Task in tlr_tables.h).
+  std::vector<uint32_t> *counts = nullptr;              // tasks signalling each counter so far
+  int32_t cS0 = -1, cPrep = -1, cL3 = -1;               // this rectangle's counters
+  int32_t war = -1;                                     // counter of the rectangle whose arena we reuse
+  uint32_t war_tgt = 0;
+  int32_t sig = -1, sigw = 0, dep[2] = {-1, -1};
+  uint32_t tgt[2] = {0, 0};
+  void deps(int32_t s, int w, int32_t d0, int32_t d1) {
+    sig = s;
+    sigw = w;
+    dep[0] = dep[1] = -1;
+    tgt[0] = tgt[1] = 0;
+    int n = 0;
+    for (int32_t d : {d0, d1}) {
+      if (d < 0) continue;
+      const uint32_t t = d == war ? war_tgt : (counts ? (*counts)[d] : 0);
+      if (t == 0) continue;
+      dep[n] = d;
+      tgt[n] = t;
+      ++n;
+    }
+  }
 
   int map_of(const View &v, bool mn) {
     auto key = std::make_tuple(v.addr, v.rows, v.cols, v.ld, mn ? 1 : 0);
@@ -515,6 +537,13 @@ struct Builder {
     t.npiece = static_cast<int32_t>(pc.size());
     t.row0 = row0;
     t.col0 = col0;
+    t.signal = sig;
+    t.signal_writes = sigw;
+    t.dep[0] = dep[0];
+    t.dep[1] = dep[1];
+    t.dep_target[0] = tgt[0];
+    t.dep_target[1] = tgt[1];
+    if (sig >= 0 && counts) (*counts)[sig] += 1;
     segs->insert(segs->end(), sg.begin(), sg.end());
     pieces->insert(pieces->end(), pc.begin(), pc.end());
     tasks->push_back(t);
@@ -675,6 +704,7 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
   for (int k = 0; k < X.nc; ++k) {
     std::vector<RPart> Ap = restrict_panel(X.colp[k], X.cpos[k], i0, i1, xcol(k), es);
     if (Ap.empty()) continue;
+    B.deps(B.cPrep, 1, B.war, -1);
     if (Y.dense) {
       // T_i rows of block k: V_{:,k}^T B_k over the rectangle's columns
       const ORef bm = B.dense_block(Y.ro[k], Y.rd[k], Y.co[j0], L.WJ);
@@ -693,6 +723,7 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
     }
     // Stage 1, written transposed: S_k^T = W_{k,J}^T V_{k,I}
     if (L.Soff[k] >= 0) {
+      B.deps(B.cS0 >= 0 ? B.cS0 + k : -1, 1, B.war, -1);
       const uint64_t S = B.ws + static_cast<uint64_t>(L.Soff[k]);
       const int outS = B.out_ws(S, L.Sld[k]);
       std::vector<RPart> Bp = restrict_panel(Y.rowp[k], Y.rpos[k], j0, j1, yrow(k), es);
@@ -715,6 +746,7 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
     }
     // k = j block with a dense tile of op(B): T_i[k-block, k-block] = V_ik^T D_kk
     if (k >= j0 && k < j1 && k < Y.nr && Y.dt(k, k)) {
+      B.deps(B.cPrep, 1, B.war, -1);
       const ORef bm = B.input(Y.diag[k], Y.diag_trans);
       for (const RPart &ap : Ap) {
         const ORef am = B.input(ap.v, false);
@@ -735,6 +767,7 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
       if (L.Poff[i] < 0) continue;
       const uint64_t P = B.ws + static_cast<uint64_t>(L.Poff[i]);
       const int outP = B.out_ws(P, L.Pld[i]);
+      B.deps(B.cPrep, 1, B.war, -1);
       // B operand (kk, n) = op(X)_ii[n, kk]: MN-major on the stored tile unless op(X)_ii is stored^T
       const ORef dm = B.input(X.diag[i], !X.diag_trans);
       std::vector<RPart> Bp = restrict_panel(Y.rowp[i], Y.rpos[i], j0, j1, yrow(i), es);
@@ -759,6 +792,7 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
     for (int k = 0; k < X.nc; ++k) {
       const int64_t sig = L.Ssig[k];
       if (sig == 0) continue;
+      B.deps(B.cPrep, 1, B.cS0 >= 0 ? B.cS0 + k : -1, B.war);
       std::vector<RPart> Ap = restrict_panel(X.colp[k], X.cpos[k], i0, i1, xcol(k), es);
       std::vector<int64_t> base;
       int64_t acc = 0;
@@ -793,6 +827,7 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
   // ---------------- L3: Stage 3, C[i, J] = alpha (U_i T_i + dense segment) + beta C
   B.tasks = &l3;
   const int outC = B.out_c();
+  B.deps(B.cL3, 0, B.cPrep, -1);
   for (int i = i0; i < i1; ++i) {
     const auto &parts = X.rowp[i];
     std::vector<ORef> am(parts.size()), bm(parts.size());
@@ -890,6 +925,8 @@ struct tlr_plan_s {
   std::vector<float *> round_dst;
   std::vector<int64_t> round_n;
   const TJob *d_tjobs = nullptr;
+  unsigned int *d_counters = nullptr;   // [0] ticket, then the dependency counters
+  size_t counters_bytes = 0;
   int ntjobs = 0;
   int64_t ttiles = 0;
   tlr_plan_info_t info{};
@@ -1078,9 +1115,9 @@ int choose(const PlanCore &pc, int i0, int i1, int j0, int j1, int64_t arena, tl
 
 // Rectangles for a budget: widest feasible block of tile columns, then the
 // longest runs of tile rows that fit.
-bool split(const PlanCore &pc, int64_t budget, tlr_order_t force, int es, std::vector<Rect> &rects) {
+bool split(const PlanCore &pc, int64_t arena, tlr_order_t force, int es, std::vector<Rect> &rects,
+           int max_rows) {
   rects.clear();
-  const int64_t arena = budget - pc.fixed;
   if (arena < 0) return false;
   int w = pc.nJ;
   for (; w >= 1; --w) {
@@ -1096,13 +1133,59 @@ bool split(const PlanCore &pc, int64_t budget, tlr_order_t force, int es, std::v
     int i0 = 0;
     while (i0 < pc.nI) {
       int i1 = i0 + 1;
-      while (i1 < pc.nI && choose(pc, i0, i1 + 1, j0, j1, arena, force, es) >= 0) ++i1;
+      while (i1 < pc.nI && (max_rows <= 0 || i1 - i0 < max_rows) &&
+             choose(pc, i0, i1 + 1, j0, j1, arena, force, es) >= 0)
+        ++i1;
       const int o = choose(pc, i0, i1, j0, j1, arena, force, es);
       rects.push_back(Rect{i0, i1, j0, j1, o == 1});
       i0 = i1;
     }
   }
   return true;
+}
+
+// Largest rows per rectangle for a product large enough to pipeline: with at
+// least four rectangles, Stages 1-2 of one rectangle run interleaved with
+// Stage 3 of the previous one and only a quarter of the work is left without a
+// partner at each end (measured best on the large workload: four rectangles
+// beat two and eight). Small products keep one rectangle.
+int pipeline_rows(const PlanCore &pc) {
+  if (const char *e = getenv("TLR_PIPELINE_ROWS")) return atoi(e);   // tuning override (0: off)
+  if (pc.nI < 8) return 0;
+  const LOp &X = pc.can_right ? pc.XR : pc.XL;
+  int64_t W = 0;
+  for (int64_t x : pc.Ccd) W += x;
+  if (final_cost(X, 0, X.nr, pc.can_right ? W : W) < 1e11) return 0;
+  return static_cast<int>((pc.nI + 3) / 4);
+}
+
+// Rectangles and arena count for a budget. With more than one rectangle the
+// arena is doubled so that rectangle r + 1 can be prepared while rectangle r
+// finishes (the two-arena pipelining of the first page's "Association order
+// and workspace"); a budget too small for two arenas runs the rectangles one
+// after another in a single arena.
+bool plan_split(const PlanCore &pc, int64_t budget, tlr_order_t force, int es, std::vector<Rect> &rects,
+                int &narenas) {
+  const int64_t avail = budget - pc.fixed;
+  if (avail < 0) return false;
+  const int cap = pipeline_rows(pc);
+  if (const char *e = getenv("TLR_ARENAS")) {                         // tuning override
+    if (atoi(e) == 1) { narenas = 1; return split(pc, avail, force, es, rects, cap); }
+  }
+  if (cap == 0) {
+    if (!split(pc, avail, force, es, rects, 0)) return false;
+    narenas = 1;
+    if (rects.size() == 1) return true;
+    std::vector<Rect> two;
+    if (split(pc, avail / 2, force, es, two, 0)) { rects = two; narenas = 2; }
+    return true;
+  }
+  if (split(pc, avail / 2, force, es, rects, cap)) {
+    narenas = rects.size() > 1 ? 2 : 1;
+    return true;
+  }
+  narenas = 1;
+  return split(pc, avail, force, es, rects, cap);
 }
 
 int64_t max_rect_bytes(const PlanCore &pc, const std::vector<Rect> &rects, int es) {
@@ -1130,17 +1213,50 @@ struct Tables {
   std::vector<Launch> launches;
   std::vector<std::pair<View, int>> views;
   std::vector<int> task_rect;               // rectangle of each task
+  std::vector<uint32_t> counter_counts;     // tasks signalling each dependency counter
+  int narenas = 1;
+  int64_t arena_bytes = 0;
+  std::vector<uint64_t> rect_arena;         // arena base of each rectangle
   std::vector<RectLayout> layouts;          // per rectangle (in the order it was built)
   std::vector<uint8_t> rect_left;
   tlr_plan_info_t info{};
 };
 
-tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, uint64_t ws, bool dry, Tables &tb) {
+// Estimated SM clocks of a task: tensor-core time or store time, whichever is larger.
+double task_cost(const Task &t, const std::vector<Seg> &segs, const std::vector<Out> &outs, int bn) {
+  int64_t k = 0;
+  for (int q = 0; q < t.nseg; ++q) k += segs[t.seg0 + q].k_len;
+  const double mma = static_cast<double>(bn) * static_cast<double>(k) / 32.0;
+  const int ob = outs[t.out].kind == kOutBF16 ? 2 : 4;
+  const double st = static_cast<double>(t.rows) * t.cols * ob / 32.0;
+  return std::max(mma, st) + 200.0;
+}
+
+// Merge two task lists so that each list's share of the estimated work advances
+// evenly; `from_a` records which list each merged task came from.
+void interleave(const std::vector<Task> &a, const std::vector<Task> &b, const std::vector<Seg> &segs,
+                const std::vector<Out> &outs, int bn, std::vector<Task> &out, std::vector<uint8_t> &from_a) {
+  double ta = 0, tb = 0;
+  for (const Task &t : a) ta += task_cost(t, segs, outs, bn);
+  for (const Task &t : b) tb += task_cost(t, segs, outs, bn);
+  size_t ia = 0, ib = 0;
+  double ca = 0, cb = 0;
+  while (ia < a.size() || ib < b.size()) {
+    const bool take_a = ib >= b.size() || (ia < a.size() && ca / std::max(ta, 1.0) <= cb / std::max(tb, 1.0));
+    if (take_a) { ca += task_cost(a[ia], segs, outs, bn); out.push_back(a[ia++]); from_a.push_back(1); }
+    else { cb += task_cost(b[ib], segs, outs, bn); out.push_back(b[ib++]); from_a.push_back(0); }
+  }
+}
+
+tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, int narenas, uint64_t ws, bool dry,
+                          Tables &tb) {
   const int es = elem_size(pc.pv.dtype);
   const bool tf32 = pc.pv.dtype == TLR_F32;
-  const uint64_t arena = ws + static_cast<uint64_t>(pc.fixed);
+  const int64_t arena_bytes = align_up(max_rect_bytes(pc, rects, es), 256);
   tlr_plan_info_t &info = tb.info;
   memset(&info, 0, sizeof info);
+  std::vector<std::vector<Task>> prep(rects.size()), fin(rects.size());
+  std::vector<int32_t> cl3(rects.size(), -1);
   for (size_t ri = 0; ri < rects.size(); ++ri) {
     const Rect &r = rects[ri];
     const LOp &X = r.left ? pc.XL : pc.XR;
@@ -1148,26 +1264,38 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, ui
     const int i0 = r.left ? r.j0 : r.i0, i1 = r.left ? r.j1 : r.i1;
     const int j0 = r.left ? r.i0 : r.j0, j1 = r.left ? r.i1 : r.j1;
     RectLayout L = layout_rect(X, Y, i0, i1, j0, j1, es);
+    const uint64_t arena = ws + static_cast<uint64_t>(pc.fixed + (static_cast<int64_t>(ri) % narenas) * arena_bytes);
     Builder B{X, Y, es, tf32, tb.bn, r.left, arena, &tb.maps, &tb.map_index, nullptr, &tb.segs, &tb.pieces, &tb.outs};
     B.dry = dry;
     B.views = &tb.views;
     B.tcopy = &pc.tcopy;
+    // counters: S_k per contraction tile, "T and P ready", "Stage 3 done"
+    B.counts = &tb.counter_counts;
+    B.cS0 = static_cast<int32_t>(tb.counter_counts.size());
+    tb.counter_counts.resize(tb.counter_counts.size() + X.nc, 0);
+    B.cPrep = static_cast<int32_t>(tb.counter_counts.size());
+    tb.counter_counts.push_back(0);
+    // Stage 3 of this rectangle only signals when a later rectangle reuses its arena
+    if (ri + narenas < rects.size()) {
+      B.cL3 = static_cast<int32_t>(tb.counter_counts.size());
+      tb.counter_counts.push_back(0);
+    }
+    cl3[ri] = B.cL3;
+    if (ri >= static_cast<size_t>(narenas)) {
+      B.war = cl3[ri - narenas];
+      B.war_tgt = tb.counter_counts[B.war];
+    }
     std::vector<Task> l1, l2, l3;
     build_rect(B, L, l1, l2, l3);
     if (B.status) return B.status;
     sort_by_work(l1, tb.segs);
     sort_by_work(l2, tb.segs);
-    const std::vector<Task> *lists[3] = {&l1, &l2, &l3};
-    const int kinds[3] = {kKindStage1, kKindStage2, kKindStage3};
-    for (int q = 0; q < 3; ++q) {
-      if (lists[q]->empty()) continue;
-      const int64_t t0 = static_cast<int64_t>(tb.all.size());
-      tb.all.insert(tb.all.end(), lists[q]->begin(), lists[q]->end());
-      tb.task_rect.insert(tb.task_rect.end(), lists[q]->size(), static_cast<int>(ri));
-      tb.launches.push_back(Launch{kinds[q], t0, static_cast<int64_t>(tb.all.size())});
-    }
+    prep[ri] = l1;
+    prep[ri].insert(prep[ri].end(), l2.begin(), l2.end());
+    fin[ri] = l3;
     tb.layouts.push_back(L);
     tb.rect_left.push_back(r.left ? 1 : 0);
+    tb.rect_arena.push_back(arena);
     info.runs += 1;
     if (r.left) info.runs_left += 1; else info.runs_right += 1;
     info.flops_stage1 += B.fl_s1;
@@ -1178,6 +1306,34 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, ui
     if (pc.can_right) info.flops_right_final += rect_cost(pc, r.i0, r.i1, r.j0, r.j1, false);
     if (pc.can_left) info.flops_left_final += rect_cost(pc, r.i0, r.i1, r.j0, r.j1, true);
   }
+  // One launch; ticket order: the preparation of rectangle r (Stages 1-2) is
+  // interleaved with Stage 3 of rectangle r - 1 when it has its own arena.
+  std::vector<Task> stream;
+  std::vector<int> stream_rect;
+  auto push = [&](const std::vector<Task> &v, int rr) {
+    for (const Task &t : v) { stream.push_back(t); stream_rect.push_back(rr); }
+  };
+  const size_t nr = rects.size();
+  for (size_t ri = 0; ri < nr; ++ri) {
+    if (narenas >= 2 && ri >= 1) {
+      std::vector<Task> mix;
+      std::vector<uint8_t> from_a;
+      interleave(prep[ri], fin[ri - 1], tb.segs, tb.outs, tb.bn, mix, from_a);
+      for (size_t q = 0; q < mix.size(); ++q) {
+        stream.push_back(mix[q]);
+        stream_rect.push_back(static_cast<int>(from_a[q] ? ri : ri - 1));
+      }
+    } else {
+      if (ri >= 1) push(fin[ri - 1], static_cast<int>(ri - 1));
+      push(prep[ri], static_cast<int>(ri));
+    }
+  }
+  if (nr) push(fin[nr - 1], static_cast<int>(nr - 1));
+  tb.all = stream;
+  tb.task_rect = stream_rect;
+  tb.launches.push_back(Launch{kKindTasks, 0, static_cast<int64_t>(tb.all.size())});
+  tb.narenas = narenas;
+  tb.arena_bytes = arena_bytes;
   info.flops_executed = info.flops_stage1 + info.flops_stage2 + info.flops_stage3 + info.flops_dense_terms;
   info.tasks = static_cast<int64_t>(tb.all.size());
   return TLR_STATUS_OK;
@@ -1293,12 +1449,38 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
     }
   }
   if (carea != static_cast<double>(Cm) * static_cast<double>(Cn)) return "tiles of C do not cover C exactly";
+  // dependencies: every counter a task waits for reaches its target only through
+  // tasks with lower tickets, and the target is the number of signalling tasks
+  {
+    const size_t nc = tb.counter_counts.size();
+    std::vector<int64_t> last(nc, -1);
+    std::vector<uint32_t> cnt(nc, 0);
+    for (size_t ti = 0; ti < tb.all.size(); ++ti) {
+      const Task &t = tb.all[ti];
+      for (int d = 0; d < 2; ++d) {
+        if (t.dep[d] < 0) continue;
+        if (static_cast<size_t>(t.dep[d]) >= nc) { snprintf(buf, sizeof buf, "task %zu: bad counter", ti); return buf; }
+        if (t.dep_target[d] != tb.counter_counts[t.dep[d]] || cnt[t.dep[d]] != t.dep_target[d]) {
+          snprintf(buf, sizeof buf, "task %zu: waits for counter %d before all %u signals have lower tickets",
+                   ti, t.dep[d], t.dep_target[d]);
+          return buf;
+        }
+      }
+      if (t.signal >= 0) {
+        if (static_cast<size_t>(t.signal) >= nc) { snprintf(buf, sizeof buf, "task %zu: bad signal", ti); return buf; }
+        cnt[t.signal] += 1;
+        last[t.signal] = static_cast<int64_t>(ti);
+      }
+    }
+    for (size_t c = 0; c < nc; ++c)
+      if (cnt[c] != tb.counter_counts[c]) return "counter counts differ";
+  }
   // T coverage per rectangle
   for (size_t ri = 0; ri < tb.layouts.size(); ++ri) {
     const RectLayout &L = tb.layouts[ri];
     const bool left = tb.rect_left[ri] != 0;
     const LOp &X = left ? pc.XL : pc.XR;
-    const uint64_t T = ws + static_cast<uint64_t>(pc.fixed + L.Toffset);
+    const uint64_t T = tb.rect_arena[ri] + static_cast<uint64_t>(L.Toffset);
     // column interval -> written row intervals
     std::map<std::pair<int64_t, int64_t>, std::vector<std::pair<int64_t, int64_t>>> wr;
     for (size_t ti = 0; ti < tb.all.size(); ++ti) {
@@ -1477,20 +1659,23 @@ tlr_status_t tlr_gemm_workspace_bytes(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB
   const int es = elem_size(pc.pv.dtype);
   if (runs <= 0) runs = 1;
   std::vector<Rect> rects;
-  int64_t whole = INT64_MAX / 4;
+  int na = 1;
+  int64_t whole = INT64_MAX / 8;
   if (pc.can_right) whole = std::min(whole, rect_bytes(pc, 0, pc.nI, 0, pc.nJ, false, es));
   if (pc.can_left) whole = std::min(whole, rect_bytes(pc, 0, pc.nI, 0, pc.nJ, true, es));
-  int64_t hi = pc.fixed + whole;
-  if (!split(pc, hi, TLR_ORDER_AUTO, es, rects)) return TLR_STATUS_INVALID_ARG;
+  int64_t hi = pc.fixed + 2 * whole;
+  if (!plan_split(pc, hi, TLR_ORDER_AUTO, es, rects, na)) return TLR_STATUS_INVALID_ARG;
+  const int min_runs = static_cast<int>(rects.size());
+  runs = std::max(runs, min_runs);
   int64_t lo = pc.fixed;
-  // smallest budget whose split has at most `runs` rectangles
+  // smallest budget whose plan has at most `runs` rectangles
   while (lo < hi) {
     const int64_t mid = lo + (hi - lo) / 2;
-    if (split(pc, mid, TLR_ORDER_AUTO, es, rects) && static_cast<int>(rects.size()) <= runs) hi = mid;
+    if (plan_split(pc, mid, TLR_ORDER_AUTO, es, rects, na) && static_cast<int>(rects.size()) <= runs) hi = mid;
     else lo = mid + 1;
   }
-  split(pc, hi, TLR_ORDER_AUTO, es, rects);
-  *bytes = static_cast<size_t>(pc.fixed + max_rect_bytes(pc, rects, es));
+  plan_split(pc, hi, TLR_ORDER_AUTO, es, rects, na);
+  *bytes = static_cast<size_t>(pc.fixed + na * align_up(max_rect_bytes(pc, rects, es), 256));
   return TLR_STATUS_OK;
 }
 
@@ -1508,8 +1693,10 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
   const int es = elem_size(pc.pv.dtype);
   const bool tf32 = pc.pv.dtype == TLR_F32;
   std::vector<Rect> rects;
-  if (!split(pc, static_cast<int64_t>(workspace_bytes), order, es, rects)) return TLR_STATUS_WORKSPACE_TOO_SMALL;
-  const int64_t need = pc.fixed + max_rect_bytes(pc, rects, es);
+  int narenas = 1;
+  if (!plan_split(pc, static_cast<int64_t>(workspace_bytes), order, es, rects, narenas))
+    return TLR_STATUS_WORKSPACE_TOO_SMALL;
+  const int64_t need = pc.fixed + narenas * align_up(max_rect_bytes(pc, rects, es), 256);
   if (need > 0 && !workspace) return TLR_STATUS_INVALID_ARG;
 
   tlr_plan_s *p = new (std::nothrow) tlr_plan_s();
@@ -1525,7 +1712,7 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
 
   Tables tb;
   tb.bn = p->bn;
-  st = build_tables(pc, rects, ws, false, tb);
+  st = build_tables(pc, rects, narenas, ws, false, tb);
   if (st) { delete p; return st; }
   p->launches = tb.launches;
   p->info = tb.info;
@@ -1557,9 +1744,10 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
     tj.push_back(d);
   }
   const size_t szj = align_up(static_cast<int64_t>(tj.size() * sizeof(TJob)), 256);
+  const size_t szc = align_up(static_cast<int64_t>((1 + tb.counter_counts.size()) * sizeof(unsigned int)), 256);
   const size_t om = 0, ot = align_up(static_cast<int64_t>(szm), 256), os = ot + szt, op = os + szs, oo = op + szp;
-  const size_t oj = oo + szo;
-  const size_t total = oj + szj + 256;
+  const size_t oj = oo + szo, oc = oj + szj;
+  const size_t total = oc + szc + 256;
   std::vector<uint8_t> host(total, 0);
   if (szm) memcpy(host.data() + om, maps.data(), szm);
   if (!all.empty()) memcpy(host.data() + ot, all.data(), all.size() * sizeof(Task));
@@ -1581,6 +1769,8 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
   p->d_pieces = reinterpret_cast<const Piece *>(dt + op);
   p->d_outs = reinterpret_cast<const Out *>(dt + oo);
   p->d_tjobs = reinterpret_cast<const TJob *>(dt + oj);
+  p->d_counters = reinterpret_cast<unsigned int *>(dt + oc);
+  p->counters_bytes = szc;
   p->ntjobs = static_cast<int>(tj.size());
   p->ttiles = tiles;
   *plan_out = p;
@@ -1597,12 +1787,14 @@ tlr_status_t tlr_debug_check_plan(tlr_op_t opA, tlr_op_t opB, const tlr_operand_
   if (st) return st;
   const int es = elem_size(pc.pv.dtype);
   std::vector<Rect> rects;
-  if (!split(pc, static_cast<int64_t>(workspace_bytes), order, es, rects)) return TLR_STATUS_WORKSPACE_TOO_SMALL;
+  int narenas = 1;
+  if (!plan_split(pc, static_cast<int64_t>(workspace_bytes), order, es, rects, narenas))
+    return TLR_STATUS_WORKSPACE_TOO_SMALL;
   Tables tb;
   tb.bn = choose_bn(pc);
-  st = build_tables(pc, rects, ws, true, tb);
+  st = build_tables(pc, rects, narenas, ws, true, tb);
   if (st) return st;
-  const int64_t need = pc.fixed + max_rect_bytes(pc, rects, es);
+  const int64_t need = pc.fixed + narenas * align_up(max_rect_bytes(pc, rects, es), 256);
   tb.info.workspace_bytes = static_cast<size_t>(need);
   tb.info.launches = static_cast<int64_t>(tb.launches.size());
   if (info) *info = tb.info;
@@ -1655,7 +1847,10 @@ tlr_status_t tlr_plan_execute(tlr_plan_t p, float alpha, float beta, float *C, i
   prm.bn = p->bn;
   prm.err = h->d_err;
   prm.wait_limit_ns = h->wait_limit_ns;
+  prm.ticket = p->d_counters;
+  prm.counters = p->d_counters + 1;
   for (const Launch &l : p->launches) {
+    if (cudaMemsetAsync(p->d_counters, 0, p->counters_bytes, h->stream) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
     prm.tasks = p->d_tasks + l.t0;
     prm.ntasks = static_cast<int32_t>(l.t1 - l.t0);
     const int grid = static_cast<int>(std::min<int64_t>(sms, l.t1 - l.t0));

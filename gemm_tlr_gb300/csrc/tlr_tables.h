@@ -34,6 +34,7 @@ constexpr int kMaxSegs = 4;         // K segments per task
 constexpr int kRing = 8;            // task descriptors staged ahead in shared memory
 constexpr int kSlotBytes = 1536;    // one staged task: header, segments, per-row destinations
 constexpr int kSmemBytes = kStages * kStageBytes + kRing * kSlotBytes + 1024 /*align*/ + 512 /*barriers*/;
+static_assert(8 * (2 * kStages + 6 + 2 * kRing) + 16 <= 512, "barrier area");
 
 enum : uint32_t {
   kSegAMN = 1u,   // A operand MN-major (rows of its view are M); else K-major
@@ -69,13 +70,24 @@ struct alignas(16) Out {
   int32_t trans;    // 1: element (r, c) of the tile goes to ptr[c + r * ld]
 };
 
+// Tasks of one launch are claimed in ticket order from a global counter. A task
+// may wait for up to two dependency counters to reach their targets before it
+// starts (every counted task has a lower ticket, so the wait always ends) and
+// may add one to a counter when it is done. When `signal_writes` is set the
+// increment is ordered after the task's global stores (they are read later by
+// TMA in other CTAs); otherwise it only records that the task's operand reads
+// have finished.
 struct alignas(16) Task {
   int32_t seg0, nseg;     // segments [seg0, seg0 + nseg); nseg == 0 writes zeros (beta * C)
   int32_t out;            // index into the output table
   int32_t rows, cols;     // valid part of the tile (<= kBM, <= BN)
   int32_t piece0, npiece; // row pieces; npiece == 0: output row = row0 + r
-  int32_t pad_;
+  int32_t signal;         // counter to increment when done, -1: none
   int64_t row0, col0;     // output coordinates of the tile origin
+  int32_t dep[2];         // counters to wait for, -1: none
+  uint32_t dep_target[2];
+  int32_t signal_writes;  // 1: the increment publishes this task's stores
+  int32_t pad_[3];
 };
 
 // One transposed input copy for the TF32 path: dst[c + r * dst_ld] =
@@ -101,6 +113,8 @@ struct Params {
   int32_t bn;             // output tile width (multiple of 64, <= kMaxBN)
   unsigned int *err;      // device error word (bounded waits that ran out)
   unsigned long long wait_limit_ns;
+  unsigned int *ticket;   // next unclaimed task of this launch (zeroed before the launch)
+  unsigned int *counters; // dependency counters (zeroed before the launch)
 };
 
 }  // namespace tlr

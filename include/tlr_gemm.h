@@ -182,8 +182,10 @@ tlr_status_t tlr_get_device_status(tlr_handle_t handle);
 
 /* Per-kernel timing with CUDA events on the handle's stream. While enabled,
  * every launch is bracketed by an event pair; tlr_get_timing synchronises and
- * returns, for kernel class `kind` (0 stage1, 1 stage2, 2 stage3, 3 rounding
- * pre-pass, 4 scale-only), the summed milliseconds and launch count since the
+ * returns, for kernel class `kind` (3 the fp32 rounding and transpose
+ * pre-pass, 4 the alpha == 0 scale-only kernel, 5 the task kernel that runs
+ * every stage of a product in one launch; 0-2 are kept for per-stage
+ * launches and read zero), the summed milliseconds and launch count since the
  * last reset. */
 tlr_status_t tlr_set_timing(tlr_handle_t handle, int enabled);
 tlr_status_t tlr_get_timing(tlr_handle_t handle, int kind, double *ms, int64_t *launches);
