@@ -1,0 +1,180 @@
+"""C-ABI library on the host (no GPU): symbols, planner metadata, validation, plan tables.
+
+The planner is pinned by the worked example's printed values ("Tile-Low-Rank
+GEMM: Designing Storage Around the Contraction", sections "One product, three
+stages" and "Association order and workspace") and cross-checked against the
+oracle's own metadata definitions on random rank maps. The table validator
+(`tlr_debug_check_plan`) proves, without a GPU, that every plan's TMA views and
+output writes stay inside their buffers and that every dependency is satisfied.
+"""
+import ctypes
+import json
+import os
+
+import numpy as np
+import pytest
+
+import tlr_inputs as ti
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def g():
+    from gemm_tlr_gb300.build import build
+    build()
+    import gemm_tlr_gb300
+    gemm_tlr_gb300.lib()
+    return gemm_tlr_gb300
+
+
+def desc(ranks, rows, cols, b, diag_dense=0, dtype=1):
+    import gemm_tlr_gb300._abi as abi
+    d = abi.tlr_operand_t()
+    r = np.ascontiguousarray(ranks, dtype=np.int32)
+    d.kind, d.dtype, d.rows, d.cols, d.b, d.diag_dense, d.ranks = 0, dtype, rows, cols, b, diag_dense, r.ctypes.data
+    return d, r
+
+
+def test_library_exports_every_declared_symbol(g):
+    L = ctypes.CDLL(g._abi.LIB_PATH)
+    names = g.header_symbols()
+    assert len(names) >= 18
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(g):
+    assert g.tlr_status_string(0) == "TLR_STATUS_OK"
+    assert g.tlr_status_string(6) == "TLR_STATUS_TIMEOUT"
+
+
+def test_create_without_gpu_reports_not_initialized(g):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(g.TLRError) as e:
+        g.tlr_create(0)
+    assert e.value.code == 7
+
+
+@pytest.mark.parametrize("sol", [0, 1])
+def test_planner_matches_worked_example(g, sol):
+    gold = json.load(open(os.path.join(GOLDEN, "worked_example.json")))
+    b, pr = gold["b"], gold["printed"]
+    A, ka = desc(gold["rA"], 2 * b, 3 * b, b)
+    B, kb = desc(gold["rB_solutions"][sol], 3 * b, 3 * b, b)
+    out = g.tlr_analyze(0, 0, A, B, 2, 3, 3)
+    assert list(out["rho"]) == pr["rho"] and list(out["gamma"]) == pr["gamma"]
+    assert out["F_R"] == 2 * b * b * pr["F_R_over_2b2"] and out["F_L"] == 2 * b * b * pr["F_L_over_2b2"]
+    assert out["stage1_mnk"].reshape(-1, 3).tolist() == pr["stage1_shapes"]
+    assert out["stage3_mnk"].reshape(-1, 3).tolist() == pr["stage3_shapes"]
+    assert out["coupling_products"] == pr["coupling_products"]
+    assert out["distinct_shapes"] == pr["distinct_shapes"]
+    assert [out["T_right_rows"], out["T_right_cols"]] == pr["T_R"]
+    assert [out["T_left_rows"], out["T_left_cols"]] == pr["T_L"]
+    assert out["order"] == (1 if pr["order"] == "R" else 2)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_planner_matches_oracle_metadata_on_random_ranks(g, seed):
+    from oracle import planner_ref
+    rng = np.random.default_rng(seed)
+    nI, nK, nJ, b = rng.integers(1, 6, size=3).tolist() + [64]
+    rA = rng.integers(0, b + 1, size=(nI, nK))
+    rB = rng.integers(0, b + 1, size=(nK, nJ))
+    A, ka = desc(rA, nI * b, nK * b, b)
+    B, kb = desc(rB, nK * b, nJ * b, b)
+    out = g.tlr_analyze(0, 0, A, B, nI, nK, nJ)
+    md = planner_ref.metadata(rA, rB, [b] * nI, [b] * nK, [b] * nJ)
+    assert list(out["rho"]) == md["rho"] and list(out["gamma"]) == md["gamma"]
+    assert list(out["sigma"]) == md["sigma"] and list(out["Gamma"]) == md["Gamma"]
+    assert out["F_R"] == md["F_R"] and out["F_L"] == md["F_L"]
+    assert out["coupling_products"] == md["coupling_products"]
+    assert out["distinct_shapes"] == md["distinct_shapes"]
+
+
+def test_invalid_descriptors_are_rejected_before_launch(g):
+    from gemm_tlr_gb300.device import fake_descriptor
+    rng = np.random.default_rng(1)
+    X = ti.make_tlr(rng, 256, 64, ti.rank_fixed(8), "bf16")
+    A, ka = fake_descriptor(X, 1 << 40)
+    B, kb = fake_descriptor(X, 1 << 41)
+    assert g.tlr_debug_check_plan(0, 0, A, B, 1 << 30)[0] == 0
+    bad_rank = X.ranks.copy()
+    bad_rank[0, 1] = 65                              # larger than the tile
+    A2, k2 = desc(bad_rank, 256, 256, 64, 1)
+    A2.U, A2.V, A2.D = A.U, A.V, A.D
+    assert g.tlr_debug_check_plan(0, 0, A2, B, 1 << 30)[0] == 1
+    A3, k3 = fake_descriptor(X, (1 << 40) + 8)      # base not 16-byte aligned
+    assert g.tlr_debug_check_plan(0, 0, A3, B, 1 << 30)[0] == 2
+    Y = ti.make_tlr(rng, 260, 65, ti.rank_fixed(8), "bf16")   # tile dimension not a multiple of 8
+    A4, k4 = fake_descriptor(Y, 1 << 40)
+    assert g.tlr_debug_check_plan(0, 0, A4, A4, 1 << 30)[0] == 2
+    assert g.tlr_debug_check_plan(0, 0, A, B, 1024)[0] == 3          # workspace too small
+    D = ti.make_dense(rng, 256, 256, "bf16")
+    Dd, kd = fake_descriptor(D, 1 << 42)
+    assert g.tlr_debug_check_plan(0, 0, Dd, Dd, 1 << 30)[0] == 4      # dense x dense unsupported
+    F = ti.make_tlr(rng, 256, 64, ti.rank_fixed(8), "f32")
+    Fd, kf = fake_descriptor(F, 1 << 42)
+    assert g.tlr_debug_check_plan(0, 0, A, Fd, 1 << 30)[0] == 4       # mixed element types
+
+
+def test_offsets_are_checked_against_prefix_sums(g):
+    from gemm_tlr_gb300.device import fake_descriptor
+    rng = np.random.default_rng(2)
+    X = ti.make_tlr(rng, 256, 64, ti.rank_uniform(1, 8), "bf16")
+    A, ka = fake_descriptor(X, 1 << 40)
+    R = X.ranks.astype(np.int64)
+    uoff = np.zeros_like(R)
+    c = 0
+    for i in range(4):
+        for k in range(4):
+            if i != k:
+                uoff[i, k] = 64 * c
+                c += R[i, k]
+    uoff = np.ascontiguousarray(uoff.reshape(-1))
+    A.u_offsets = uoff.ctypes.data
+    assert g.tlr_debug_check_plan(0, 0, A, A, 1 << 30)[0] == 0
+    uoff[6] += 64                              # tile (1, 2)
+    assert g.tlr_debug_check_plan(0, 0, A, A, 1 << 30)[0] == 1
+
+
+CASES = [(1, 1), (2, 1), (3, 1), (4, 1), (5, 1), (5, 8), (3, 8), (2, 4)]
+
+
+@pytest.mark.parametrize("cfg,scale", CASES)
+@pytest.mark.parametrize("order", [0, 1, 2])
+def test_plan_tables_are_valid(g, cfg, scale, order):
+    from gemm_tlr_gb300.device import fake_descriptor
+    p = ti.problem(cfg, scale_down=scale)
+    A, ka = fake_descriptor(p.A, 1 << 40)
+    B, kb = fake_descriptor(p.B, 1 << 41)
+    opA = 1 if p.opA == "T" else 0
+    if cfg == 4 and order == 2:
+        pytest.skip("a dense right operand has only the right order")
+    budget = p.budget or g.tlr_gemm_workspace_bytes(0, opA, 0, A, B, 1)
+    st, msg, info = g.tlr_debug_check_plan(opA, 0, A, B, budget, order)
+    assert st == 0, msg
+    if order == 0:
+        from gemm_tlr_gb300 import flops
+        want = flops.executed_flops(p, "R")["total"]
+        if info["runs_left"] == 0:
+            assert abs(info["flops_executed"] - want) <= 1e-9 * want
+    if cfg == 5 and scale == 1:
+        assert info["runs"] >= 2 and info["workspace_bytes"] <= p.budget
+
+
+def test_workspace_bytes_gives_the_requested_runs(g):
+    from gemm_tlr_gb300.device import fake_descriptor
+    p = ti.problem(5, scale_down=8)
+    A, ka = fake_descriptor(p.A, 1 << 40)
+    B, kb = fake_descriptor(p.B, 1 << 41)
+    prev = None
+    for runs in (1, 2, 3, 6):
+        need = g.tlr_gemm_workspace_bytes(0, 0, 0, A, B, runs)
+        st, msg, info = g.tlr_debug_check_plan(0, 0, A, B, need)
+        assert st == 0 and info["runs"] <= max(runs, 1) and info["workspace_bytes"] <= need
+        if prev is not None:
+            assert need <= prev
+        prev = need
