@@ -68,15 +68,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait on one phase of an mbarrier. Returns false when the limit ran
 // out (the error word and the CTA's abort flag are then set) or when another
 // role of this CTA already gave up.
 __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          const Params &p, uint32_t where) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                          const Params &p, uint32_t where, bool cluster_scope = false) {
+  auto try_once = [&]() { return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (try_once()) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_once()) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
       if (global_ns() - t0 > p.wait_limit_ns) {
@@ -139,6 +152,38 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
       : "memory");
 }
 
+// Pair mode (cta_group::2): copies issued by either CTA of the pair complete on
+// the leader CTA's mbarrier.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap, int32_t x, int32_t y,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of `addr` (a shared::cta address) in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -160,7 +205,7 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
 }
 
 // Instruction descriptor for kind::f16 (bf16 inputs) / kind::tf32, fp32 D.
-__device__ __forceinline__ uint32_t idesc(bool tf32, bool a_mn, bool b_mn, uint32_t n) {
+__device__ __forceinline__ uint32_t idesc(bool tf32, bool a_mn, bool b_mn, uint32_t n, uint32_t m = kBM) {
   uint32_t d = 0;
   d |= 1u << 4;                                   // D format: f32
   d |= (tf32 ? 2u : 1u) << 7;                     // A format: tf32 / bf16
@@ -168,7 +213,7 @@ __device__ __forceinline__ uint32_t idesc(bool tf32, bool a_mn, bool b_mn, uint3
   d |= (a_mn ? 1u : 0u) << 15;                    // A major: 0 K, 1 MN
   d |= (b_mn ? 1u : 0u) << 16;                    // B major
   d |= (n >> 3) << 17;                            // N / 8
-  d |= (static_cast<uint32_t>(kBM) >> 4) << 24;   // M / 16
+  d |= (m >> 4) << 24;                            // M / 16
   return d;
 }
 
@@ -188,6 +233,38 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uin
         "l"(a), "l"(b), "r"(id), "r"(accumulate)
         : "memory");
   }
+}
+
+template <bool kTF32>
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                         uint32_t accumulate) {
+  if constexpr (kTF32) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(id), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(id), "r"(accumulate)
+        : "memory");
+  }
+}
+
+// Commit for a pair: the mbarrier at the same offset in both CTAs gets one arrival.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  const uint16_t mask = 0x3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -231,8 +308,14 @@ struct Slot {
 };
 static_assert(sizeof(Slot) <= kSlotBytes, "slot size");
 
-template <bool kTF32>
+template <bool kTF32, int kPair>
 __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_constant__ Params p) {
+  static_assert(kPair == 1 || kPair == 2, "one CTA or a CTA pair per output tile");
+  // kPair == 2: the tile is 256 rows; each CTA of the pair holds 128 rows of A and
+  // half of the columns of B; the leader issues cta_group::2 MMAs into both TMEMs.
+  constexpr int kSt = kPair == 2 ? 6 : kStages;          // pipeline stages
+  constexpr int kStB = kSmemA + kMaxBN / kPair * 128;     // bytes per stage in this CTA
+  static_assert(kSt * kStB == kStages * kStageBytes, "same shared-memory footprint");
   constexpr int kElt = kTF32 ? 4 : 2;
   constexpr int kCH = 128 / kElt;     // elements per 128-byte row: MN chunk and K block
   constexpr int kBK = kCH;
@@ -242,32 +325,35 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *base_ptr = smem_raw + (base - raw);
-  Slot *ring = reinterpret_cast<Slot *>(base_ptr + kStages * kStageBytes);
-  const uint32_t bars = base + kStages * kStageBytes + kRing * kSlotBytes;
+  Slot *ring = reinterpret_cast<Slot *>(base_ptr + kSt * kStB);
+  const uint32_t bars = base + kSt * kStB + kRing * kSlotBytes;
   auto full_bar = [&](int s) { return bars + 8u * s; };
-  auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
-  auto tfull_bar = [&](int a) { return bars + 8u * (2 * kStages + a); };
-  auto tempty_bar = [&](int a) { return bars + 8u * (2 * kStages + 2 + a); };
-  const uint32_t drain_bar = bars + 8u * (2 * kStages + 4);
-  auto sfull_bar = [&](int r) { return bars + 8u * (2 * kStages + 5 + r); };
-  auto sempty_bar = [&](int r) { return bars + 8u * (2 * kStages + 5 + kRing + r); };
-  const uint32_t sig_bar = bars + 8u * (2 * kStages + 5 + 2 * kRing);   // epilogue stores published
+  auto empty_bar = [&](int s) { return bars + 8u * (kSt + s); };
+  auto tfull_bar = [&](int a) { return bars + 8u * (2 * kSt + a); };
+  auto tempty_bar = [&](int a) { return bars + 8u * (2 * kSt + 2 + a); };
+  const uint32_t drain_bar = bars + 8u * (2 * kSt + 4);
+  auto sfull_bar = [&](int r) { return bars + 8u * (2 * kSt + 5 + r); };
+  auto sempty_bar = [&](int r) { return bars + 8u * (2 * kSt + 5 + kRing + r); };
+  const uint32_t sig_bar = bars + 8u * (2 * kSt + 5 + 2 * kRing);   // epilogue stores published
+  static_assert(8 * (2 * kSt + 6 + 2 * kRing) + 16 <= 512, "barrier area");
   uint32_t *tmem_holder =
-      reinterpret_cast<uint32_t *>(base_ptr + kStages * kStageBytes + kRing * kSlotBytes + 8 * (2 * kStages + 6 + 2 * kRing));
+      reinterpret_cast<uint32_t *>(base_ptr + kSt * kStB + kRing * kSlotBytes + 8 * (2 * kSt + 6 + 2 * kRing));
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bn = p.bn;
+  const uint32_t rank = kPair == 2 ? cluster_rank() : 0u;   // 0: leader of the pair
+  const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSt; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpiThreads);
+      mbar_init(tempty_bar(a), kEpiThreads * kPair);   // every epilogue thread of the pair
     }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(sfull_bar(r), 1);
@@ -279,68 +365,121 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_holder)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (kPair == 2) {
+      // one warp of each CTA of the pair allocates collectively
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_holder)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_holder)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair == 2) cluster_sync_all();   // the peer's barriers exist before anyone signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const char *maps = reinterpret_cast<const char *>(p.maps);
 
   if (warp == 2) {
     // ---------------------------------------------------------------- descriptors
-    // Claim the next ticket, wait for its dependencies, stage it in ring slot
-    // n % kRing (up to kRing tasks ahead of the consumers). A slot whose task
-    // has nseg < 0 tells the consumers that the launch has no more work.
-    for (int n = 0;; ++n) {
-      const int r = n % kRing;
-      const uint32_t ph = (n / kRing) & 1;
-      Slot &sl = ring[r];
-      int ok = 1;
-      unsigned int t = 0;
+    // Claim tickets in batches of kBatch (one CTA: from a global counter; a pair:
+    // batches pair, pair + npairs, ...; every pair is resident, so a dependency
+    // on a lower ticket is always met), load the batch's task headers in parallel,
+    // then per task: wait for its dependencies, load its segments, output
+    // descriptor and row pieces in one parallel round, resolve the destination of
+    // each tile row with shuffles and stage everything in ring slot n % kRing.
+    // A slot whose task has nseg < 0 tells the consumers there is no more work.
+    constexpr int kBatch = 4;
+    int n = 0;
+    bool done = false;
+    for (uint32_t b = 0; !done; ++b) {
+      unsigned int t0 = 0;
       if (lane == 0) {
-        ok = wait_bounded(sempty_bar(r), ph ^ 1u, abort_flag, p, 5) ? 1 : 0;
-        if (ok) t = atomicAdd(p.ticket, 1u);
+        if constexpr (kPair == 1) t0 = atomicAdd(p.ticket, static_cast<unsigned int>(kBatch));
+        else t0 = static_cast<unsigned int>((blockIdx.x / 2 + static_cast<uint64_t>(b) * (gridDim.x / 2)) * kBatch);
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      t = __shfl_sync(0xffffffffu, t, 0);
-      if (!ok) break;
-      if (t >= static_cast<unsigned int>(p.ntasks)) {
-        if (lane == 0) {
-          sl.task.nseg = -1;
-          mbar_arrive(sfull_bar(r));
+      t0 = __shfl_sync(0xffffffffu, t0, 0);
+      Task mine;
+      if (lane < kBatch && t0 + lane < static_cast<unsigned int>(p.ntasks)) mine = p.tasks[t0 + lane];
+      for (int j = 0; j < kBatch; ++j, ++n) {
+        const int r = n % kRing;
+        const uint32_t ph = (n / kRing) & 1;
+        Slot &sl = ring[r];
+        int ok = 1;
+        if (lane == 0) ok = wait_bounded(sempty_bar(r), ph ^ 1u, abort_flag, p, 5) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) { done = true; break; }
+        if (t0 + j >= static_cast<unsigned int>(p.ntasks)) {
+          if (lane == 0) {
+            sl.task.nseg = -1;
+            mbar_arrive(sfull_bar(r));
+          }
+          done = true;
+          break;
         }
-        break;
-      }
-      const Task task = p.tasks[t];
-      if (lane == 0) {
-        for (int d = 0; d < 2 && ok; ++d)
-          if (task.dep[d] >= 0) ok = wait_counter(p.counters + task.dep[d], task.dep_target[d], abort_flag, p) ? 1 : 0;
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (lane == 0) { sl.task = task; sl.out = p.outs[task.out]; }
-      if (lane < task.nseg) sl.segs[lane] = p.segs[task.seg0 + lane];
-      for (int row = lane; row < kBM; row += 32) {
-        int64_t d = -1;
-        if (row < task.rows) {
-          if (task.npiece == 0) {
-            d = task.row0 + row;
-          } else {
-            for (int pc = 0; pc < task.npiece; ++pc) {
-              const Piece pe = p.pieces[task.piece0 + pc];
-              if (row >= pe.src0 && row < pe.src0 + pe.len) { d = pe.dst0 + (row - pe.src0); break; }
+        // broadcast task j's header from lane j
+        Task task;
+        {
+          const int32_t *src = reinterpret_cast<const int32_t *>(&mine);
+          int32_t *dst = reinterpret_cast<int32_t *>(&task);
+#pragma unroll
+          for (int w = 0; w < static_cast<int>(sizeof(Task) / 4); ++w) dst[w] = __shfl_sync(0xffffffffu, src[w], j);
+        }
+        // one parallel round of loads: output descriptor, segments, row pieces
+        Out out;
+        if (lane == 0) out = p.outs[task.out];
+        Seg sg;
+        if (lane < task.nseg) sg = p.segs[task.seg0 + lane];
+        Piece pe;
+        pe.src0 = 0; pe.len = 0; pe.dst0 = 0;
+        const int np = task.npiece < 32 ? task.npiece : 32;
+        if (lane < np) pe = p.pieces[task.piece0 + lane];
+        if (lane == 0) {
+          for (int d = 0; d < 2 && ok; ++d)
+            if (task.dep[d] >= 0) ok = wait_counter(p.counters + task.dep[d], task.dep_target[d], abort_flag, p) ? 1 : 0;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) { done = true; break; }
+        if (lane == 0) { sl.task = task; sl.out = out; }
+        if (lane < task.nseg) sl.segs[lane] = sg;
+        int64_t d[kBM / 32];
+#pragma unroll
+        for (int q4 = 0; q4 < kBM / 32; ++q4) {
+          const int trow = static_cast<int>(rank) * kBM + q4 * 32 + lane;   // row of the (pair) tile
+          d[q4] = trow < task.rows && task.npiece == 0 ? task.row0 + trow : -1;
+        }
+        if (task.npiece > 0) {
+          for (int base_p = 0; base_p < task.npiece; base_p += 32) {
+            if (base_p > 0) {   // more than 32 pieces: next round
+              const int m = task.npiece - base_p < 32 ? task.npiece - base_p : 32;
+              pe.src0 = 0; pe.len = 0; pe.dst0 = 0;
+              if (lane < m) pe = p.pieces[task.piece0 + base_p + lane];
+            }
+            const int m = task.npiece - base_p < 32 ? task.npiece - base_p : 32;
+            for (int q = 0; q < m; ++q) {
+              const int32_t s0 = __shfl_sync(0xffffffffu, pe.src0, q);
+              const int32_t ln = __shfl_sync(0xffffffffu, pe.len, q);
+              const int64_t d0 = __shfl_sync(0xffffffffu, pe.dst0, q);
+#pragma unroll
+              for (int q4 = 0; q4 < kBM / 32; ++q4) {
+                const int trow = static_cast<int>(rank) * kBM + q4 * 32 + lane;
+                if (trow < task.rows && trow >= s0 && trow < s0 + ln) d[q4] = d0 + (trow - s0);
+              }
             }
           }
         }
-        sl.rowdst[row] = d;
+#pragma unroll
+        for (int q4 = 0; q4 < kBM / 32; ++q4) sl.rowdst[q4 * 32 + lane] = d[q4];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfull_bar(r));
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sfull_bar(r));
     }
   } else if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -362,38 +501,50 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
           const void *ma = maps + 128 * static_cast<size_t>(sg.a_map);
           const void *mb = maps + 128 * static_cast<size_t>(sg.b_map);
           const int nkb = (sg.k_len + kBK - 1) / kBK;
+          // Box walk of each operand: MN-major boxes are kCH wide along MN (x) and
+          // step K along y; K-major boxes are 64 rows along MN (y) and step K along x.
+          const int32_t am0 = static_cast<int32_t>(rank) * kBM;   // this CTA's rows of A
+          const int bnc = bn / kPair;                             // this CTA's columns of B
+          const int32_t bn0 = static_cast<int32_t>(rank) * bnc;
+          const bool amn = (sg.flags & kSegAMN) != 0, bmn = (sg.flags & kSegBMN) != 0;
+          int32_t ax = amn ? sg.a_x + am0 : sg.a_x, ay = amn ? sg.a_y : sg.a_y + am0;
+          int32_t bx = bmn ? sg.b_x + bn0 : sg.b_x, by = bmn ? sg.b_y : sg.b_y + bn0;
+          const int32_t adx = amn ? kCH : 0, ady = amn ? 0 : 64, akx = amn ? 0 : kBK, aky = amn ? kBK : 0;
+          const int32_t bdx = bmn ? kCH : 0, bdy = bmn ? 0 : 64, bkx = bmn ? 0 : kBK, bky = bmn ? kBK : 0;
+          const int nba = amn ? kBM / kCH : kBM / 64, nbb = bmn ? bnc / kCH : bnc / 64;
+          const uint32_t sta = amn ? kBK * 128 : 64 * 128, stb = sta;
           for (int kb = 0; kb < nkb; ++kb) {
-            if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p, 1)) { ok = false; break; }
+            const uint32_t eb = empty_bar(stage);
+            if (!mbar_try_wait(eb, phase ^ 1u) && !wait_bounded(eb, phase ^ 1u, abort_flag, p, 1)) { ok = false; break; }
             const uint32_t fb = full_bar(stage);
-            mbar_expect_tx(fb, kSmemA + bn * 128);
-            const uint32_t sa = base + stage * kStageBytes;
+            // one CTA: its own barrier; a pair: both CTAs' copies complete on the leader's
+            // barrier, which the leader arms with the bytes of both
+            if (leader) mbar_expect_tx(fb, kPair * kSmemA + bn * 128);
+            const uint32_t fb_tma = kPair == 2 ? map_to_rank(fb, 0) : fb;
+            const uint32_t sa = base + stage * kStB;
             const uint32_t sb = sa + kSmemA;
-            if (sg.flags & kSegAMN) {
-#pragma unroll
-              for (int c = 0; c < kBM / kCH; ++c)
-                tma_load_2d(sa + c * kBK * 128, ma, sg.a_x + c * kCH, sg.a_y + kb * kBK, fb);
-            } else {
-#pragma unroll
-              for (int c = 0; c < kBM / 64; ++c)
-                tma_load_2d(sa + c * 64 * 128, ma, sg.a_x + kb * kBK, sg.a_y + c * 64, fb);
+            for (int c = 0; c < nba; ++c) {
+              if constexpr (kPair == 2) tma_load_2d_pair(sa + c * sta, ma, ax + c * adx, ay + c * ady, fb_tma);
+              else tma_load_2d(sa + c * sta, ma, ax + c * adx, ay + c * ady, fb_tma);
             }
-            if (sg.flags & kSegBMN) {
-              for (int c = 0; c < bn / kCH; ++c)
-                tma_load_2d(sb + c * kBK * 128, mb, sg.b_x + c * kCH, sg.b_y + kb * kBK, fb);
-            } else {
-              for (int c = 0; c < bn / 64; ++c)
-                tma_load_2d(sb + c * 64 * 128, mb, sg.b_x + kb * kBK, sg.b_y + c * 64, fb);
+            for (int c = 0; c < nbb; ++c) {
+              if constexpr (kPair == 2) tma_load_2d_pair(sb + c * stb, mb, bx + c * bdx, by + c * bdy, fb_tma);
+              else tma_load_2d(sb + c * stb, mb, bx + c * bdx, by + c * bdy, fb_tma);
             }
+            ax += akx; ay += aky; bx += bkx; by += bky;
             issued_mask |= 1u << stage;
             issued_phase_mask = (issued_phase_mask & ~(1u << stage)) | (phase << stage);
-            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            if (++stage == kSt) { stage = 0; phase ^= 1u; }
           }
         }
         mbar_arrive(sempty_bar(r));
       }
-      // Every copy this thread issued must land before the CTA may exit.
-      for (int s = 0; s < kStages; ++s)
-        if (issued_mask & (1u << s)) wait_drain(full_bar(s), (issued_phase_mask >> s) & 1u, 200000000ull);
+      // Every copy this thread issued must land before the CTA may exit (a pair's
+      // copies complete on the leader's barriers; the peer leaves after the leader
+      // at the final cluster barrier).
+      if (leader)
+        for (int s = 0; s < kSt; ++s)
+          if (issued_mask & (1u << s)) wait_drain(full_bar(s), (issued_phase_mask >> s) & 1u, 200000000ull);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -409,45 +560,71 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
         const Slot &sl = ring[r];
         const int nseg = sl.task.nseg;
         if (nseg < 0) break;
-        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p, 2)) break;
+        if (kPair == 2 && !leader) {   // the peer's MMA warp only walks the ring
+          mbar_arrive(sempty_bar(r));
+          continue;
+        }
+        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p, 2, kPair == 2)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kMaxBN);
         uint32_t accumulate = 0;
         for (int s = 0; ok && s < nseg; ++s) {
           const Seg sg = sl.segs[s];
           const bool a_mn = sg.flags & kSegAMN, b_mn = sg.flags & kSegBMN;
-          const uint32_t id = idesc(kTF32, a_mn, b_mn, static_cast<uint32_t>(bn));
+          const uint32_t id = idesc(kTF32, a_mn, b_mn, static_cast<uint32_t>(bn), kBM * kPair);
           const int nkb = (sg.k_len + kBK - 1) / kBK;
+          // Descriptors of stage 0; a stage is kStB bytes further, an MMA step 32 bytes
+          // (K-major: the next K slice of each 128-byte swizzled row) or kUK rows of
+          // 128 bytes (MN-major: whole 8-row groups). The start address sits in the
+          // low 14 bits (>> 4), so steps are plain additions.
+          const uint64_t a0 = a_mn ? sdesc(base, kBK * 128, 1024) : sdesc(base, 16, 1024);
+          const uint64_t b0 = b_mn ? sdesc(base + kSmemA, kBK * 128, 1024) : sdesc(base + kSmemA, 16, 1024);
+          const uint64_t da = a_mn ? (kUK * 128) >> 4 : 32 >> 4, db = b_mn ? (kUK * 128) >> 4 : 32 >> 4;
+          constexpr uint64_t dst = kStB >> 4;
           for (int kb = 0; kb < nkb; ++kb) {
-            if (!wait_bounded(full_bar(stage), phase, abort_flag, p, 3)) { ok = false; break; }
+            const uint32_t fb = full_bar(stage);
+            if (!mbar_try_wait(fb, phase) && !wait_bounded(fb, phase, abort_flag, p, 3)) { ok = false; break; }
             tc_fence_after();
+            const uint64_t ad = a0 + stage * dst, bd = b0 + stage * dst;
             const int kleft = sg.k_len - kb * kBK;
-            const int nmma = kleft >= kBK ? kBK / kUK : (kleft + kUK - 1) / kUK;
-            const uint32_t sa = base + stage * kStageBytes;
-            const uint32_t sb = sa + kSmemA;
-            for (int k = 0; k < nmma; ++k) {
-              // K-major: the next 32-byte K slice of each 128-byte swizzled row.
-              // MN-major: the next kUK rows of 128 bytes (whole 8-row groups).
-              const uint64_t ad = a_mn ? sdesc(sa + k * kUK * 128, kBK * 128, 1024)
-                                       : sdesc(sa + k * 32, 16, 1024);
-              const uint64_t bd = b_mn ? sdesc(sb + k * kUK * 128, kBK * 128, 1024)
-                                       : sdesc(sb + k * 32, 16, 1024);
-              mma<kTF32>(d_tmem, ad, bd, id, accumulate);
-              accumulate = 1;
+            if (kleft >= kBK) {
+#pragma unroll
+              for (int k = 0; k < kBK / kUK; ++k) {
+                if constexpr (kPair == 2) mma_pair<kTF32>(d_tmem, ad + k * da, bd + k * db, id, accumulate);
+                else mma<kTF32>(d_tmem, ad + k * da, bd + k * db, id, accumulate);
+                accumulate = 1;
+              }
+            } else {
+              const int nmma = (kleft + kUK - 1) / kUK;
+              for (int k = 0; k < nmma; ++k) {
+                if constexpr (kPair == 2) mma_pair<kTF32>(d_tmem, ad + k * da, bd + k * db, id, accumulate);
+                else mma<kTF32>(d_tmem, ad + k * da, bd + k * db, id, accumulate);
+                accumulate = 1;
+              }
             }
-            mma_commit(empty_bar(stage));   // frees the stage once these MMAs have read it
-            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            // frees the stage (in both CTAs of a pair) once these MMAs have read it
+            if constexpr (kPair == 2) mma_commit_pair(empty_bar(stage));
+            else mma_commit(empty_bar(stage));
+            if (++stage == kSt) { stage = 0; phase ^= 1u; }
           }
         }
         mbar_arrive(sempty_bar(r));
         if (!ok) break;
-        if (accumulate) mma_commit(tfull_bar(acc));
-        else mbar_arrive(tfull_bar(acc));
+        if (accumulate) {
+          if constexpr (kPair == 2) mma_commit_pair(tfull_bar(acc));
+          else mma_commit(tfull_bar(acc));
+        } else {
+          mbar_arrive(tfull_bar(acc));
+          if constexpr (kPair == 2) mbar_arrive_remote(map_to_rank(tfull_bar(acc), 1));
+        }
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
       // All MMAs issued by this thread complete before TMEM is released.
-      mma_commit(drain_bar);
-      wait_drain(drain_bar, 0, 200000000ull);
+      if (leader) {
+        if constexpr (kPair == 2) mma_commit_pair_local(drain_bar);
+        else mma_commit(drain_bar);
+        wait_drain(drain_bar, 0, 200000000ull);
+      }
     }
   } else {
     // ---------------------------------------------------------------- epilogue
@@ -456,9 +633,29 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
     const int grp = (warp - 3) >> 2;      // epilogue group: its share of the column chunks
     int acc = 0;
     uint32_t acc_phase = 0;
-    uint32_t sig_phase = 0;
+    // Completion signals are per warp and deferred: the signal of task t is
+    // published right before task t+1's stores (its own stores have had the
+    // accumulator wait to drain), or at once whenever this warp would otherwise
+    // block, so a dependency on task t can always be met.
+    int32_t pend = -1;
+    bool pend_writes = false;
+    auto flush = [&]() {
+      if (pend < 0) return;
+      if (pend_writes) {
+        fence_proxy_async_global();   // publish this lane's stores to TMA readers
+        __threadfence();
+      }
+      __syncwarp();
+      if (lane == 0) red_release_add(p.counters + pend, 1u);
+      pend = -1;
+    };
+    auto ready = [&](uint32_t bar, uint32_t parity) {
+      const uint32_t ok = lane == 0 ? (kPair == 2 ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) : 0u;
+      return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
     for (int n = 0;; ++n) {
       const int r = n % kRing;
+      if (!ready(sfull_bar(r), (n / kRing) & 1)) flush();
       if (!wait_bounded(sfull_bar(r), (n / kRing) & 1, abort_flag, p, 8)) break;
       const Slot &sl = ring[r];
       if (sl.task.nseg < 0) break;
@@ -472,8 +669,10 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       const Out o = sl.out;
       __syncwarp();
       if (lane == 0) mbar_arrive(sempty_bar(r));
-      if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p, 4)) break;
+      if (!ready(tfull_bar(acc), acc_phase)) flush();
+      if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p, 4, kPair == 2)) break;
       tc_fence_after();
+      flush();
       const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                               static_cast<uint32_t>(acc * kMaxBN);
       for (int cc = 32 * grp; cc < ncols; cc += 32 * kEpiGroups) {
@@ -564,30 +763,26 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
         }
       }
       tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
+      if (leader) mbar_arrive(tempty_bar(acc));
+      else mbar_arrive_remote(map_to_rank(tempty_bar(acc), 0));   // the leader's MMA reuses both TMEMs
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
-      if (signal >= 0) {
-        if (signal_writes) {
-          // publish this thread's stores to TMA readers in other CTAs
-          fence_proxy_async_global();
-          __threadfence();
-        }
-        // every epilogue thread waits for the phase, so none can arrive for a later task early
-        mbar_arrive(sig_bar);
-        if (!wait_bounded(sig_bar, sig_phase, abort_flag, p, 10)) break;
-        if (warp == 3 && lane == 0) red_release_add(p.counters + signal, 1u);
-        sig_phase ^= 1u;
-      }
+      pend = signal;
+      pend_writes = signal_writes;
     }
+    flush();
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair == 2) cluster_sync_all();   // neither CTA leaves while the other may signal it
   tc_fence_after();
   if (warp == 1) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(kTmemCols)
-                 : "memory");
+    if constexpr (kPair == 2)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                   : "memory");
   }
 }
 
@@ -675,20 +870,67 @@ __global__ void unsatisfied_wait_kernel(const __grid_constant__ Params p) {
 }
 
 // ------------------------------------------------------------------ launchers
-cudaError_t launch_task_gemm(bool tf32, const Params &p, int grid, cudaStream_t stream) {
-  static bool configured[2] = {false, false};
-  const void *fn = tf32 ? reinterpret_cast<const void *>(&tlr_task_gemm<true>)
-                        : reinterpret_cast<const void *>(&tlr_task_gemm<false>);
-  if (!configured[tf32 ? 1 : 0]) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+template <bool kTF32, int kPair>
+cudaError_t launch_one(const Params &p, int grid, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(&tlr_task_gemm<kTF32, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[tf32 ? 1 : 0] = true;
+    configured = true;
   }
-  if (tf32)
-    tlr_task_gemm<true><<<grid, kThreads, kSmemBytes, stream>>>(p);
-  else
-    tlr_task_gemm<false><<<grid, kThreads, kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  if constexpr (kPair == 1) {
+    tlr_task_gemm<kTF32, 1><<<grid, kThreads, kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, &tlr_task_gemm<kTF32, 2>, p);
+  }
+}
+
+// Pairs that can be resident at once (all must be, since tasks are assigned to pairs in turn).
+template <bool kTF32>
+int resident_pairs() {
+  static int n = -1;
+  if (n < 0) {
+    cudaFuncSetAttribute(&tlr_task_gemm<kTF32, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int c = 0;
+    if (cudaOccupancyMaxActiveClusters(&c, &tlr_task_gemm<kTF32, 2>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      c = 0;
+    }
+    n = c;
+  }
+  return n;
+}
+
+int max_resident_pairs(bool tf32) { return tf32 ? resident_pairs<true>() : resident_pairs<false>(); }
+
+cudaError_t launch_task_gemm(bool tf32, int pair, const Params &p, int grid, cudaStream_t stream) {
+  if (pair == 2) return tf32 ? launch_one<true, 2>(p, grid, stream) : launch_one<false, 2>(p, grid, stream);
+  return tf32 ? launch_one<true, 1>(p, grid, stream) : launch_one<false, 1>(p, grid, stream);
 }
 
 cudaError_t launch_round_tf32(const float *const *src, float *const *dst, const int64_t *count, int n,

@@ -52,7 +52,8 @@
 #include "tlr_tables.h"
 
 namespace tlr {
-cudaError_t launch_task_gemm(bool tf32, const Params &p, int grid, cudaStream_t stream);
+cudaError_t launch_task_gemm(bool tf32, int pair, const Params &p, int grid, cudaStream_t stream);
+int max_resident_pairs(bool tf32);
 cudaError_t launch_round_tf32(const float *const *src, float *const *dst, const int64_t *count, int n,
                               int grid, cudaStream_t stream);
 cudaError_t launch_scale_c(float *C, int64_t ldc, int64_t m, int64_t n, float beta, int grid,
@@ -427,8 +428,10 @@ struct Builder {
   // MN-major is replaced by its transposed copy (made by the pre-pass).
   const std::map<ViewKey, View> *tcopy = nullptr;
   std::set<ViewKey> *need_copy = nullptr;               // collection pass: record, do not build
+  int bm = kBM;                         // output tile rows: 128, or 256 for a CTA pair
+  int pair = 1;                         // CTAs per output tile (each epilogue warp of each signals)
   // Dependency counters of the merged launch (see Task in tlr_tables.h).
-  std::vector<uint32_t> *counts = nullptr;              // tasks signalling each counter so far
+  std::vector<uint32_t> *counts = nullptr;              // signals each counter receives so far
   int32_t cS0 = -1, cPrep = -1, cL3 = -1;               // this rectangle's counters
   int32_t war = -1;                                     // counter of the rectangle whose arena we reuse
   uint32_t war_tgt = 0;
@@ -543,7 +546,7 @@ struct Builder {
     t.dep[1] = dep[1];
     t.dep_target[0] = tgt[0];
     t.dep_target[1] = tgt[1];
-    if (sig >= 0 && counts) (*counts)[sig] += 1;
+    if (sig >= 0 && counts) (*counts)[sig] += static_cast<uint32_t>(pair * 4 * kEpiGroups);
     segs->insert(segs->end(), sg.begin(), sg.end());
     pieces->insert(pieces->end(), pc.begin(), pc.end());
     tasks->push_back(t);
@@ -685,6 +688,7 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
   const LOp &X = B.X;
   const LOp &Y = B.Y;
   const int es = B.es, bn = B.bn;
+  const int64_t BM = B.bm;             // rows of an output tile (256 for a CTA pair)
   const int i0 = L.i0, i1 = L.i1, j0 = L.j0, j1 = L.j1;
   const uint64_t T = B.ws + static_cast<uint64_t>(L.Toffset);
   const int outT = B.out_ws(T, L.Tld, L.Trow);
@@ -710,12 +714,12 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
       const ORef bm = B.dense_block(Y.ro[k], Y.rd[k], Y.co[j0], L.WJ);
       for (const RPart &ap : Ap) {
         const ORef am = B.input(ap.v, false);
-        for (int64_t mt = 0; mt < ceil_div(ap.v.cols, kBM); ++mt) {
-          const int64_t rows = std::min<int64_t>(kBM, ap.v.cols - mt * kBM);
-          auto pc = pieces_for(ap, 0, mt * kBM, rows, [&](int i) { return trow(i, k); });
+        for (int64_t mt = 0; mt < ceil_div(ap.v.cols, BM); ++mt) {
+          const int64_t rows = std::min<int64_t>(BM, ap.v.cols - mt * BM);
+          auto pc = pieces_for(ap, 0, mt * BM, rows, [&](int i) { return trow(i, k); });
           for (int64_t nt = 0; nt < ceil_div(L.WJ, bn); ++nt)
             B.emit(outT, 0, nt * bn, rows, std::min<int64_t>(bn, L.WJ - nt * bn),
-                   {Builder::seg(am, bm, mt * kBM, nt * bn, X.cd[k])}, pc);
+                   {Builder::seg(am, bm, mt * BM, nt * bn, X.cd[k])}, pc);
         }
         B.fl_s1 += 2.0 * ap.v.cols * static_cast<double>(L.WJ) * X.cd[k];
       }
@@ -729,15 +733,15 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
       std::vector<RPart> Bp = restrict_panel(Y.rowp[k], Y.rpos[k], j0, j1, yrow(k), es);
       for (const RPart &bp : Bp) {
         const ORef am = B.input(bp.v, false);
-        for (int64_t mt = 0; mt < ceil_div(bp.v.cols, kBM); ++mt) {
-          const int64_t rows = std::min<int64_t>(kBM, bp.v.cols - mt * kBM);
-          auto pc = pieces_for(bp, 0, mt * kBM, rows, [&](int j) { return L.Srow[k][j - j0]; });
+        for (int64_t mt = 0; mt < ceil_div(bp.v.cols, BM); ++mt) {
+          const int64_t rows = std::min<int64_t>(BM, bp.v.cols - mt * BM);
+          auto pc = pieces_for(bp, 0, mt * BM, rows, [&](int j) { return L.Srow[k][j - j0]; });
           int64_t ra = 0;
           for (const RPart &ap : Ap) {
             const ORef bm = B.input(ap.v, false);
             for (int64_t nt = 0; nt < ceil_div(ap.v.cols, bn); ++nt)
               B.emit(outS, 0, ra + nt * bn, rows, std::min<int64_t>(bn, ap.v.cols - nt * bn),
-                     {Builder::seg(am, bm, mt * kBM, nt * bn, X.cd[k])}, pc);
+                     {Builder::seg(am, bm, mt * BM, nt * bn, X.cd[k])}, pc);
             ra += ap.v.cols;
           }
         }
@@ -750,12 +754,12 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
       const ORef bm = B.input(Y.diag[k], Y.diag_trans);
       for (const RPart &ap : Ap) {
         const ORef am = B.input(ap.v, false);
-        for (int64_t mt = 0; mt < ceil_div(ap.v.cols, kBM); ++mt) {
-          const int64_t rows = std::min<int64_t>(kBM, ap.v.cols - mt * kBM);
-          auto pc = pieces_for(ap, 0, mt * kBM, rows, [&](int i) { return trow(i, k); });
+        for (int64_t mt = 0; mt < ceil_div(ap.v.cols, BM); ++mt) {
+          const int64_t rows = std::min<int64_t>(BM, ap.v.cols - mt * BM);
+          auto pc = pieces_for(ap, 0, mt * BM, rows, [&](int i) { return trow(i, k); });
           for (int64_t nt = 0; nt < ceil_div(Y.cd[k], bn); ++nt)
             B.emit(outT, 0, L.colT[k - j0] + nt * bn, rows, std::min<int64_t>(bn, Y.cd[k] - nt * bn),
-                   {Builder::seg(am, bm, mt * kBM, nt * bn, Y.rd[k])}, pc);
+                   {Builder::seg(am, bm, mt * BM, nt * bn, Y.rd[k])}, pc);
         }
         B.fl_dense += 2.0 * ap.v.cols * static_cast<double>(Y.cd[k]) * Y.rd[k];
       }
@@ -773,12 +777,12 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
       std::vector<RPart> Bp = restrict_panel(Y.rowp[i], Y.rpos[i], j0, j1, yrow(i), es);
       for (const RPart &bp : Bp) {
         const ORef am = B.input(bp.v, false);
-        for (int64_t mt = 0; mt < ceil_div(bp.v.cols, kBM); ++mt) {
-          const int64_t rows = std::min<int64_t>(kBM, bp.v.cols - mt * kBM);
-          auto pc = pieces_for(bp, 0, mt * kBM, rows, [&](int j) { return L.Prow[i][j - j0]; });
+        for (int64_t mt = 0; mt < ceil_div(bp.v.cols, BM); ++mt) {
+          const int64_t rows = std::min<int64_t>(BM, bp.v.cols - mt * BM);
+          auto pc = pieces_for(bp, 0, mt * BM, rows, [&](int j) { return L.Prow[i][j - j0]; });
           for (int64_t nt = 0; nt < ceil_div(X.rd[i], bn); ++nt)
             B.emit(outP, 0, nt * bn, rows, std::min<int64_t>(bn, X.rd[i] - nt * bn),
-                   {Builder::seg(am, dm, mt * kBM, nt * bn, X.cd[i])}, pc);
+                   {Builder::seg(am, dm, mt * BM, nt * bn, X.cd[i])}, pc);
         }
         B.fl_dense += 2.0 * X.rd[i] * static_cast<double>(bp.v.cols) * X.cd[i];
       }
@@ -806,16 +810,16 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
           bm = B.input(Y.inner[static_cast<size_t>(k) * Y.nc + j], true);
           B.fl_s2 += 2.0 * sig * static_cast<double>(Y.cd[j]) * r;
         }
-        for (int64_t mt = 0; mt < ceil_div(sig, kBM); ++mt) {
-          const int64_t rows = std::min<int64_t>(kBM, sig - mt * kBM);
+        for (int64_t mt = 0; mt < ceil_div(sig, BM); ++mt) {
+          const int64_t rows = std::min<int64_t>(BM, sig - mt * BM);
           std::vector<Piece> pc;
           for (size_t q = 0; q < Ap.size(); ++q) {
-            auto pp = pieces_for(Ap[q], base[q], mt * kBM, rows, [&](int i) { return trow(i, k); });
+            auto pp = pieces_for(Ap[q], base[q], mt * BM, rows, [&](int i) { return trow(i, k); });
             pc.insert(pc.end(), pp.begin(), pp.end());
           }
           for (int64_t nt = 0; nt < ceil_div(Y.cd[j], bn); ++nt) {
             std::vector<Seg> sg;
-            if (r > 0) sg.push_back(Builder::seg(am, bm, mt * kBM, nt * bn, r));
+            if (r > 0) sg.push_back(Builder::seg(am, bm, mt * BM, nt * bn, r));
             B.emit(outT, 0, L.colT[j - j0] + nt * bn, rows, std::min<int64_t>(bn, Y.cd[j] - nt * bn), sg, pc);
           }
         }
@@ -861,13 +865,13 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
         if (klen > 0) B.fl_dense += 2.0 * X.rd[i] * static_cast<double>(Y.cd[j]) * klen;
       }
       for (int64_t nt = 0; nt < ceil_div(Y.cd[j], bn); ++nt)
-        for (int64_t mt = 0; mt < ceil_div(X.rd[i], kBM); ++mt) {
+        for (int64_t mt = 0; mt < ceil_div(X.rd[i], BM); ++mt) {
           std::vector<Seg> sg;
           for (size_t pi = 0; pi < parts.size(); ++pi)
             if (parts[pi].v.cols > 0)
-              sg.push_back(Builder::seg(am[pi], bm[pi], mt * kBM, L.colT[j - j0] + nt * bn, parts[pi].v.cols));
-          if (klen > 0) sg.push_back(Builder::seg(sa, sb, mt * kBM, nt * bn, klen));
-          B.emit(outC, X.ro[i] + mt * kBM, Y.co[j] + nt * bn, std::min<int64_t>(kBM, X.rd[i] - mt * kBM),
+              sg.push_back(Builder::seg(am[pi], bm[pi], mt * BM, L.colT[j - j0] + nt * bn, parts[pi].v.cols));
+          if (klen > 0) sg.push_back(Builder::seg(sa, sb, mt * BM, nt * bn, klen));
+          B.emit(outC, X.ro[i] + mt * BM, Y.co[j] + nt * bn, std::min<int64_t>(BM, X.rd[i] - mt * BM),
                  std::min<int64_t>(bn, Y.cd[j] - nt * bn), sg, {});
         }
     }
@@ -913,6 +917,7 @@ struct tlr_plan_s {
   tlr_handle_t h = nullptr;
   bool tf32 = false;
   int bn = 256;
+  int pair = 1;
   int64_t Cm = 0, Cn = 0;                 // dimensions of C
   void *d_tables = nullptr;
   const void *d_maps = nullptr;
@@ -925,7 +930,7 @@ struct tlr_plan_s {
   std::vector<float *> round_dst;
   std::vector<int64_t> round_n;
   const TJob *d_tjobs = nullptr;
-  unsigned int *d_counters = nullptr;   // [0] ticket, then the dependency counters
+  unsigned int *d_counters = nullptr;   // one ticket per launch, then the dependency counters
   size_t counters_bytes = 0;
   int ntjobs = 0;
   int64_t ttiles = 0;
@@ -1202,8 +1207,20 @@ int choose_bn(const PlanCore &pc) {
   return static_cast<int>(std::min<int64_t>(kMaxBN, align_up(std::max<int64_t>(bmax, 64), 64)));
 }
 
+// CTA pairs (256-row tiles, cta_group::2) need 256-wide tiles. Measured on the
+// 32768-wide bf16 product they speed up the final products but slow down the
+// T products by more, so one CTA per tile is the default and pairs are a
+// tuning override (TLR_PAIR=2).
+int choose_pair(const PlanCore &pc, int bn) {
+  (void)pc;
+  if (bn != kMaxBN) return 1;
+  if (const char *e = getenv("TLR_PAIR")) return atoi(e) == 2 ? 2 : 1;
+  return 1;
+}
+
 struct Tables {
   int bn = 256;
+  int pair = 1;
   std::vector<CUtensorMap> maps;
   std::map<std::tuple<uint64_t, int64_t, int64_t, int64_t, int>, int> map_index;
   std::vector<Task> all;
@@ -1256,6 +1273,7 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
   tlr_plan_info_t &info = tb.info;
   memset(&info, 0, sizeof info);
   std::vector<std::vector<Task>> prep(rects.size()), fin(rects.size());
+  std::vector<size_t> l2count(rects.size(), 0);
   std::vector<int32_t> cl3(rects.size(), -1);
   for (size_t ri = 0; ri < rects.size(); ++ri) {
     const Rect &r = rects[ri];
@@ -1269,6 +1287,8 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
     B.dry = dry;
     B.views = &tb.views;
     B.tcopy = &pc.tcopy;
+    B.pair = tb.pair;
+    B.bm = kBM * tb.pair;
     // counters: S_k per contraction tile, "T and P ready", "Stage 3 done"
     B.counts = &tb.counter_counts;
     B.cS0 = static_cast<int32_t>(tb.counter_counts.size());
@@ -1292,6 +1312,7 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
     sort_by_work(l2, tb.segs);
     prep[ri] = l1;
     prep[ri].insert(prep[ri].end(), l2.begin(), l2.end());
+    l2count[ri] = l2.size();
     fin[ri] = l3;
     tb.layouts.push_back(L);
     tb.rect_left.push_back(r.left ? 1 : 0);
@@ -1314,6 +1335,30 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
     for (const Task &t : v) { stream.push_back(t); stream_rect.push_back(rr); }
   };
   const size_t nr = rects.size();
+  if (const char *e = getenv("TLR_SPLIT_LAUNCHES")) {
+    // diagnostic: one launch per rectangle and stage class, in stream order
+    if (atoi(e) == 1) {
+      for (size_t ri = 0; ri < nr; ++ri) {
+        const size_t n1 = prep[ri].size() - l2count[ri];
+        std::vector<Task> a(prep[ri].begin(), prep[ri].begin() + n1), b(prep[ri].begin() + n1, prep[ri].end());
+        const std::vector<Task> *lists[3] = {&a, &b, &fin[ri]};
+        const int kinds[3] = {kKindStage1, kKindStage2, kKindStage3};
+        for (int q = 0; q < 3; ++q) {
+          if (lists[q]->empty()) continue;
+          const int64_t t0 = static_cast<int64_t>(stream.size());
+          push(*lists[q], static_cast<int>(ri));
+          tb.launches.push_back(Launch{kinds[q], t0, static_cast<int64_t>(stream.size())});
+        }
+      }
+      tb.all = stream;
+      tb.task_rect = stream_rect;
+      tb.narenas = narenas;
+      tb.arena_bytes = arena_bytes;
+      info.flops_executed = info.flops_stage1 + info.flops_stage2 + info.flops_stage3 + info.flops_dense_terms;
+      info.tasks = static_cast<int64_t>(tb.all.size());
+      return TLR_STATUS_OK;
+    }
+  }
   for (size_t ri = 0; ri < nr; ++ri) {
     if (narenas >= 2 && ri >= 1) {
       std::vector<Task> mix;
@@ -1394,7 +1439,7 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
   double carea = 0;
   for (size_t ti = 0; ti < tb.all.size(); ++ti) {
     const Task &t = tb.all[ti];
-    if (t.rows < 1 || t.rows > kBM || t.cols < 1 || t.cols > tb.bn || t.nseg > kMaxSegs) { snprintf(buf, sizeof buf, "task %zu: bad extent or segment count", ti); return buf; }
+    if (t.rows < 1 || t.rows > kBM * tb.pair || t.cols < 1 || t.cols > tb.bn || t.nseg > kMaxSegs) { snprintf(buf, sizeof buf, "task %zu: bad extent or segment count", ti); return buf; }
     for (int q = 0; q < t.nseg; ++q) {
       const Seg &g = tb.segs[t.seg0 + q];
       if (g.k_len <= 0 || g.a_map < 0 || g.b_map < 0 || g.a_map >= (int)tb.views.size() || g.b_map >= (int)tb.views.size()) {
@@ -1468,7 +1513,7 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
       }
       if (t.signal >= 0) {
         if (static_cast<size_t>(t.signal) >= nc) { snprintf(buf, sizeof buf, "task %zu: bad signal", ti); return buf; }
-        cnt[t.signal] += 1;
+        cnt[t.signal] += static_cast<uint32_t>(tb.pair * 4 * kEpiGroups);
         last[t.signal] = static_cast<int64_t>(ti);
       }
     }
@@ -1712,6 +1757,7 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
 
   Tables tb;
   tb.bn = p->bn;
+  tb.pair = p->pair = choose_pair(pc, p->bn);
   st = build_tables(pc, rects, narenas, ws, false, tb);
   if (st) { delete p; return st; }
   p->launches = tb.launches;
@@ -1744,7 +1790,7 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
     tj.push_back(d);
   }
   const size_t szj = align_up(static_cast<int64_t>(tj.size() * sizeof(TJob)), 256);
-  const size_t szc = align_up(static_cast<int64_t>((1 + tb.counter_counts.size()) * sizeof(unsigned int)), 256);
+  const size_t szc = align_up(static_cast<int64_t>((tb.launches.size() + tb.counter_counts.size()) * sizeof(unsigned int)), 256);
   const size_t om = 0, ot = align_up(static_cast<int64_t>(szm), 256), os = ot + szt, op = os + szs, oo = op + szp;
   const size_t oj = oo + szo, oc = oj + szj;
   const size_t total = oc + szc + 256;
@@ -1792,6 +1838,7 @@ tlr_status_t tlr_debug_check_plan(tlr_op_t opA, tlr_op_t opB, const tlr_operand_
     return TLR_STATUS_WORKSPACE_TOO_SMALL;
   Tables tb;
   tb.bn = choose_bn(pc);
+  tb.pair = choose_pair(pc, tb.bn);
   st = build_tables(pc, rects, narenas, ws, true, tb);
   if (st) return st;
   const int64_t need = pc.fixed + narenas * align_up(max_rect_bytes(pc, rects, es), 256);
@@ -1847,15 +1894,22 @@ tlr_status_t tlr_plan_execute(tlr_plan_t p, float alpha, float beta, float *C, i
   prm.bn = p->bn;
   prm.err = h->d_err;
   prm.wait_limit_ns = h->wait_limit_ns;
-  prm.ticket = p->d_counters;
-  prm.counters = p->d_counters + 1;
-  for (const Launch &l : p->launches) {
-    if (cudaMemsetAsync(p->d_counters, 0, p->counters_bytes, h->stream) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+  // one ticket per launch, then the dependency counters; all start at zero
+  prm.counters = p->d_counters + p->launches.size();
+  if (cudaMemsetAsync(p->d_counters, 0, p->counters_bytes, h->stream) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+  for (size_t li = 0; li < p->launches.size(); ++li) {
+    const Launch &l = p->launches[li];
+    prm.ticket = p->d_counters + li;
     prm.tasks = p->d_tasks + l.t0;
     prm.ntasks = static_cast<int32_t>(l.t1 - l.t0);
-    const int grid = static_cast<int>(std::min<int64_t>(sms, l.t1 - l.t0));
+    int grid = static_cast<int>(std::min<int64_t>(sms, l.t1 - l.t0));
+    if (p->pair == 2) {
+      const int pairs = max_resident_pairs(p->tf32);
+      if (pairs <= 0) return TLR_STATUS_UNSUPPORTED;
+      grid = 2 * static_cast<int>(std::min<int64_t>(pairs, l.t1 - l.t0));
+    }
     if (record_start(h, l.kind, ev) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
-    if (launch_task_gemm(p->tf32, prm, grid, h->stream) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+    if (launch_task_gemm(p->tf32, p->pair, prm, grid, h->stream) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
     if (record_stop(h, ev) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
   }
   return TLR_STATUS_OK;

@@ -70,13 +70,14 @@ struct alignas(16) Out {
   int32_t trans;    // 1: element (r, c) of the tile goes to ptr[c + r * ld]
 };
 
-// Tasks of one launch are claimed in ticket order from a global counter. A task
-// may wait for up to two dependency counters to reach their targets before it
-// starts (every counted task has a lower ticket, so the wait always ends) and
-// may add one to a counter when it is done. When `signal_writes` is set the
-// increment is ordered after the task's global stores (they are read later by
-// TMA in other CTAs); otherwise it only records that the task's operand reads
-// have finished.
+// Tasks of one launch are claimed in ticket order. A task may wait for up to
+// two dependency counters to reach their targets before it starts (every
+// counted task has a lower ticket, so the wait always ends) and signals one
+// counter when done: each epilogue warp of each CTA working on the task adds
+// one, so a counter's target is tasks x epilogue warps x CTAs per task. When
+// `signal_writes` is set the increment is ordered after the warp's global
+// stores (they are read later by TMA in other CTAs); otherwise it only records
+// that the task's operand reads have finished.
 struct alignas(16) Task {
   int32_t seg0, nseg;     // segments [seg0, seg0 + nseg); nseg == 0 writes zeros (beta * C)
   int32_t out;            // index into the output table

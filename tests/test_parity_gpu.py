@@ -132,6 +132,15 @@ def test_small_budget_many_rectangles(oracle_lib, handle):
     assert rel(out, oracle_lib.gemm_problem(p)) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("cfg,scale", [(5, 4), (3, 2), (2, 1)])
+def test_cta_pair_mode_matches_oracle(oracle_lib, handle, monkeypatch, cfg, scale):
+    """256-row tiles on CTA pairs (cta_group::2), the planner's tuning override."""
+    monkeypatch.setenv("TLR_PAIR", "2")
+    p = ti.problem(cfg, scale_down=scale)
+    out, info = run(p, handle)
+    assert rel(out, oracle_lib.gemm_problem(p)) <= TOL[p.dtype]
+
+
 def test_rank_extremes(oracle_lib, handle):
     """Rank-0 tiles, full-rank tiles and a tile row with no low-rank work at all."""
     rng = np.random.default_rng(22)
