@@ -84,6 +84,8 @@ _SIGS = {
     "tlr_plan_destroy": (ctypes.c_int, [_P]),
     "tlr_gemm": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.c_float, _OP, _OP, ctypes.c_float,
                                 _P, ctypes.c_int64, _P, ctypes.c_size_t]),
+    "tlr_gemm_static_scratch": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.c_float, _OP, _OP,
+                                               ctypes.c_float, _P, ctypes.c_int64]),
     "tlr_get_device_status": (ctypes.c_int, [_P]),
     "tlr_set_timing": (ctypes.c_int, [_P, ctypes.c_int]),
     "tlr_get_timing": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
@@ -201,6 +203,12 @@ def tlr_gemm(h: int, opA: int, opB: int, alpha: float, A: tlr_operand_t, B: tlr_
              C: int, ldc: int, ws: int, ws_bytes: int) -> None:
     check(lib().tlr_gemm(_P(h), opA, opB, alpha, ctypes.byref(A), ctypes.byref(B), beta, _P(C), ldc,
                          _P(ws), ws_bytes), "tlr_gemm")
+
+
+def tlr_gemm_static_scratch(h: int, opA: int, opB: int, alpha: float, A: tlr_operand_t, B: tlr_operand_t,
+                            beta: float, C: int, ldc: int) -> None:
+    check(lib().tlr_gemm_static_scratch(_P(h), opA, opB, alpha, ctypes.byref(A), ctypes.byref(B), beta, _P(C),
+                                        ldc), "tlr_gemm_static_scratch")
 
 
 def tlr_get_device_status(h: int) -> int:

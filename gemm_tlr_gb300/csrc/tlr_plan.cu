@@ -46,6 +46,7 @@
 #include <string>
 #include <set>
 #include <tuple>
+#include <mutex>
 #include <vector>
 
 #include "tlr_gemm.h"
@@ -1591,6 +1592,40 @@ cudaError_t record_stop(tlr_handle_t h, const std::pair<cudaEvent_t, cudaEvent_t
 
 }  // namespace
 
+// ------------------------------------------------------------------ static scratch
+// Device memory of tlr_gemm_static_scratch: one product's workspace, descriptor
+// tables and counters. The CUDA runtime reserves it when it loads this
+// translation unit's module (with lazy loading: at the first address lookup),
+// never during a product.
+static __device__ __align__(256) unsigned char g_static_scratch[TLR_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device. The host never takes the symbol itself as a device address.
+tlr_status_t static_scratch_ptr(void **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return TLR_STATUS_CUDA_ERROR; }
+  if (dev < 0 || dev >= kMaxDevices) return TLR_STATUS_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return TLR_STATUS_CUDA_ERROR;
+    }
+    g_static_ptr[dev] = ptr;
+  }
+  *out = g_static_ptr[dev];
+  return TLR_STATUS_OK;
+}
+
+}  // namespace
+
 // ------------------------------------------------------------------ exported ABI
 extern "C" {
 
@@ -1931,6 +1966,102 @@ tlr_status_t tlr_gemm(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, float alpha, c
   st = tlr_plan_execute(p, alpha, beta, C, ldc);
   tlr_plan_destroy(p);
   return st;
+}
+
+// For callers that may not allocate device memory while they run a product:
+// code whose allocator owns every free byte of the device, or loops that must
+// not touch the allocator (allocation can synchronise the device and take
+// milliseconds). Workspace, tables and counters of the product go into
+// g_static_scratch; the tables are uploaded from host memory with one
+// stream-ordered copy. Nothing is allocated or freed on the device.
+tlr_status_t tlr_gemm_static_scratch(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, float alpha,
+                                     const tlr_operand_t *A, const tlr_operand_t *B, float beta, float *C,
+                                     int64_t ldc) {
+  if (!h || !C) return TLR_STATUS_INVALID_ARG;
+  if (!aligned16(C) || ldc % 4) return TLR_STATUS_ALIGNMENT;
+  void *scratch = nullptr;
+  tlr_status_t st = static_scratch_ptr(&scratch);
+  if (st) return st;
+  const uint64_t ws = reinterpret_cast<uint64_t>(scratch);   // the workspace comes first
+  PlanCore pc;
+  st = core_init(pc, opA, opB, A, B, true, ws);
+  if (st) return st;
+  if (ldc < pc.pv.Cm) return TLR_STATUS_INVALID_ARG;
+  const int es = elem_size(pc.pv.dtype);
+  std::vector<Rect> rects;
+  int narenas = 1;
+  constexpr int64_t kTableReserve = 2 << 20;   // the tables of any product that fits take far less
+  if (!plan_split(pc, static_cast<int64_t>(TLR_STATIC_SCRATCH_BYTES) - kTableReserve, TLR_ORDER_AUTO, es, rects, narenas))
+    return TLR_STATUS_WORKSPACE_TOO_SMALL;
+  const int64_t need = pc.fixed + narenas * align_up(max_rect_bytes(pc, rects, es), 256);
+
+  tlr_plan_s p;
+  p.h = h;
+  p.tf32 = pc.pv.dtype == TLR_F32;
+  p.Cm = pc.pv.Cm;
+  p.Cn = pc.pv.Cn;
+  p.round_src = pc.round_src;
+  p.round_dst = pc.round_dst;
+  p.round_n = pc.round_n;
+  p.bn = choose_bn(pc);
+  Tables tb;
+  tb.bn = p.bn;
+  tb.pair = p.pair = choose_pair(pc, p.bn);
+  st = build_tables(pc, rects, narenas, ws, false, tb);
+  if (st) return st;
+  p.launches = tb.launches;
+  p.info = tb.info;
+
+  // tables after the workspace: tensor maps, tasks, segments, pieces, outputs,
+  // transpose jobs, then the counters (one ticket per launch, then the
+  // dependency counters), which tlr_plan_execute zeroes on the stream
+  std::vector<TJob> tj;
+  int64_t tiles = 0;
+  for (const TJobHost &j : pc.tjobs) {
+    TJob d;
+    memset(&d, 0, sizeof d);
+    d.src = reinterpret_cast<const float *>(j.src);
+    d.dst = reinterpret_cast<float *>(j.dst);
+    d.src_ld = j.src_ld; d.dst_ld = j.dst_ld; d.rows = j.rows; d.cols = j.cols; d.tile0 = tiles;
+    tiles += ceil_div(j.rows, 32) * ceil_div(j.cols, 32);
+    tj.push_back(d);
+  }
+  auto bytes_of = [](size_t n, size_t sz) { return static_cast<size_t>(align_up(static_cast<int64_t>(n * sz), 256)); };
+  const size_t ot = bytes_of(tb.maps.size(), sizeof(CUtensorMap));
+  const size_t os = ot + bytes_of(tb.all.size(), sizeof(Task));
+  const size_t op = os + bytes_of(tb.segs.size(), sizeof(Seg));
+  const size_t oo = op + bytes_of(tb.pieces.size(), sizeof(Piece));
+  const size_t oj = oo + bytes_of(tb.outs.size(), sizeof(Out));
+  const size_t oc = oj + bytes_of(tj.size(), sizeof(TJob));
+  const size_t szc = bytes_of(tb.launches.size() + tb.counter_counts.size(), sizeof(unsigned int));
+  const size_t total = oc + szc;
+  const size_t t0 = static_cast<size_t>(align_up(need, 256));
+  if (t0 + total > static_cast<size_t>(TLR_STATIC_SCRATCH_BYTES)) return TLR_STATUS_WORKSPACE_TOO_SMALL;
+  std::vector<uint8_t> host(oc, 0);
+  if (!tb.maps.empty()) memcpy(host.data(), tb.maps.data(), tb.maps.size() * sizeof(CUtensorMap));
+  if (!tb.all.empty()) memcpy(host.data() + ot, tb.all.data(), tb.all.size() * sizeof(Task));
+  if (!tb.segs.empty()) memcpy(host.data() + os, tb.segs.data(), tb.segs.size() * sizeof(Seg));
+  if (!tb.pieces.empty()) memcpy(host.data() + op, tb.pieces.data(), tb.pieces.size() * sizeof(Piece));
+  if (!tb.outs.empty()) memcpy(host.data() + oo, tb.outs.data(), tb.outs.size() * sizeof(Out));
+  if (!tj.empty()) memcpy(host.data() + oj, tj.data(), tj.size() * sizeof(TJob));
+  uint8_t *dt = static_cast<uint8_t *>(scratch) + t0;
+  // From pageable memory the copy returns once `host` has been staged, so it
+  // may go out of scope; the copy stays ordered after earlier work on the stream.
+  if (oc && cudaMemcpyAsync(dt, host.data(), oc, cudaMemcpyHostToDevice, h->stream) != cudaSuccess) {
+    cudaGetLastError();
+    return TLR_STATUS_CUDA_ERROR;
+  }
+  p.d_maps = dt;
+  p.d_tasks = reinterpret_cast<const Task *>(dt + ot);
+  p.d_segs = reinterpret_cast<const Seg *>(dt + os);
+  p.d_pieces = reinterpret_cast<const Piece *>(dt + op);
+  p.d_outs = reinterpret_cast<const Out *>(dt + oo);
+  p.d_tjobs = reinterpret_cast<const TJob *>(dt + oj);
+  p.d_counters = reinterpret_cast<unsigned int *>(dt + oc);
+  p.counters_bytes = szc;
+  p.ntjobs = static_cast<int>(tj.size());
+  p.ttiles = tiles;
+  return tlr_plan_execute(&p, alpha, beta, C, ldc);
 }
 
 tlr_status_t tlr_get_device_status(tlr_handle_t h) {

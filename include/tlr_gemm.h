@@ -175,6 +175,35 @@ tlr_status_t tlr_gemm(tlr_handle_t handle, tlr_op_t opA, tlr_op_t opB, float alp
                       const tlr_operand_t *A, const tlr_operand_t *B, float beta,
                       float *C, int64_t ldc, void *workspace, size_t workspace_bytes);
 
+/* Size of the static device scratch used by tlr_gemm_static_scratch: 64 MiB. */
+#define TLR_STATIC_SCRATCH_BYTES ((size_t)64 * 1024 * 1024)
+
+/* One-shot product like tlr_gemm, but with no workspace argument and no device
+ * allocation: the workspace, descriptor tables and counters live in one static
+ * device array of TLR_STATIC_SCRATCH_BYTES inside the library, reserved by the
+ * CUDA runtime when it loads the module that holds the array (with lazy module
+ * loading, during the first call on a device). The method's description has no
+ * counterpart to this call; it serves callers that may not allocate device
+ * memory while they run (an allocator that owns all free memory, or a loop
+ * that must not stall on allocation).
+ *   Setup: the first call on each device (that device current) looks up the
+ *   array's device address with cudaGetSymbolAddress and keeps it; make that
+ *   first call before any stream capture. The current device must be the
+ *   handle's device.
+ *   Sharing: every call on a device, from any handle or thread, uses the same
+ *   array. Calls must be ordered (one stream, or events between streams);
+ *   overlapping calls race on the workspace and the counters and give wrong
+ *   results. The counters are zeroed on the stream at every call; nothing else
+ *   needs to start at zero.
+ *   Limits: the planner splits C into rectangles to fit the array; a product
+ *   whose smallest split, plus its tables, exceeds it returns
+ *   TLR_STATUS_WORKSPACE_TOO_SMALL before anything is launched or copied.
+ *   Host memory is used for planning as in every other call; with timing on,
+ *   the handle may create CUDA events. Other errors as tlr_gemm. */
+tlr_status_t tlr_gemm_static_scratch(tlr_handle_t handle, tlr_op_t opA, tlr_op_t opB, float alpha,
+                                     const tlr_operand_t *A, const tlr_operand_t *B, float beta,
+                                     float *C, int64_t ldc);
+
 /* Asynchronous device status: synchronises the handle's stream and returns
  * TLR_STATUS_TIMEOUT if a kernel ran out of a bounded wait since the last call
  * (the word is then cleared), TLR_STATUS_CUDA_ERROR on a sticky CUDA error. */
