@@ -169,6 +169,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--scale-down", type=int, default=1,
+                    help="profile a smaller member of the workload family (N/s, b/s, budget/s^2); "
+                         "bench lines are taken at 1")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -192,7 +195,7 @@ def main():
     stream = torch.cuda.current_stream()
     h = g.tlr_create(stream.cuda_stream)
 
-    p = tlr_inputs.problem(5)
+    p = tlr_inputs.problem(5, scale_down=args.scale_down)
     dp = DeviceProblem(p, pinned=True)
     dp.make_plan(h)
     info = dp.info()
@@ -275,7 +278,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "N": p.m, "b": p.A.b, "tile_grid": [32, 32],
+        "config": {"workload": WORKLOAD if args.scale_down == 1 else p.name, "N": p.m, "b": p.A.b, "tile_grid": [p.m // p.A.b, p.n // p.A.b],
                    "ranks": "clamp(round(256 exp(-|i-j|/4)), 8, 256)", "alpha": p.alpha, "beta": p.beta,
                    "workspace_budget_bytes": p.budget, "runs": info["runs"], "order": order,
                    "l2": "inputs larger than L2 (C alone is 4.3 GB; factors 0.42 GB)",

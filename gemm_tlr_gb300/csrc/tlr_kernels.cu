@@ -163,6 +163,21 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
       : "memory");
 }
 
+// Bulk tensor store of a shared-memory box (one thread), tracked per thread in bulk groups.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Shared-memory source of every committed bulk store has been read.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Every committed bulk store is complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Generic-proxy writes to shared memory become visible to bulk copies.
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -273,21 +288,31 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 64 consecutive fp32 columns of this warp's 32 TMEM lanes. The wait is part of
+// the same statement, so no use of the registers can be scheduled before it.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
+      "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]),
+        "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]),
+        "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+        "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]),
+        "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ float round_tf32(float x) {
@@ -297,6 +322,192 @@ __device__ __forceinline__ float round_tf32(float x) {
 }
 
 // ------------------------------------------------------------------ the GEMM
+// Stores one 32-column chunk of an output tile. Lane l of the warp holds the
+// 32 accumulator values of tile row 32q + l (columns c0 .. c0 + nc - 1 of the
+// output); `drow` is that row's destination (valid: the row is stored) and `stg`
+// is the warp's 2 KiB staging area in shared memory.
+__device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, int64_t drow, bool valid,
+                                            const Params &p, const Out &o, int lane, uint8_t *stg) {
+  if (o.kind == kOutC) {
+    // fp32 C through shared memory in two 16-column halves. The warp's block is
+    // 32 rows x 16 columns of column-major C (tile rows are rows of C), or 16
+    // rows x 32 columns (transposed tile: tile row r is column drow(r) of C,
+    // tile columns are its rows). With beta == 0 and a whole block inside the
+    // task, one bulk tensor store writes it; otherwise every store instruction
+    // writes 16 contiguous bytes per lane (4 columns x 128 bytes, or 8 columns
+    // x 64 bytes), and C is read the same way when beta != 0.
+    float *C = p.C;
+    const int64_t ld = p.ldc;
+    const int64_t d0 = __shfl_sync(0xffffffffu, drow, 0);
+    const bool contiguous = __all_sync(0xffffffffu, valid && drow == d0 + lane);
+    const bool rows_ok = contiguous && (d0 & 3) == 0;
+    const bool fast = o.trans ? (nc & 3) == 0 : rows_ok;
+    // bulk stores need the box's first row (the map's inner coordinate) on a 16-byte boundary
+    const bool bulk = p.cmap_ok && p.beta == 0.f && contiguous && ((o.trans ? c0 : d0) & 3) == 0;
+    if (fast) {
+      float *sf = reinterpret_cast<float *>(stg);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int nch = nc - 16 * h < 16 ? nc - 16 * h : 16;   // columns of this half
+        if (nch <= 0) break;
+        if (p.cmap_ok) {   // an earlier bulk store may still be reading the staging area
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
+        }
+        if (!o.trans) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) sf[j * 32 + lane] = p.alpha * v[16 * h + j];   // [column][row]
+          if (bulk && nch == 16) {
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) tma_store_2d(&p.cmap[0], smem_u32(sf), static_cast<int32_t>(d0),
+                                        static_cast<int32_t>(c0 + 16 * h));
+            continue;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const int j = 4 * s + (lane >> 3), r4 = 4 * (lane & 7);
+            if (j < nch) {
+              float4 x = *reinterpret_cast<const float4 *>(sf + j * 32 + r4);
+              float4 *dst = reinterpret_cast<float4 *>(C + d0 + r4 + (c0 + 16 * h + j) * ld);
+              if (p.beta != 0.f) {
+                const float4 c = *dst;
+                x.x = fmaf(p.beta, c.x, x.x); x.y = fmaf(p.beta, c.y, x.y);
+                x.z = fmaf(p.beta, c.z, x.z); x.w = fmaf(p.beta, c.w, x.w);
+              }
+              *dst = x;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<float4 *>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+                make_float4(p.alpha * v[16 * h + 4 * c], p.alpha * v[16 * h + 4 * c + 1],
+                            p.alpha * v[16 * h + 4 * c + 2], p.alpha * v[16 * h + 4 * c + 3]);
+          if (bulk && nch == 16) {   // the XOR layout above is the map's 64-byte swizzle
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) tma_store_2d(&p.cmap[1], smem_u32(stg), static_cast<int32_t>(c0 + 16 * h),
+                                        static_cast<int32_t>(d0));
+            continue;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const int r = 8 * s + (lane >> 2), c = lane & 3;
+            float4 x = *reinterpret_cast<const float4 *>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+            const int64_t d = __shfl_sync(0xffffffffu, valid ? drow : int64_t(-1), r);
+            if (d >= 0 && 4 * c < nch) {
+              float4 *dst = reinterpret_cast<float4 *>(C + (c0 + 16 * h + 4 * c) + d * ld);
+              if (p.beta != 0.f) {
+                const float4 cv = *dst;
+                x.x = fmaf(p.beta, cv.x, x.x); x.y = fmaf(p.beta, cv.y, x.y);
+                x.z = fmaf(p.beta, cv.z, x.z); x.w = fmaf(p.beta, cv.w, x.w);
+              }
+              *dst = x;
+            }
+          }
+        }
+        __syncwarp();   // the staging area is reused by the next half
+      }
+      return;
+    }
+  }
+  if (o.kind == kOutC && o.trans) {
+    // Ragged transposed tile: transpose the warp's 32 x 32 block across lanes
+    // (XOR butterfly) so that lane i holds tile column c0 + i for the warp's 32
+    // rows; every store then writes consecutive floats of one column of C.
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) {
+      const bool upper = (lane & sh) != 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (j & sh) continue;
+        const float send = upper ? v[j] : v[j | sh];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, sh);
+        if (upper) v[j] = recv;
+        else v[j | sh] = recv;
+      }
+    }
+    float *C = p.C;
+    const int64_t ld = p.ldc;
+    const bool cok = lane < nc;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int64_t dj = __shfl_sync(0xffffffffu, valid ? drow : int64_t(-1), j);
+      if (cok && dj >= 0) {
+        const int64_t off = (c0 + lane) + dj * ld;
+        float val = p.alpha * v[j];
+        if (p.beta != 0.f) val = fmaf(p.beta, C[off], val);
+        C[off] = val;
+      }
+    }
+    return;
+  }
+  if (o.kind == kOutBF16 && o.trans && nc == 32) {
+    // Row-major bf16 output through shared memory: each lane parks its row's
+    // 64 bytes (16-byte chunks XOR-swizzled by row pair, so neither the writes
+    // nor the reads conflict on banks); then each store instruction writes
+    // 8 rows x 64 contiguous bytes instead of 32 rows x 16 bytes.
+    __nv_bfloat16 *W = static_cast<__nv_bfloat16 *>(o.ptr);
+    if (p.cmap_ok) {   // an earlier bulk store may still be reading the staging area
+      if (lane == 0) bulk_wait_read();
+      __syncwarp();
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      pk[i] = *reinterpret_cast<const uint32_t *>(&h2);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4 *>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+          make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int r = 8 * s + (lane >> 2), c = lane & 3;
+      const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+      const int64_t d = __shfl_sync(0xffffffffu, valid ? drow : int64_t(-1), r);
+      if (d >= 0) *reinterpret_cast<uint4 *>(W + d * o.ld + c0 + 8 * c) = val;
+    }
+    __syncwarp();   // the staging area is reused by the next chunk
+    return;
+  }
+  if (!valid) return;
+  if (o.kind == kOutC) {
+    float *C = p.C;
+    const int64_t ld = p.ldc;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i < nc) {
+        const int64_t off = drow + (c0 + i) * ld;
+        float val = p.alpha * v[i];
+        if (p.beta != 0.f) val = fmaf(p.beta, C[off], val);
+        C[off] = val;
+      }
+    }
+  } else if (o.kind == kOutBF16) {
+    __nv_bfloat16 *W = static_cast<__nv_bfloat16 *>(o.ptr);
+    if (o.trans) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nc) W[drow * o.ld + c0 + i] = __float2bfloat16_rn(v[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nc) W[drow + (c0 + i) * o.ld] = __float2bfloat16_rn(v[i]);
+    }
+  } else {
+    float *W = static_cast<float *>(o.ptr);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nc) W[o.trans ? (c0 + i) + drow * o.ld : drow + (c0 + i) * o.ld] = round_tf32(v[i]);
+  }
+}
+
 // One staged task in shared memory (written by the descriptor warp).
 struct Slot {
   Task task;                 // 48 B
@@ -630,14 +841,17 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;               // TMEM lanes 32q..32q+31 belong to this warp
     const int row = q * 32 + lane;        // accumulator row held by this thread
-    const int grp = (warp - 3) >> 2;      // epilogue group: its share of the column chunks
+    const int grp = (warp - 3) >> 2;      // epilogue group: its share of the 64-column chunks
+    uint8_t *stg = base_ptr + kSt * kStB + kRing * kSlotBytes + 512 + (warp - 3) * kEpiStageBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
-    // Completion signals are per warp and deferred: the signal of task t is
-    // published right before task t+1's stores (its own stores have had the
-    // accumulator wait to drain), or at once whenever this warp would otherwise
-    // block, so a dependency on task t can always be met.
+    // Completion signals are per warp and batched: consecutive tasks that
+    // signal the same counter add their counts and publish them with one fence.
+    // A warp publishes what it holds before it would block (next task not yet
+    // staged, accumulator not yet ready), when the counter changes, and every
+    // kSignalBatch tasks, so a dependency on its tasks can always be met.
     int32_t pend = -1;
+    uint32_t pend_n = 0;
     bool pend_writes = false;
     auto flush = [&]() {
       if (pend < 0) return;
@@ -646,8 +860,10 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
         __threadfence();
       }
       __syncwarp();
-      if (lane == 0) red_release_add(p.counters + pend, 1u);
+      if (lane == 0) red_release_add(p.counters + pend, pend_n);
       pend = -1;
+      pend_n = 0;
+      pend_writes = false;
     };
     auto ready = [&](uint32_t bar, uint32_t parity) {
       const uint32_t ok = lane == 0 ? (kPair == 2 ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) : 0u;
@@ -672,104 +888,40 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       if (!ready(tfull_bar(acc), acc_phase)) flush();
       if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p, 4, kPair == 2)) break;
       tc_fence_after();
-      flush();
+      if (pend != signal || pend_n >= kSignalBatch) flush();   // the earlier stores have had time to drain
       const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                               static_cast<uint32_t>(acc * kMaxBN);
-      for (int cc = 32 * grp; cc < ncols; cc += 32 * kEpiGroups) {
-        float v[32];
+      for (int cc = 64 * grp; cc < ncols; cc += 64 * kEpiGroups) {
+        float v64[64];
         if (has_acc) {
-          tmem_ld32(t_addr + cc, v);
+          tmem_ld64(t_addr + cc, v64);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          for (int i = 0; i < 64; ++i) v64[i] = 0.f;
         }
-        const int nc = ncols - cc < 32 ? ncols - cc : 32;
-        const int64_t c0 = col0 + cc;
-        if (o.kind == kOutC && o.trans) {
-          // Output tile element (r, c) goes to C[c + r * ldc]. Transpose the warp's
-          // 32 x 32 block across lanes (XOR butterfly) so that lane i holds tile
-          // column c0 + i for the warp's 32 rows; every store then writes 32
-          // consecutive floats of one column of C.
 #pragma unroll
-          for (int sh = 16; sh > 0; sh >>= 1) {
-            const bool upper = (lane & sh) != 0;
+        for (int h = 0; h < 2; ++h) {
+          const int c = cc + 32 * h;
+          if (c >= ncols) break;
+          float v[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (j & sh) continue;
-              const float send = upper ? v[j] : v[j | sh];
-              const float recv = __shfl_xor_sync(0xffffffffu, send, sh);
-              if (upper) v[j] = recv;
-              else v[j | sh] = recv;
-            }
-          }
-          float *C = p.C;
-          const int64_t ld = p.ldc;
-          const bool cok = lane < nc;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int64_t dj = __shfl_sync(0xffffffffu, valid ? drow : int64_t(-1), j);
-            if (cok && dj >= 0) {
-              const int64_t off = (c0 + lane) + dj * ld;
-              float val = p.alpha * v[j];
-              if (p.beta != 0.f) val = fmaf(p.beta, C[off], val);
-              C[off] = val;
-            }
-          }
-          continue;
-        }
-        if (!valid) continue;
-        if (o.kind == kOutC) {
-          float *C = p.C;
-          const int64_t ld = p.ldc;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (i < nc) {
-              const int64_t off = drow + (c0 + i) * ld;
-              float val = p.alpha * v[i];
-              if (p.beta != 0.f) val = fmaf(p.beta, C[off], val);
-              C[off] = val;
-            }
-          }
-        } else if (o.kind == kOutBF16) {
-          __nv_bfloat16 *W = static_cast<__nv_bfloat16 *>(o.ptr);
-          if (o.trans) {
-            // row-major output: this thread's 32 values are 64 contiguous bytes of one row
-            __nv_bfloat16 *dst = W + drow * o.ld + c0;
-            if (nc == 32) {
-              uint32_t pk[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                pk[i] = *reinterpret_cast<const uint32_t *>(&h2);
-              }
-              uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (i < nc) dst[i] = __float2bfloat16_rn(v[i]);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nc) W[drow + (c0 + i) * o.ld] = __float2bfloat16_rn(v[i]);
-          }
-        } else {
-          float *W = static_cast<float *>(o.ptr);
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i < nc) W[o.trans ? (c0 + i) + drow * o.ld : drow + (c0 + i) * o.ld] = round_tf32(v[i]);
+          for (int i = 0; i < 32; ++i) v[i] = v64[32 * h + i];
+          store_chunk(v, ncols - c < 32 ? ncols - c : 32, col0 + c, drow, valid, p, o, lane, stg);
         }
       }
       tc_fence_before();
       if (leader) mbar_arrive(tempty_bar(acc));
       else mbar_arrive_remote(map_to_rank(tempty_bar(acc), 0));   // the leader's MMA reuses both TMEMs
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
-      pend = signal;
-      pend_writes = signal_writes;
+      if (signal >= 0) {
+        pend = signal;
+        pend_n += 1;
+        pend_writes = pend_writes || signal_writes;
+      }
     }
     flush();
+    if (lane == 0) bulk_wait_all();   // bulk stores read shared memory until they complete
+    __syncwarp();
   }
 
   tc_fence_before();

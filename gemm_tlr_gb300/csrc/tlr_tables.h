@@ -13,6 +13,7 @@
 // Multiplication", section "Regular TLR GEMM", join the same accumulator so C is
 // written once.
 #pragma once
+#include <cuda.h>
 #include <stdint.h>
 
 namespace tlr {
@@ -33,7 +34,11 @@ constexpr int kTmemCols = 512;      // two accumulators of up to 256 fp32 column
 constexpr int kMaxSegs = 4;         // K segments per task
 constexpr int kRing = 8;            // task descriptors staged ahead in shared memory
 constexpr int kSlotBytes = 1536;    // one staged task: header, segments, per-row destinations
-constexpr int kSmemBytes = kStages * kStageBytes + kRing * kSlotBytes + 1024 /*align*/ + 512 /*barriers*/;
+constexpr int kEpiStageBytes = 2048; // per epilogue warp: a 32 x 32 bf16 block on its way to a row-major output
+constexpr int kSignalBatch = 16;    // completion signals an epilogue warp may hold back (same counter)
+constexpr int kSmemBytes = kStages * kStageBytes + kRing * kSlotBytes + 1024 /*align*/ + 512 /*barriers*/ +
+                           4 * kEpiGroups * kEpiStageBytes;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 static_assert(8 * (2 * kStages + 6 + 2 * kRing) + 16 <= 512, "barrier area");
 
 enum : uint32_t {
@@ -102,6 +107,12 @@ struct alignas(16) TJob {
 };
 
 struct Params {
+  // C as a 2-D fp32 tensor (rows x columns, column-major) for tensor-memory-
+  // accelerated stores of whole 2 KiB blocks: [0] boxes of 32 rows x 16 columns,
+  // [1] 16 rows x 32 columns with the 64-byte swizzle (transposed tiles).
+  // Used when cmap_ok is set and beta == 0.
+  CUtensorMap cmap[2];
+  int32_t cmap_ok;
   const void *maps;       // CUtensorMap[], 64-byte aligned, device memory
   const Task *tasks;
   const Seg *segs;

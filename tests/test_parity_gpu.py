@@ -133,9 +133,9 @@ def test_small_budget_many_rectangles(oracle_lib, handle):
 
 
 @pytest.mark.parametrize("cfg,scale", [(5, 4), (3, 2), (2, 1)])
-def test_cta_pair_mode_matches_oracle(oracle_lib, handle, monkeypatch, cfg, scale):
-    """256-row tiles on CTA pairs (cta_group::2), the planner's tuning override."""
-    monkeypatch.setenv("TLR_PAIR", "2")
+def test_single_cta_tiles_match_oracle(oracle_lib, handle, monkeypatch, cfg, scale):
+    """128-row tiles on single CTAs (cta_group::1) for products whose default is CTA pairs."""
+    monkeypatch.setenv("TLR_PAIR", "1")
     p = ti.problem(cfg, scale_down=scale)
     out, info = run(p, handle)
     assert rel(out, oracle_lib.gemm_problem(p)) <= TOL[p.dtype]
