@@ -35,6 +35,28 @@ if ROOT not in sys.path:
 METRIC = "TLR GEMM executed TFLOP/s and % of GB300 tensor peak (N=32768, var. rank)"
 WORKLOAD = "large_var_rank_bf16_N32768_b1024"
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
+# task kernel on this workload, from one ncu capture (summary and command in
+# profiles/tlr_task_gemm_large_var_rank_N32768_launches.md). The figure belongs
+# to the kernel sources it was taken with: `sources_sha256` is their hash, and the
+# bench reports null traffic once the sources differ.
+TRAFFIC = {"sources_sha256": "3a69748b05953e080f330472eea4ea1d346fbd9fc84624640153c3759f5b141f",
+           "bytes_per_launch": 7.5116e9 + 7.7185e9}
+# Algorithmic bytes of one product: inputs 0.553 GB, C 4.295 GB written, T 3.354 GB
+# written and read back, S^T 0.167 GB and P^T 0.105 GB written and read back.
+ALGORITHMIC_BYTES = 12.100e9
+
+
+def sources_sha256() -> str:
+    import hashlib
+    root = os.path.join(ROOT, "gemm_tlr_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(root)):
+        h.update(f.encode())
+        with open(os.path.join(root, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
 
 def _peaks():
     try:
@@ -268,8 +290,11 @@ def main():
         per_launch_flops = flops_step / launches_per_step
         avg_ms = k_ms / k_n
         achieved = per_launch_flops / (avg_ms * 1e-3) / 1e12
+        same = args.scale_down == 1 and sources_sha256() == TRAFFIC["sources_sha256"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": achieved / peak_sus, "traffic": None,
+                "frac": achieved / peak_sus, "traffic": TRAFFIC["bytes_per_launch"] if same else None,
+                "traffic_unit": "bytes per launch (DRAM read + write)",
+                "algorithmic_bytes": ALGORITHMIC_BYTES * (per_launch_flops / flops_step),
                 "kernel": "tlr_task_gemm<bf16>: Stages 1-3 and the dense-tile terms of a product in one "
                           "persistent launch (executed FLOPs per launch / mean launch time)",
                 "peak_source": f"{peak_src} bf16 sustained (kernel timed inside back-to-back steps)",

@@ -163,11 +163,25 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
       : "memory");
 }
 
+// L2 policy for data written once and not read again in the launch (C): its
+// lines are the first candidates for eviction, ahead of operands still in use.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void st_global_evict_first(void *ptr, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
+
 // Bulk tensor store of a shared-memory box (one thread), tracked per thread in bulk groups.
-__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int32_t x, int32_t y, uint64_t pol) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
                    reinterpret_cast<uint64_t>(tmap)),
-               "r"(src), "r"(x), "r"(y)
+               "r"(src), "r"(x), "r"(y), "l"(pol)
                : "memory");
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -361,7 +375,7 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
             fence_async_shared();
             __syncwarp();
             if (lane == 0) tma_store_2d(&p.cmap[0], smem_u32(sf), static_cast<int32_t>(d0),
-                                        static_cast<int32_t>(c0 + 16 * h));
+                                        static_cast<int32_t>(c0 + 16 * h), policy_evict_first());
             continue;
           }
           __syncwarp();
@@ -389,7 +403,7 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
             fence_async_shared();
             __syncwarp();
             if (lane == 0) tma_store_2d(&p.cmap[1], smem_u32(stg), static_cast<int32_t>(c0 + 16 * h),
-                                        static_cast<int32_t>(d0));
+                                        static_cast<int32_t>(d0), policy_evict_first());
             continue;
           }
           __syncwarp();
@@ -466,12 +480,15 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
       *reinterpret_cast<uint4 *>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
           make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
     __syncwarp();
+    const uint64_t pol = policy_evict_first();
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       const int r = 8 * s + (lane >> 2), c = lane & 3;
       const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
       const int64_t d = __shfl_sync(0xffffffffu, valid ? drow : int64_t(-1), r);
-      if (d >= 0) *reinterpret_cast<uint4 *>(W + d * o.ld + c0 + 8 * c) = val;
+      // T is read by a later rectangle's final products, long after it would have
+      // left L2: its lines go first, ahead of the operands being reused now
+      if (d >= 0) st_global_evict_first(W + d * o.ld + c0 + 8 * c, val, pol);
     }
     __syncwarp();   // the staging area is reused by the next chunk
     return;
@@ -564,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpiThreads * kPair);   // every epilogue thread of the pair
+      mbar_init(tempty_bar(a), 4 * kEpiGroups * kPair);   // one arrival per epilogue warp of the pair
     }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(sfull_bar(r), 1);
@@ -607,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
     // descriptor and row pieces in one parallel round, resolve the destination of
     // each tile row with shuffles and stage everything in ring slot n % kRing.
     // A slot whose task has nseg < 0 tells the consumers there is no more work.
-    constexpr int kBatch = 4;
+    constexpr int kBatch = kTicketBatch;
     int n = 0;
     bool done = false;
     for (uint32_t b = 0; !done; ++b) {
@@ -909,9 +926,14 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
           store_chunk(v, ncols - c < 32 ? ncols - c : 32, col0 + c, drow, valid, p, o, lane, stg);
         }
       }
+      // every lane's TMEM reads are complete; one arrival per warp hands the
+      // accumulator back (the peer's go to the leader, whose MMA reuses both TMEMs)
       tc_fence_before();
-      if (leader) mbar_arrive(tempty_bar(acc));
-      else mbar_arrive_remote(map_to_rank(tempty_bar(acc), 0));   // the leader's MMA reuses both TMEMs
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(tempty_bar(acc));
+        else mbar_arrive_remote(map_to_rank(tempty_bar(acc), 0));
+      }
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       if (signal >= 0) {
         pend = signal;

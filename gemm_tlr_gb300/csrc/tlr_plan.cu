@@ -865,8 +865,16 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
         }
         if (klen > 0) B.fl_dense += 2.0 * X.rd[i] * static_cast<double>(Y.cd[j]) * klen;
       }
-      for (int64_t nt = 0; nt < ceil_div(Y.cd[j], bn); ++nt)
-        for (int64_t mt = 0; mt < ceil_div(X.rd[i], BM); ++mt) {
+      // Ticket order inside a block of kTicketBatch column tiles: row tile
+      // first. A CTA claims kTicketBatch consecutive tickets, so it gets one row
+      // tile (one slice of U_i) against kTicketBatch column tiles of T_i, and
+      // the CTAs holding the other row tiles read the same T columns at the same
+      // time, while they are in L2. (Consecutive row tiles of one column tile in
+      // one batch made a CTA re-read that T chunk after L2 had dropped it.)
+      const int64_t nnt = ceil_div(Y.cd[j], bn), nmt = ceil_div(X.rd[i], BM);
+      for (int64_t nt0 = 0; nt0 < nnt; nt0 += kTicketBatch)
+        for (int64_t mt = 0; mt < nmt; ++mt)
+          for (int64_t nt = nt0; nt < std::min<int64_t>(nnt, nt0 + kTicketBatch); ++nt) {
           std::vector<Seg> sg;
           for (size_t pi = 0; pi < parts.size(); ++pi)
             if (parts[pi].v.cols > 0)

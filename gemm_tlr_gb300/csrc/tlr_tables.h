@@ -33,6 +33,7 @@ constexpr int kThreads = 96 + kEpiThreads;   // warp 0 TMA, warp 1 MMA, warp 2 d
 constexpr int kTmemCols = 512;      // two accumulators of up to 256 fp32 columns
 constexpr int kMaxSegs = 4;         // K segments per task
 constexpr int kRing = 8;            // task descriptors staged ahead in shared memory
+constexpr int kTicketBatch = 4;     // consecutive tickets a CTA (or CTA pair) claims at once
 constexpr int kSlotBytes = 1536;    // one staged task: header, segments, per-row destinations
 constexpr int kEpiStageBytes = 2048; // per epilogue warp: a 32 x 32 bf16 block on its way to a row-major output
 constexpr int kSignalBatch = 16;    // completion signals an epilogue warp may hold back (same counter)
