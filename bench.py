@@ -36,12 +36,17 @@ METRIC = "TLR GEMM executed TFLOP/s and % of GB300 tensor peak (N=32768, var. ra
 WORKLOAD = "large_var_rank_bf16_N32768_b1024"
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
-# task kernel on this workload, from one ncu capture (summary and command in
+# dominant kernel on this workload (the final-product launch), from one ncu
+# capture (summary and command in
 # profiles/tlr_task_gemm_large_var_rank_N32768_launches.md). The figure belongs
 # to the kernel sources it was taken with: `sources_sha256` is their hash, and the
 # bench reports null traffic once the sources differ.
-TRAFFIC = {"sources_sha256": "3a69748b05953e080f330472eea4ea1d346fbd9fc84624640153c3759f5b141f",
-           "bytes_per_launch": 7.5116e9 + 7.7185e9}
+TRAFFIC = {"sources_sha256": "4cf5fd1439cec5a0e87bde0347047a8a2ed41ab963204d96a5a624a92f9aee61",
+           # final-product launch (CTA pairs), mean of four: 0.974 GB read + 1.021 GB written
+           "bytes_per_launch": 0.974e9 + 1.021e9,
+           # its operands once and C once: (T 3.354 + C 4.295 + U 0.105 + P^T 0.105 + Z 0.105
+           # + dense tiles 0.134 GB) over the four rectangles of the product
+           "algorithmic_bytes_per_launch": 8.098e9 / 4}
 # Algorithmic bytes of one product: inputs 0.553 GB, C 4.295 GB written, T 3.354 GB
 # written and read back, S^T 0.167 GB and P^T 0.105 GB written and read back.
 ALGORITHMIC_BYTES = 12.100e9
@@ -282,21 +287,32 @@ def main():
     peaks, peak_src = _peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     peak_burst = float(peaks.get("bf16_tflops"))
-    # dominant kernel: the task kernel (one launch per step runs every stage)
-    k_ms, k_n = kern[5]
+    # dominant kernel: the launch class with the most time. Classes: 5 = a whole
+    # product in one launch; 1 = Stages 1-2 of a rectangle and 2 = its final
+    # products (two launches per rectangle); 0 = Stage 1 alone (diagnostic split).
+    fl = info["flops_launch"]
+    class_flops = {5: flops_step, 2: fl[2], 1: fl[0] + fl[1], 0: fl[0]}
+    if os.environ.get("TLR_SPLIT_LAUNCHES") == "1":
+        class_flops[1] = fl[1]
+    names = {5: "tlr_task_gemm<bf16>: Stages 1-3 and the dense-tile terms of a product in one persistent launch",
+             2: "tlr_task_gemm<bf16, CTA pairs>: final products (Stage 3 and the dense-tile segment) of a rectangle",
+             1: "tlr_task_gemm<bf16, single CTAs>: Stages 1-2 and the dense precomputes of a rectangle",
+             0: "tlr_task_gemm<bf16>: Stage 1"}
+    dom = max((k for k in (5, 2, 1, 0) if kern[k][1]), key=lambda k: kern[k][0], default=None)
     roof = None
-    if k_n:
+    if dom is not None:
+        k_ms, k_n = kern[dom]
         launches_per_step = k_n / args.steps
-        per_launch_flops = flops_step / launches_per_step
+        per_launch_flops = class_flops[dom] / launches_per_step
         avg_ms = k_ms / k_n
         achieved = per_launch_flops / (avg_ms * 1e-3) / 1e12
         same = args.scale_down == 1 and sources_sha256() == TRAFFIC["sources_sha256"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
                 "frac": achieved / peak_sus, "traffic": TRAFFIC["bytes_per_launch"] if same else None,
                 "traffic_unit": "bytes per launch (DRAM read + write)",
-                "algorithmic_bytes": ALGORITHMIC_BYTES * (per_launch_flops / flops_step),
-                "kernel": "tlr_task_gemm<bf16>: Stages 1-3 and the dense-tile terms of a product in one "
-                          "persistent launch (executed FLOPs per launch / mean launch time)",
+                "algorithmic_bytes": TRAFFIC["algorithmic_bytes_per_launch"],
+                "kernel": names[dom] + " (executed FLOPs per launch / mean launch time)",
+                "launches_per_step": launches_per_step,
                 "peak_source": f"{peak_src} bf16 sustained (kernel timed inside back-to-back steps)",
                 "frac_of_burst": achieved / peak_burst}
     line = {
@@ -312,7 +328,8 @@ def main():
                         "source": peak_src},
         "flops_per_step": flops_step,
         "kernel_ms_per_step": {name: kern[k][0] / args.steps for k, name in
-                               enumerate(["stage1", "stage2", "stage3", "round", "scale", "tasks"]) if kern[k][1]},
+                               enumerate(["stage1", "stages1_2" if os.environ.get("TLR_SPLIT_LAUNCHES") != "1"
+                                          else "stage2", "final", "round", "scale", "tasks"]) if kern[k][1]},
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},

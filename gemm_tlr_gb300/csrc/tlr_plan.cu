@@ -68,6 +68,8 @@ using namespace tlr;
 namespace {
 
 constexpr int kKindStage1 = 0, kKindStage2 = 1, kKindStage3 = 2, kKindRound = 3, kKindScale = 4, kKindTasks = 5;
+// launch classes of the two-launch-per-rectangle schedule
+constexpr int kKindPrep = kKindStage2, kKindFinal = kKindStage3;
 constexpr int kNumKinds = 6;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -395,6 +397,7 @@ struct Rect {
 struct Launch {
   int kind;
   int64_t t0, t1;
+  int pair = 1;          // CTAs per output tile in this launch (1, or 2 for CTA pairs)
 };
 
 // ------------------------------------------------------------------ builder
@@ -429,8 +432,10 @@ struct Builder {
   // MN-major is replaced by its transposed copy (made by the pre-pass).
   const std::map<ViewKey, View> *tcopy = nullptr;
   std::set<ViewKey> *need_copy = nullptr;               // collection pass: record, do not build
-  int bm = kBM;                         // output tile rows: 128, or 256 for a CTA pair
-  int pair = 1;                         // CTAs per output tile (each epilogue warp of each signals)
+  int bm = kBM;                         // output tile rows of the final products: 128, or 256 for a CTA pair
+  int pair = 1;                         // CTAs per final-product tile (each epilogue warp of each signals)
+  int prep_bm = kBM, prep_pair = 1;     // the same for Stages 1-2 and the dense precomputes
+  int cur_pair = 1;                     // of the list being built
   // Dependency counters of the merged launch (see Task in tlr_tables.h).
   std::vector<uint32_t> *counts = nullptr;              // signals each counter receives so far
   int32_t cS0 = -1, cPrep = -1, cL3 = -1;               // this rectangle's counters
@@ -547,7 +552,7 @@ struct Builder {
     t.dep[1] = dep[1];
     t.dep_target[0] = tgt[0];
     t.dep_target[1] = tgt[1];
-    if (sig >= 0 && counts) (*counts)[sig] += static_cast<uint32_t>(pair * 4 * kEpiGroups);
+    if (sig >= 0 && counts) (*counts)[sig] += static_cast<uint32_t>(cur_pair * 4 * kEpiGroups);
     segs->insert(segs->end(), sg.begin(), sg.end());
     pieces->insert(pieces->end(), pc.begin(), pc.end());
     tasks->push_back(t);
@@ -689,7 +694,8 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
   const LOp &X = B.X;
   const LOp &Y = B.Y;
   const int es = B.es, bn = B.bn;
-  const int64_t BM = B.bm;             // rows of an output tile (256 for a CTA pair)
+  int64_t BM = B.prep_bm;              // rows of an output tile (256 for a CTA pair)
+  B.cur_pair = B.prep_pair;
   const int i0 = L.i0, i1 = L.i1, j0 = L.j0, j1 = L.j1;
   const uint64_t T = B.ws + static_cast<uint64_t>(L.Toffset);
   const int outT = B.out_ws(T, L.Tld, L.Trow);
@@ -831,6 +837,8 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
   const double before3 = B.fl_s3 + B.fl_dense;
   // ---------------- L3: Stage 3, C[i, J] = alpha (U_i T_i + dense segment) + beta C
   B.tasks = &l3;
+  BM = B.bm;
+  B.cur_pair = B.pair;
   const int outC = B.out_c();
   B.deps(B.cL3, 0, B.cPrep, -1);
   for (int i = i0; i < i1; ++i) {
@@ -1178,10 +1186,39 @@ int pipeline_rows(const PlanCore &pc) {
 // finishes (the two-arena pipelining of the first page's "Association order
 // and workspace"); a budget too small for two arenas runs the rectangles one
 // after another in a single arena.
+int choose_bn(const PlanCore &pc);
+int choose_pair(const PlanCore &pc, int bn);
+
+// CTAs per tile for Stages 1-2 and the dense precomputes. When the final
+// products run on CTA pairs, the rest runs on single CTAs in a launch of its own
+// before each rectangle's final products: Stage-2 tiles are short (K = one rank)
+// and bound by their stores, and on the large bf16 product they ran 1.5x faster
+// on single CTAs than on pairs (1.03 vs 1.53 ms), while the final products ran
+// 1.2x faster on pairs (2.35 vs 2.85 ms); two launches per rectangle beat one
+// merged launch of pairs. TLR_HYBRID=0 keeps the merged launch.
+int choose_prep_pair(const PlanCore &pc, int bn, int pair) {
+  (void)pc;
+  (void)bn;
+  if (pair != 2) return pair;
+  if (const char *e = getenv("TLR_HYBRID"))
+    if (atoi(e) == 0) return pair;
+  return 1;
+}
+
 bool plan_split(const PlanCore &pc, int64_t budget, tlr_order_t force, int es, std::vector<Rect> &rects,
                 int &narenas) {
   const int64_t avail = budget - pc.fixed;
   if (avail < 0) return false;
+  {
+    const int bn = choose_bn(pc), pair = choose_pair(pc, bn);
+    if (choose_prep_pair(pc, bn, pair) != pair) {
+      // launches in stream order, so one arena; large products still in at least
+      // four rectangles (measured on the 32768-wide product: 3.94 ms with four,
+      // 4.08 with two, 4.40 with eight)
+      narenas = 1;
+      return split(pc, avail, force, es, rects, pipeline_rows(pc));
+    }
+  }
   const int cap = pipeline_rows(pc);
   if (const char *e = getenv("TLR_ARENAS")) {                         // tuning override
     if (atoi(e) == 1) { narenas = 1; return split(pc, avail, force, es, rects, cap); }
@@ -1233,6 +1270,7 @@ int choose_pair(const PlanCore &pc, int bn) {
 struct Tables {
   int bn = 256;
   int pair = 1;
+  int prep_pair = 1;
   std::vector<CUtensorMap> maps;
   std::map<std::tuple<uint64_t, int64_t, int64_t, int64_t, int>, int> map_index;
   std::vector<Task> all;
@@ -1301,6 +1339,8 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
     B.tcopy = &pc.tcopy;
     B.pair = tb.pair;
     B.bm = kBM * tb.pair;
+    B.prep_pair = tb.prep_pair;
+    B.prep_bm = kBM * tb.prep_pair;
     // counters: S_k per contraction tile, "T and P ready", "Stage 3 done"
     B.counts = &tb.counter_counts;
     B.cS0 = static_cast<int32_t>(tb.counter_counts.size());
@@ -1359,7 +1399,7 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
           if (lists[q]->empty()) continue;
           const int64_t t0 = static_cast<int64_t>(stream.size());
           push(*lists[q], static_cast<int>(ri));
-          tb.launches.push_back(Launch{kinds[q], t0, static_cast<int64_t>(stream.size())});
+          tb.launches.push_back(Launch{kinds[q], t0, static_cast<int64_t>(stream.size()), tb.pair});
         }
       }
       tb.all = stream;
@@ -1370,6 +1410,29 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
       info.tasks = static_cast<int64_t>(tb.all.size());
       return TLR_STATUS_OK;
     }
+  }
+  if (tb.prep_pair != tb.pair) {
+    // Two launches per rectangle in stream order: Stages 1-2 and the dense
+    // precomputes on single CTAs, then the final products on CTA pairs. A
+    // launch only waits for counters of its own lower tickets; everything an
+    // earlier launch signals is complete before the next one starts.
+    for (size_t ri = 0; ri < nr; ++ri) {
+      const std::vector<Task> *lists[2] = {&prep[ri], &fin[ri]};
+      const int kinds[2] = {kKindPrep, kKindFinal}, pairs[2] = {tb.prep_pair, tb.pair};
+      for (int q = 0; q < 2; ++q) {
+        if (lists[q]->empty()) continue;
+        const int64_t t0 = static_cast<int64_t>(stream.size());
+        push(*lists[q], static_cast<int>(ri));
+        tb.launches.push_back(Launch{kinds[q], t0, static_cast<int64_t>(stream.size()), pairs[q]});
+      }
+    }
+    tb.all = stream;
+    tb.task_rect = stream_rect;
+    tb.narenas = narenas;
+    tb.arena_bytes = arena_bytes;
+    info.flops_executed = info.flops_stage1 + info.flops_stage2 + info.flops_stage3 + info.flops_dense_terms;
+    info.tasks = static_cast<int64_t>(tb.all.size());
+    return TLR_STATUS_OK;
   }
   for (size_t ri = 0; ri < nr; ++ri) {
     if (narenas >= 2 && ri >= 1) {
@@ -1388,7 +1451,7 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
   if (nr) push(fin[nr - 1], static_cast<int>(nr - 1));
   tb.all = stream;
   tb.task_rect = stream_rect;
-  tb.launches.push_back(Launch{kKindTasks, 0, static_cast<int64_t>(tb.all.size())});
+  tb.launches.push_back(Launch{kKindTasks, 0, static_cast<int64_t>(tb.all.size()), tb.pair});
   tb.narenas = narenas;
   tb.arena_bytes = arena_bytes;
   info.flops_executed = info.flops_stage1 + info.flops_stage2 + info.flops_stage3 + info.flops_dense_terms;
@@ -1447,11 +1510,14 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
     if (!inside(regs, v.addr, span)) { snprintf(buf, sizeof buf, "map %zu: view outside every buffer", m); return buf; }
   }
   const int64_t Cm = pc.pv.Cm, Cn = pc.pv.Cn;
+  std::vector<int> task_pair(tb.all.size(), tb.pair);
+  for (const Launch &l : tb.launches)
+    for (int64_t ti = l.t0; ti < l.t1; ++ti) task_pair[ti] = l.pair;
   std::set<std::pair<int64_t, int64_t>> ctiles;
   double carea = 0;
   for (size_t ti = 0; ti < tb.all.size(); ++ti) {
     const Task &t = tb.all[ti];
-    if (t.rows < 1 || t.rows > kBM * tb.pair || t.cols < 1 || t.cols > tb.bn || t.nseg > kMaxSegs) { snprintf(buf, sizeof buf, "task %zu: bad extent or segment count", ti); return buf; }
+    if (t.rows < 1 || t.rows > kBM * task_pair[ti] || t.cols < 1 || t.cols > tb.bn || t.nseg > kMaxSegs) { snprintf(buf, sizeof buf, "task %zu: bad extent or segment count", ti); return buf; }
     for (int q = 0; q < t.nseg; ++q) {
       const Seg &g = tb.segs[t.seg0 + q];
       if (g.k_len <= 0 || g.a_map < 0 || g.b_map < 0 || g.a_map >= (int)tb.views.size() || g.b_map >= (int)tb.views.size()) {
@@ -1525,7 +1591,7 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
       }
       if (t.signal >= 0) {
         if (static_cast<size_t>(t.signal) >= nc) { snprintf(buf, sizeof buf, "task %zu: bad signal", ti); return buf; }
-        cnt[t.signal] += static_cast<uint32_t>(tb.pair * 4 * kEpiGroups);
+        cnt[t.signal] += static_cast<uint32_t>(task_pair[ti] * 4 * kEpiGroups);
         last[t.signal] = static_cast<int64_t>(ti);
       }
     }
@@ -1804,6 +1870,7 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
   Tables tb;
   tb.bn = p->bn;
   tb.pair = p->pair = choose_pair(pc, p->bn);
+  tb.prep_pair = choose_prep_pair(pc, p->bn, tb.pair);
   st = build_tables(pc, rects, narenas, ws, false, tb);
   if (st) { delete p; return st; }
   p->launches = tb.launches;
@@ -1885,6 +1952,7 @@ tlr_status_t tlr_debug_check_plan(tlr_op_t opA, tlr_op_t opB, const tlr_operand_
   Tables tb;
   tb.bn = choose_bn(pc);
   tb.pair = choose_pair(pc, tb.bn);
+  tb.prep_pair = choose_prep_pair(pc, tb.bn, tb.pair);
   st = build_tables(pc, rects, narenas, ws, true, tb);
   if (st) return st;
   const int64_t need = pc.fixed + narenas * align_up(max_rect_bytes(pc, rects, es), 256);
@@ -1969,13 +2037,13 @@ tlr_status_t tlr_plan_execute(tlr_plan_t p, float alpha, float beta, float *C, i
     prm.tasks = p->d_tasks + l.t0;
     prm.ntasks = static_cast<int32_t>(l.t1 - l.t0);
     int grid = static_cast<int>(std::min<int64_t>(sms, l.t1 - l.t0));
-    if (p->pair == 2) {
+    if (l.pair == 2) {
       const int pairs = max_resident_pairs(p->tf32);
       if (pairs <= 0) return TLR_STATUS_UNSUPPORTED;
       grid = 2 * static_cast<int>(std::min<int64_t>(pairs, l.t1 - l.t0));
     }
     if (record_start(h, l.kind, ev) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
-    if (launch_task_gemm(p->tf32, p->pair, prm, grid, h->stream) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+    if (launch_task_gemm(p->tf32, l.pair, prm, grid, h->stream) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
     if (record_stop(h, ev) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
   }
   return TLR_STATUS_OK;
@@ -2038,6 +2106,7 @@ tlr_status_t tlr_gemm_static_scratch(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB,
   Tables tb;
   tb.bn = p.bn;
   tb.pair = p.pair = choose_pair(pc, p.bn);
+  tb.prep_pair = choose_prep_pair(pc, p.bn, tb.pair);
   st = build_tables(pc, rects, narenas, ws, false, tb);
   if (st) return st;
   p.launches = tb.launches;

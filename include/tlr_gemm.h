@@ -211,11 +211,14 @@ tlr_status_t tlr_get_device_status(tlr_handle_t handle);
 
 /* Per-kernel timing with CUDA events on the handle's stream. While enabled,
  * every launch is bracketed by an event pair; tlr_get_timing synchronises and
- * returns, for kernel class `kind` (3 the fp32 rounding and transpose
- * pre-pass, 4 the alpha == 0 scale-only kernel, 5 the task kernel that runs
- * every stage of a product in one launch; 0-2 are kept for per-stage
- * launches and read zero), the summed milliseconds and launch count since the
- * last reset. */
+ * returns, for launch class `kind`, the summed milliseconds and launch count
+ * since the last reset. Classes: 1 the launch of a rectangle's Stages 1-2 and
+ * dense precomputes, 2 the launch of its final products (products whose final
+ * tiles run on CTA pairs use these two launches per rectangle); 5 a whole
+ * product in one launch (every other product); 3 the fp32 rounding and
+ * transpose pre-pass; 4 the alpha == 0 scale-only kernel; 0 Stage 1 alone
+ * (only with the per-stage diagnostic schedule, which also splits 1 into
+ * Stage 2 alone). */
 tlr_status_t tlr_set_timing(tlr_handle_t handle, int enabled);
 tlr_status_t tlr_get_timing(tlr_handle_t handle, int kind, double *ms, int64_t *launches);
 tlr_status_t tlr_reset_timing(tlr_handle_t handle);

@@ -238,3 +238,17 @@ def test_kernel_timing_counts_launches(handle):
     ms, n = g.tlr_get_timing(handle, 5)
     g.tlr_set_timing(handle, False)
     assert n >= 1 and ms > 0
+
+
+def test_two_launch_schedule_times_both_classes(oracle_lib, handle):
+    """Final tiles on CTA pairs: each rectangle runs a Stages 1-2 launch (class 1)
+    and a final-product launch (class 2); the result still matches the oracle."""
+    import gemm_tlr_gb300 as g
+    g.tlr_reset_timing(handle)
+    g.tlr_set_timing(handle, True)
+    p = ti.problem(5, scale_down=4)
+    out, info = run(p, handle)
+    (ms1, n1), (ms2, n2), (_, n5) = (g.tlr_get_timing(handle, k) for k in (1, 2, 5))
+    g.tlr_set_timing(handle, False)
+    assert n5 == 0 and n1 == info["runs"] and n2 == info["runs"] and ms1 > 0 and ms2 > 0
+    assert rel(out, oracle_lib.gemm_problem(p)) <= TOL["bf16"]
