@@ -1212,11 +1212,15 @@ bool plan_split(const PlanCore &pc, int64_t budget, tlr_order_t force, int es, s
   {
     const int bn = choose_bn(pc), pair = choose_pair(pc, bn);
     if (choose_prep_pair(pc, bn, pair) != pair) {
-      // launches in stream order, so one arena; large products still in at least
-      // four rectangles (measured on the 32768-wide product: 3.94 ms with four,
-      // 4.08 with two, 4.40 with eight)
+      // Launches in stream order, so one arena. A large TLR x TLR product still
+      // goes in at least four rectangles, whose smaller terminal matrices let
+      // more of them take the cheaper association order (32768-wide bf16
+      // product: 3.87 ms with four, 4.05 with two, 4.40 with eight); a product
+      // with a dense operand (no Stage 2) takes the fewest the budget allows
+      // (16384 x 16384 TLR times a dense 16384 x 4096: 0.54 ms in one, 0.66 in four).
       narenas = 1;
-      return split(pc, avail, force, es, rects, pipeline_rows(pc));
+      const bool dense_operand = pc.pv.dense_left || pc.pv.dense_right;
+      return split(pc, avail, force, es, rects, dense_operand ? 0 : pipeline_rows(pc));
     }
   }
   const int cap = pipeline_rows(pc);
@@ -1360,11 +1364,11 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
     std::vector<Task> l1, l2, l3;
     build_rect(B, L, l1, l2, l3);
     if (B.status) return B.status;
+    l2count[ri] = l2.size();
     sort_by_work(l1, tb.segs);
     sort_by_work(l2, tb.segs);
     prep[ri] = l1;
     prep[ri].insert(prep[ri].end(), l2.begin(), l2.end());
-    l2count[ri] = l2.size();
     fin[ri] = l3;
     tb.layouts.push_back(L);
     tb.rect_left.push_back(r.left ? 1 : 0);
@@ -1395,11 +1399,12 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
         std::vector<Task> a(prep[ri].begin(), prep[ri].begin() + n1), b(prep[ri].begin() + n1, prep[ri].end());
         const std::vector<Task> *lists[3] = {&a, &b, &fin[ri]};
         const int kinds[3] = {kKindStage1, kKindStage2, kKindStage3};
+        const int pairs[3] = {tb.prep_pair, tb.prep_pair, tb.pair};
         for (int q = 0; q < 3; ++q) {
           if (lists[q]->empty()) continue;
           const int64_t t0 = static_cast<int64_t>(stream.size());
           push(*lists[q], static_cast<int>(ri));
-          tb.launches.push_back(Launch{kinds[q], t0, static_cast<int64_t>(stream.size()), tb.pair});
+          tb.launches.push_back(Launch{kinds[q], t0, static_cast<int64_t>(stream.size()), pairs[q]});
         }
       }
       tb.all = stream;
