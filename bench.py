@@ -199,6 +199,11 @@ def main():
     ap.add_argument("--scale-down", type=int, default=1,
                     help="profile a smaller member of the workload family (N/s, b/s, budget/s^2); "
                          "bench lines are taken at 1")
+    ap.add_argument("--workload", default="large_var_rank", choices=["large_var_rank", "skewed8x8"],
+                    help="skewed8x8: the pages' variable-rank 8 x 8 grid (b = N/8, ranks on [b/32, b/16]), "
+                         "a second measurement beside the metric's workload")
+    ap.add_argument("--n", type=int, default=65536, help="order of the skewed8x8 workload")
+    ap.add_argument("--dtype", default="f16", choices=["f16", "bf16", "f32"], help="element type of skewed8x8")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -222,7 +227,12 @@ def main():
     stream = torch.cuda.current_stream()
     h = g.tlr_create(stream.cuda_stream)
 
-    p = tlr_inputs.problem(5, scale_down=args.scale_down)
+    main_workload = args.workload == "large_var_rank"
+    if main_workload:
+        p = tlr_inputs.problem(5, scale_down=args.scale_down)
+    else:
+        p = tlr_inputs.skewed_grid(args.n, args.dtype)
+        args.no_cpu_baseline = True
     dp = DeviceProblem(p, pinned=True)
     dp.make_plan(h)
     info = dp.info()
@@ -287,6 +297,8 @@ def main():
     peaks, peak_src = _peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     peak_burst = float(peaks.get("bf16_tflops"))
+    if p.dtype == "f32":   # TF32 runs at half the bf16 rate (nominal 1.1 vs 2.25 PFLOP/s dense)
+        peak_sus, peak_burst = peak_sus / 2, peak_burst / 2
     # dominant kernel: the launch class with the most time. Classes: 5 = a whole
     # product in one launch; 1 = Stages 1-2 of a rectangle and 2 = its final
     # products (two launches per rectangle); 0 = Stage 1 alone (diagnostic split).
@@ -294,10 +306,11 @@ def main():
     class_flops = {5: flops_step, 2: fl[2], 1: fl[0] + fl[1], 0: fl[0]}
     if os.environ.get("TLR_SPLIT_LAUNCHES") == "1":
         class_flops[1] = fl[1]
-    names = {5: "tlr_task_gemm<bf16>: Stages 1-3 and the dense-tile terms of a product in one persistent launch",
-             2: "tlr_task_gemm<bf16, CTA pairs>: final products (Stage 3 and the dense-tile segment) of a rectangle",
-             1: "tlr_task_gemm<bf16, single CTAs>: Stages 1-2 and the dense precomputes of a rectangle",
-             0: "tlr_task_gemm<bf16>: Stage 1"}
+    et = {"bf16": "bf16", "f16": "fp16", "f32": "tf32"}[p.dtype]
+    names = {5: f"tlr_task_gemm<{et}>: Stages 1-3 and the dense-tile terms of a product in one persistent launch",
+             2: f"tlr_task_gemm<{et}, CTA pairs>: final products (Stage 3 and the dense-tile segment) of a rectangle",
+             1: f"tlr_task_gemm<{et}, single CTAs>: Stages 1-2 and the dense precomputes of a rectangle",
+             0: f"tlr_task_gemm<{et}>: Stage 1"}
     dom = max((k for k in (5, 2, 1, 0) if kern[k][1]), key=lambda k: kern[k][0], default=None)
     roof = None
     if dom is not None:
@@ -306,23 +319,28 @@ def main():
         per_launch_flops = class_flops[dom] / launches_per_step
         avg_ms = k_ms / k_n
         achieved = per_launch_flops / (avg_ms * 1e-3) / 1e12
-        same = args.scale_down == 1 and sources_sha256() == TRAFFIC["sources_sha256"]
+        same = main_workload and args.scale_down == 1 and sources_sha256() == TRAFFIC["sources_sha256"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
                 "frac": achieved / peak_sus, "traffic": TRAFFIC["bytes_per_launch"] if same else None,
                 "traffic_unit": "bytes per launch (DRAM read + write)",
-                "algorithmic_bytes": TRAFFIC["algorithmic_bytes_per_launch"],
+                "algorithmic_bytes": TRAFFIC["algorithmic_bytes_per_launch"] if main_workload else None,
                 "kernel": names[dom] + " (executed FLOPs per launch / mean launch time)",
                 "launches_per_step": launches_per_step,
-                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside back-to-back steps)",
+                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside back-to-back steps)"
+                               + ("; tf32 = bf16 x 1.1/2.25" if p.dtype == "f32" else ""),
                 "frac_of_burst": achieved / peak_burst}
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if main_workload else "TLR GEMM executed TFLOP/s (pages' skewed-rank 8x8 grid)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD if args.scale_down == 1 else p.name, "N": p.m, "b": p.A.b, "tile_grid": [p.m // p.A.b, p.n // p.A.b],
-                   "ranks": "clamp(round(256 exp(-|i-j|/4)), 8, 256)", "alpha": p.alpha, "beta": p.beta,
+        "vs_baseline": None, "dtype": p.dtype, "data": "synthetic",
+        "config": {"workload": WORKLOAD if main_workload and args.scale_down == 1 else p.name, "N": p.m, "b": p.A.b,
+                   "tile_grid": [p.m // p.A.b, p.n // p.A.b],
+                   "ranks": "clamp(round(256 exp(-|i-j|/4)), 8, 256)" if main_workload else
+                            "b/32 + floor((b/32 + 1) u^2), u ~ U[0,1), on [b/32, b/16]",
+                   "alpha": p.alpha, "beta": p.beta,
                    "workspace_budget_bytes": p.budget, "runs": info["runs"], "order": order,
-                   "l2": "inputs larger than L2 (C alone is 4.3 GB; factors 0.42 GB)",
+                   "l2": f"inputs larger than L2 (C alone is {p.m * p.n * 4 / 1e9:.1f} GB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": {"burst": value / world / peak_burst, "sustained": value / world / peak_sus,
                         "source": peak_src},

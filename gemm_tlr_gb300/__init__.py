@@ -8,7 +8,7 @@ and builds the operand descriptors, and ``flops`` counts executed FLOPs from
 ranks for the benchmark's metric.
 """
 from ._abi import (  # noqa: F401
-    TLR_BF16, TLR_F32, TLR_KIND_DENSE, TLR_KIND_TLR, TLR_OP_N, TLR_OP_T, TLR_ORDER_AUTO,
+    TLR_BF16, TLR_F16, TLR_F32, TLR_KIND_DENSE, TLR_KIND_TLR, TLR_OP_N, TLR_OP_T, TLR_ORDER_AUTO,
     TLR_ORDER_LEFT, TLR_ORDER_RIGHT, TLRError, header_symbols, lib, tlr_analysis_t,
     tlr_analyze, tlr_create, tlr_debug_check_plan, tlr_debug_unsatisfied_wait, tlr_destroy, tlr_gemm,
     tlr_gemm_static_scratch, tlr_gemm_workspace_bytes, tlr_get_device_status, tlr_get_timing, tlr_operand_t,

@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(HERE, "libtlrgemm.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "tlr_gemm.h")
 
 TLR_OP_N, TLR_OP_T = 0, 1
-TLR_F32, TLR_BF16 = 0, 1
+TLR_F32, TLR_BF16, TLR_F16 = 0, 1, 2
 TLR_KIND_TLR, TLR_KIND_DENSE = 0, 1
 TLR_ORDER_AUTO, TLR_ORDER_RIGHT, TLR_ORDER_LEFT = 0, 1, 2
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "ALIGNMENT", 3: "WORKSPACE_TOO_SMALL", 4: "UNSUPPORTED",

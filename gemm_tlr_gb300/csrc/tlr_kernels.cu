@@ -25,6 +25,7 @@
 // in the device error word, drains its own copies and MMAs, frees TMEM, exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -233,12 +234,14 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   return d;
 }
 
-// Instruction descriptor for kind::f16 (bf16 inputs) / kind::tf32, fp32 D.
-__device__ __forceinline__ uint32_t idesc(bool tf32, bool a_mn, bool b_mn, uint32_t n, uint32_t m = kBM) {
+// Instruction descriptor for kind::f16 (fp16 or bf16 inputs, both operands the
+// same type) / kind::tf32, fp32 D.
+__device__ __forceinline__ uint32_t idesc(bool tf32, bool f16, bool a_mn, bool b_mn, uint32_t n, uint32_t m = kBM) {
+  const uint32_t fmt = tf32 ? 2u : (f16 ? 0u : 1u);   // tf32 / f16 / bf16
   uint32_t d = 0;
   d |= 1u << 4;                                   // D format: f32
-  d |= (tf32 ? 2u : 1u) << 7;                     // A format: tf32 / bf16
-  d |= (tf32 ? 2u : 1u) << 10;                    // B format
+  d |= fmt << 7;                                  // A format
+  d |= fmt << 10;                                 // B format
   d |= (a_mn ? 1u : 0u) << 15;                    // A major: 0 K, 1 MN
   d |= (b_mn ? 1u : 0u) << 16;                    // B major
   d |= (n >> 3) << 17;                            // N / 8
@@ -327,6 +330,15 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// One value as a 16-bit float (fp16 or bf16, round to nearest even), as raw bits.
+__device__ __forceinline__ uint16_t to16(float x, bool f16) {
+  return f16 ? __half_as_ushort(__float2half_rn(x)) : __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+// Two values as a packed pair of 16-bit floats (low half: a).
+__device__ __forceinline__ uint32_t pack16x2(float a, float b, bool f16) {
+  return static_cast<uint32_t>(to16(a, f16)) | (static_cast<uint32_t>(to16(b, f16)) << 16);
 }
 
 __device__ __forceinline__ float round_tf32(float x) {
@@ -459,22 +471,20 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
     }
     return;
   }
-  if (o.kind == kOutBF16 && o.trans && nc == 32) {
-    // Row-major bf16 output through shared memory: each lane parks its row's
+  const bool half16 = o.kind == kOutBF16 || o.kind == kOutF16;   // 16-bit workspace output
+  if (half16 && o.trans && nc == 32) {
+    // Row-major 16-bit output through shared memory: each lane parks its row's
     // 64 bytes (16-byte chunks XOR-swizzled by row pair, so neither the writes
     // nor the reads conflict on banks); then each store instruction writes
     // 8 rows x 64 contiguous bytes instead of 32 rows x 16 bytes.
-    __nv_bfloat16 *W = static_cast<__nv_bfloat16 *>(o.ptr);
+    uint16_t *W = static_cast<uint16_t *>(o.ptr);
     if (p.cmap_ok) {   // an earlier bulk store may still be reading the staging area
       if (lane == 0) bulk_wait_read();
       __syncwarp();
     }
     uint32_t pk[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-      pk[i] = *reinterpret_cast<const uint32_t *>(&h2);
-    }
+    for (int i = 0; i < 16; ++i) pk[i] = pack16x2(v[2 * i], v[2 * i + 1], o.kind == kOutF16);
 #pragma unroll
     for (int c = 0; c < 4; ++c)
       *reinterpret_cast<uint4 *>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
@@ -506,16 +516,17 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
         C[off] = val;
       }
     }
-  } else if (o.kind == kOutBF16) {
-    __nv_bfloat16 *W = static_cast<__nv_bfloat16 *>(o.ptr);
+  } else if (half16) {
+    uint16_t *W = static_cast<uint16_t *>(o.ptr);
+    const bool f16 = o.kind == kOutF16;
     if (o.trans) {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        if (i < nc) W[drow * o.ld + c0 + i] = __float2bfloat16_rn(v[i]);
+        if (i < nc) W[drow * o.ld + c0 + i] = to16(v[i], f16);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        if (i < nc) W[drow + (c0 + i) * o.ld] = __float2bfloat16_rn(v[i]);
+        if (i < nc) W[drow + (c0 + i) * o.ld] = to16(v[i], f16);
     }
   } else {
     float *W = static_cast<float *>(o.ptr);
@@ -799,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
         for (int s = 0; ok && s < nseg; ++s) {
           const Seg sg = sl.segs[s];
           const bool a_mn = sg.flags & kSegAMN, b_mn = sg.flags & kSegBMN;
-          const uint32_t id = idesc(kTF32, a_mn, b_mn, static_cast<uint32_t>(bn), kBM * kPair);
+          const uint32_t id = idesc(kTF32, p.f16 != 0, a_mn, b_mn, static_cast<uint32_t>(bn), kBM * kPair);
           const int nkb = (sg.k_len + kBK - 1) / kBK;
           // Descriptors of stage 0; a stage is kStB bytes further, an MMA step 32 bytes
           // (K-major: the next K slice of each 128-byte swizzled row) or kUK rows of

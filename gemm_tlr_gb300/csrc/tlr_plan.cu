@@ -132,14 +132,14 @@ struct Operand {                       // validated descriptor plus device base 
   int64_t u_elems = 0, v_elems = 0, d_elems = 0, buU = 0, buV = 0, bvU = 0, bvV = 0, g_elems = 0;
 };
 
-int elem_size(int dtype) { return dtype == TLR_BF16 ? 2 : 4; }
+int elem_size(int dtype) { return dtype == TLR_F32 ? 4 : 2; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Compute stored geometry, packed offsets and the element count of each buffer.
 tlr_status_t describe(const tlr_operand_t &d, Operand &o, bool check_pointers) {
   o.d = d;
-  if (d.dtype != TLR_F32 && d.dtype != TLR_BF16) return TLR_STATUS_INVALID_ARG;
+  if (d.dtype != TLR_F32 && d.dtype != TLR_BF16 && d.dtype != TLR_F16) return TLR_STATUS_INVALID_ARG;
   if (d.rows <= 0 || d.cols <= 0) return TLR_STATUS_INVALID_ARG;
   const int es = elem_size(d.dtype);
   const int amod = 16 / es;
@@ -427,6 +427,7 @@ struct Builder {
   double fl_s1 = 0, fl_s2 = 0, fl_s3 = 0, fl_dense = 0;
   double fl_launch[3] = {0, 0, 0};      // the same FLOPs by launch class
   bool dry = false;                     // validate only: no tensor maps are encoded
+  bool f16 = false;                     // 16-bit operands and workspace are fp16 (else bf16)
   std::vector<std::pair<View, int>> *views = nullptr;   // every map's view and majorness
   // TF32 operands are read K-major only: a caller view that would be read
   // MN-major is replaced by its transposed copy (made by the pre-pass).
@@ -479,7 +480,8 @@ struct Builder {
     cuuint32_t estr[2] = {1, 1};
     auto fn = encode_fn();
     if (!fn || v.rows <= 0 || v.cols <= 0) { status = TLR_STATUS_CUDA_ERROR; return 0; }
-    CUresult r = fn(&m, es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+    CUresult r = fn(&m, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                : (f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16), 2,
                     reinterpret_cast<void *>(v.addr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -519,7 +521,7 @@ struct Builder {
     Out o;
     o.ptr = reinterpret_cast<void *>(ptr);
     o.ld = ld;
-    o.kind = tf32 ? kOutTF32 : kOutBF16;
+    o.kind = tf32 ? kOutTF32 : (f16 ? kOutF16 : kOutBF16);
     o.trans = trans ? 1 : 0;
     outs->push_back(o);
     return static_cast<int>(outs->size()) - 1;
@@ -933,6 +935,7 @@ struct tlr_handle_s {
 struct tlr_plan_s {
   tlr_handle_t h = nullptr;
   bool tf32 = false;
+  bool f16 = false;                       // 16-bit operands are fp16 (else bf16)
   int bn = 256;
   int pair = 1;
   int64_t Cm = 0, Cn = 0;                 // dimensions of C
@@ -1298,7 +1301,7 @@ double task_cost(const Task &t, const std::vector<Seg> &segs, const std::vector<
   int64_t k = 0;
   for (int q = 0; q < t.nseg; ++q) k += segs[t.seg0 + q].k_len;
   const double mma = static_cast<double>(bn) * static_cast<double>(k) / 32.0;
-  const int ob = outs[t.out].kind == kOutBF16 ? 2 : 4;
+  const int ob = (outs[t.out].kind == kOutBF16 || outs[t.out].kind == kOutF16) ? 2 : 4;
   const double st = static_cast<double>(t.rows) * t.cols * ob / 32.0;
   return std::max(mma, st) + 200.0;
 }
@@ -1338,6 +1341,7 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
     RectLayout L = layout_rect(X, Y, i0, i1, j0, j1, es);
     const uint64_t arena = ws + static_cast<uint64_t>(pc.fixed + (static_cast<int64_t>(ri) % narenas) * arena_bytes);
     Builder B{X, Y, es, tf32, tb.bn, r.left, arena, &tb.maps, &tb.map_index, nullptr, &tb.segs, &tb.pieces, &tb.outs};
+    B.f16 = pc.pv.dtype == TLR_F16;
     B.dry = dry;
     B.views = &tb.views;
     B.tcopy = &pc.tcopy;
@@ -1865,6 +1869,7 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
   if (!p) return TLR_STATUS_INVALID_ARG;
   p->h = h;
   p->tf32 = tf32;
+  p->f16 = pc.pv.dtype == TLR_F16;
   p->Cm = pc.pv.Cm;
   p->Cn = pc.pv.Cn;
   p->round_src = pc.round_src;
@@ -2033,6 +2038,7 @@ tlr_status_t tlr_plan_execute(tlr_plan_t p, float alpha, float beta, float *C, i
   prm.err = h->d_err;
   prm.wait_limit_ns = h->wait_limit_ns;
   prm.cmap_ok = encode_c_maps(prm, C, ldc, p->Cm, p->Cn) ? 1 : 0;
+  prm.f16 = p->f16 ? 1 : 0;
   // one ticket per launch, then the dependency counters; all start at zero
   prm.counters = p->d_counters + p->launches.size();
   if (cudaMemsetAsync(p->d_counters, 0, p->counters_bytes, h->stream) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
@@ -2102,6 +2108,7 @@ tlr_status_t tlr_gemm_static_scratch(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB,
   tlr_plan_s p;
   p.h = h;
   p.tf32 = pc.pv.dtype == TLR_F32;
+  p.f16 = pc.pv.dtype == TLR_F16;
   p.Cm = pc.pv.Cm;
   p.Cn = pc.pv.Cn;
   p.round_src = pc.round_src;

@@ -67,6 +67,7 @@ enum : int32_t {
   kOutC = 0,        // fp32 C: alpha * acc + beta * C (C unread when beta == 0)
   kOutBF16 = 1,     // workspace, bf16 round-to-nearest-even
   kOutTF32 = 2,     // workspace, fp32 rounded to nearest tf32
+  kOutF16 = 3,      // workspace, fp16 round-to-nearest-even
 };
 
 struct alignas(16) Out {
@@ -114,6 +115,7 @@ struct Params {
   // Used when cmap_ok is set and beta == 0.
   CUtensorMap cmap[2];
   int32_t cmap_ok;
+  int32_t f16;            // 16-bit operands are fp16 (else bf16); the TF32 kernel ignores it
   const void *maps;       // CUtensorMap[], 64-byte aligned, device memory
   const Task *tasks;
   const Seg *segs;

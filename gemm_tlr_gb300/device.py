@@ -15,11 +15,21 @@ from . import _abi
 _BUFS = ("U", "V", "D", "bu_U", "bu_V", "bv_U", "bv_V", "gamma")
 
 
+_DTYPES = {"f32": 0, "bf16": 1, "f16": 2}   # tlr_dtype_t
+
+
+def elem_bytes(dtype: str) -> int:
+    return 4 if dtype == "f32" else 2
+
+
 def _as_torch(a: np.ndarray, dtype: str):
+    """Device-upload copy of float32 values that are exact in ``dtype``."""
     import torch
     if dtype == "bf16":
         bits = (np.ascontiguousarray(a, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
         return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    if dtype == "f16":
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32).astype(np.float16))
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
 
 
@@ -27,7 +37,7 @@ def host_descriptor(X) -> tuple:
     """Descriptor with ranks only (no device pointers): for tlr_analyze and sizing."""
     d = _abi.tlr_operand_t()
     keep = []
-    d.dtype = _abi.TLR_BF16 if X.dtype == "bf16" else _abi.TLR_F32
+    d.dtype = _DTYPES[X.dtype]
     d.rows, d.cols = X.rows, X.cols
     if X.kind == "dense":
         d.kind, d.ld = _abi.TLR_KIND_DENSE, X.rows
@@ -146,6 +156,6 @@ def fake_descriptor(X, base: int) -> tuple:
         if a is None or a.size == 0:
             continue
         setattr(d, name, addr)
-        es = 2 if X.dtype == "bf16" else 4
+        es = elem_bytes(X.dtype)
         addr += ((a.size * es + 4095) // 4096) * 4096
     return d, keep

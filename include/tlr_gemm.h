@@ -36,11 +36,13 @@
  *     never frees or reallocates them. Rank and offset arrays are HOST pointers,
  *     read during the call (a plan keeps its own copy).
  *   - Element types: fp32 (run on TF32 tensor cores, inputs rounded to nearest
- *     TF32 first) or bf16 (tensor cores, fp32 accumulation). Both operands of
- *     one product have the same element type. C is always fp32.
+ *     TF32 first), bf16 or fp16 (tensor cores, fp32 accumulation; the
+ *     intermediate S, T and P products are kept in the input type, rounded to
+ *     nearest even). Both operands of one product have the same element type.
+ *     C is always fp32.
  *   - Alignment: every base pointer 16-byte aligned; every leading dimension
  *     (and each tile's dense dimension) times the element size a multiple of 16
- *     bytes (d % 4 == 0 for fp32, d % 8 == 0 for bf16); ldc % 4 == 0.
+ *     bytes (d % 4 == 0 for fp32, d % 8 == 0 for bf16 and fp16); ldc % 4 == 0.
  *     Violations return TLR_STATUS_ALIGNMENT before anything is launched.
  *   - Calls are asynchronous on the handle's stream (BLAS convention). A
  *     status other than TLR_STATUS_OK means nothing was launched, except
@@ -71,7 +73,7 @@ typedef enum {
 } tlr_status_t;
 
 typedef enum { TLR_OP_N = 0, TLR_OP_T = 1 } tlr_op_t;
-typedef enum { TLR_F32 = 0, TLR_BF16 = 1 } tlr_dtype_t;
+typedef enum { TLR_F32 = 0, TLR_BF16 = 1, TLR_F16 = 2 } tlr_dtype_t;
 typedef enum { TLR_KIND_TLR = 0, TLR_KIND_DENSE = 1 } tlr_kind_t;
 typedef enum { TLR_ORDER_AUTO = 0, TLR_ORDER_RIGHT = 1, TLR_ORDER_LEFT = 2 } tlr_order_t;
 

@@ -178,3 +178,28 @@ def test_workspace_bytes_gives_the_requested_runs(g):
         if prev is not None:
             assert need <= prev
         prev = need
+
+
+def test_fp16_descriptors_plan_and_check_like_bf16(g):
+    """fp16 operands: accepted, 16-byte rule on tile dimensions (d % 8), mixed 16-bit types rejected,
+    and the plan tables of fp16 workloads pass the host-side proof."""
+    from gemm_tlr_gb300.device import fake_descriptor
+    rng = np.random.default_rng(3)
+    X = ti.make_tlr(rng, 256, 64, ti.rank_fixed(8), "f16")
+    A, ka = fake_descriptor(X, 1 << 40)
+    B, kb = fake_descriptor(X, 1 << 41)
+    assert A.dtype == g.TLR_F16
+    assert g.tlr_debug_check_plan(0, 0, A, B, 1 << 30)[0] == 0
+    Y = ti.make_tlr(rng, 260, 65, ti.rank_fixed(8), "f16")       # tile dimension not a multiple of 8
+    Yd, ky = fake_descriptor(Y, 1 << 42)
+    assert g.tlr_debug_check_plan(0, 0, Yd, Yd, 1 << 30)[0] == 2
+    Z = ti.make_tlr(rng, 256, 64, ti.rank_fixed(8), "bf16")
+    Zd, kz = fake_descriptor(Z, 1 << 42)
+    assert g.tlr_debug_check_plan(0, 0, A, Zd, 1 << 30)[0] == 4       # fp16 x bf16: mixed element types
+    for p in (ti.problem(5, scale_down=8, dtype_override="f16"), ti.problem(4, scale_down=8, dtype_override="f16"),
+              ti.skewed_grid(2048, "f16")):
+        Ad, ka2 = fake_descriptor(p.A, 1 << 40)
+        Bd, kb2 = fake_descriptor(p.B, 1 << 44)
+        ws = p.budget or g.tlr_gemm_workspace_bytes(0, 0, 0, Ad, Bd, 1)
+        st, msg, info = g.tlr_debug_check_plan(0, 0, Ad, Bd, ws)
+        assert st == 0, (p.name, msg)

@@ -233,3 +233,44 @@ def test_planted_mistakes_are_caught(oracle_lib, tmp_path, code):
     with oracle_lib.use_library(path):
         out = oracle_lib.gemm_block(A, B, "N", "N", 1.0, 0.5, C, N, np.arange(N), np.arange(N))
     assert rel(out, ref) > 1e-3
+
+
+def test_f16_rounding_is_nearest_even():
+    """fp16 inputs: 10 stored mantissa bits, ties to even (checked on exact ties)."""
+    one = np.float32(1.0)
+    x = np.array([1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, -(1 + 2.0 ** -11), 65504.0, 2.0 ** -24], dtype=np.float32)
+    got = ti.f16_round(x)
+    assert got[0] == one                      # tie between 1 and 1 + 2^-10: the even one
+    assert got[1] == np.float32(1 + 2.0 ** -9)  # tie between 1 + 2^-10 and 1 + 2^-9: the even one
+    assert got[2] == -one
+    assert got[3] == np.float32(65504.0)      # largest finite fp16
+    assert got[4] == np.float32(2.0 ** -24)   # smallest subnormal survives
+    p = ti.skewed_grid(1024, "f16")
+    for a in (p.A.U, p.A.V, p.A.D, p.B.U):
+        assert np.array_equal(a, a.astype(np.float16).astype(np.float32))
+
+
+def test_skewed_ranks_stay_in_range_and_lean_low():
+    """The pages' second workload: 8 x 8 tiles, ranks on [b/32, b/16], skewed towards b/32."""
+    p = ti.skewed_grid(8192, "f32")
+    b = p.A.b
+    assert b == 1024 and p.A.ranks.shape == (8, 8)
+    for X in (p.A, p.B):
+        off = X.ranks[~np.eye(8, dtype=bool)]
+        assert off.min() >= b // 32 and off.max() <= b // 16
+        assert np.all(np.diag(X.ranks) == 0)            # dense diagonal
+    r = ti.rank_skewed(256, 512)(np.random.default_rng(0), 200, 200, None, None)
+    assert r.min() == 256 and r.max() == 512
+    assert abs(r.mean() - (256 + 257 / 3)) < 2.0          # E[lo + (hi-lo+1) u^2] = lo + (hi-lo+1)/3
+    assert np.median(r) < 256 + 257 / 2                   # more mass below the midpoint
+    q = ti.skewed_grid(8192, "f32")
+    assert np.array_equal(q.A.ranks, p.A.ranks)           # seeded
+
+
+def test_oracle_matches_brute_force_on_fp16_skewed_grid(oracle_lib):
+    """fp16 inputs on the 8 x 8 skewed-rank grid: oracle against a numpy product of the
+    dense reconstruction (every value is fp16-exact, so the check is dtype-independent)."""
+    p = ti.skewed_grid(512, "f16", keep_tiles=True)
+    ref = dense_from_tiles(p.A) @ dense_from_tiles(p.B)
+    got = oracle_lib.gemm_problem(p)
+    assert np.max(np.abs(got - ref)) <= 1e-12 * np.max(np.abs(ref))

@@ -1,0 +1,66 @@
+"""GPU parity for fp16 operands and for the pages' skewed-rank 8 x 8 workload.
+
+fp16 keeps 10 stored mantissa bits against bf16's 7, so its rounding errors are 8x
+smaller; the products keep fp32 accumulation and an fp16 S, T and P. The
+tolerance below is the bf16 bound (1e-2) scaled by that ratio with a 2x margin
+(2.5e-3). The skewed workload runs in fp32 (TF32), bf16 and fp16, at sizes the
+oracle computes whole and, for fp16, at the pages' largest size on sampled
+entries.
+"""
+import numpy as np
+import pytest
+
+import tlr_inputs as ti
+from test_parity_gpu import TOL as _TOL, handle, rel, run, sample_indices, torch_cuda  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+TOL = dict(_TOL, f16=2.5e-3)
+
+
+@pytest.mark.parametrize("cfg,scale", [(4, 8), (4, 4), (5, 8), (5, 4)])
+@pytest.mark.parametrize("variant", ["whole", "lowrank_only", "dense_only"])
+def test_fp16_workloads_match_oracle(oracle_lib, handle, cfg, scale, variant):
+    kw = {}
+    if variant == "lowrank_only":
+        kw = dict(zero_diag=True, beta_override=0.0)
+    elif variant == "dense_only":
+        kw = dict(zero_lowrank=True)
+    p = ti.problem(cfg, scale_down=scale, dtype_override="f16", **kw)
+    out, info = run(p, handle)
+    err = rel(out, oracle_lib.gemm_problem(p))
+    print(f"{p.name} {variant}: {err:.3e}")
+    assert np.isfinite(out).all() and err <= TOL["f16"], f"{p.name}: rel Frobenius {err:.3e}"
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("n", [2048, 4096])
+def test_skewed_grid_matches_oracle(oracle_lib, handle, dtype, n):
+    p = ti.skewed_grid(n, dtype)
+    out, info = run(p, handle)
+    err = rel(out, oracle_lib.gemm_problem(p))
+    print(f"{p.name}: {err:.3e}")
+    assert np.isfinite(out).all() and err <= TOL[dtype], f"{p.name}: rel Frobenius {err:.3e}"
+
+
+@pytest.mark.parametrize("n", [65536])
+def test_skewed_grid_largest_fp16_sampled(oracle_lib, handle, n):
+    """The pages' largest fp16 case (N = 65536, b = 8192) on sampled rows and columns of every tile."""
+    p = ti.skewed_grid(n, "f16")
+    out_rows = sample_indices(p.m, p.A.b, seed=1)
+    out_cols = sample_indices(p.n, p.A.b, seed=2)
+    import gemm_tlr_gb300 as g
+    from gemm_tlr_gb300.device import DeviceProblem
+    dp = DeviceProblem(p)
+    try:
+        dp.make_plan(handle)
+        dp.run()
+        assert g.tlr_get_device_status(handle) == 0
+        import torch
+        Cd = dp.C.view(p.n, p.m)                          # column-major: Cd[col, row]
+        sub = Cd[torch.as_tensor(out_cols, device=Cd.device)][:, torch.as_tensor(out_rows, device=Cd.device)]
+        got = sub.double().cpu().numpy().T
+    finally:
+        dp.close()
+    err = rel(got, oracle_lib.gemm_problem(p, out_rows, out_cols))
+    print(f"{p.name} sampled: {err:.3e}")
+    assert np.isfinite(got).all() and err <= TOL["f16"], f"{p.name}: sampled rel Frobenius {err:.3e}"

@@ -27,9 +27,9 @@ Multiplication", section "Introduction: TLR GEMM"):
   the boundary column packed by ascending ``i``, ``bv_U``/``bv_V`` those of the
   boundary row packed by ascending ``j``.
 
-All arrays are float32 numpy arrays. For bf16 inputs the values are rounded to
-bf16 (round-to-nearest-even) and kept as float32 holding bf16-exact values;
-``bf16_bits`` turns them into the 16-bit payload for upload.
+All arrays are float32 numpy arrays. For bf16 and fp16 inputs the values are
+rounded to that type (round-to-nearest-even) and kept as float32 holding exact
+values of it; ``bf16_bits`` turns bf16 values into the 16-bit payload for upload.
 """
 from __future__ import annotations
 
@@ -40,9 +40,10 @@ from typing import Callable, Dict, Optional, Tuple
 import numpy as np
 
 __all__ = [
-    "bf16_round", "bf16_bits", "TLRMatrix", "DenseMatrix", "Problem",
+    "bf16_round", "f16_round", "bf16_bits", "TLRMatrix", "DenseMatrix", "Problem",
     "make_tlr", "make_dense", "problem", "CONFIG_NAMES", "tile_dims",
-    "rank_fixed", "rank_uniform", "rank_inverse_distance", "rank_exp_decay",
+    "rank_fixed", "rank_uniform", "rank_inverse_distance", "rank_exp_decay", "rank_skewed",
+    "skewed_grid",
 ]
 
 
@@ -53,6 +54,11 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
     u = x.view(np.uint32).astype(np.uint64)
     r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
     return r.astype(np.uint32).view(np.float32)
+
+
+def f16_round(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest fp16 (ties to even); returns float32."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).astype(np.float32)
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -75,7 +81,7 @@ class TLRMatrix:
     b: int
     diag_dense: bool
     ranks: np.ndarray              # (nt_r, nt_c) int32, dense tiles hold 0
-    dtype: str                     # "f32" or "bf16"
+    dtype: str                     # "f32", "bf16" or "f16"
     U: np.ndarray
     V: np.ndarray
     D: Optional[np.ndarray] = None         # b*b*m, tile i at i*b*b
@@ -101,7 +107,7 @@ class TLRMatrix:
         return tile_dims(self.cols, self.b)
 
     def nbytes_device(self) -> int:
-        es = 2 if self.dtype == "bf16" else 4
+        es = 4 if self.dtype == "f32" else 2
         n = 0
         for a in (self.U, self.V, self.D, self.bu_U, self.bu_V, self.bv_U, self.bv_V, self.gamma):
             if a is not None:
@@ -153,6 +159,19 @@ def rank_uniform(lo: int, hi: int) -> Callable:
     return f
 
 
+def rank_skewed(lo: int, hi: int) -> Callable:
+    """Independent ranks on [lo, hi], skewed towards lo: lo + floor((hi - lo + 1) u^2), u ~ U[0, 1).
+
+    The pages give only the interval and the word "skewed"; squaring a uniform
+    draw is the reading taken here (density falling linearly in sqrt, mean
+    lo + (hi - lo + 1) / 3).
+    """
+    def f(rng, nt_r, nt_c, rd, cd):
+        u = rng.random(size=(nt_r, nt_c))
+        return np.minimum(hi, lo + np.floor((hi - lo + 1) * u * u).astype(np.int64))
+    return f
+
+
 def _round_half_up(x: float) -> int:
     return int(math.floor(x + 0.5))
 
@@ -186,6 +205,8 @@ def _draw(rng, n: int, scale: float, dtype: str) -> np.ndarray:
         a *= np.float32(scale)
     if dtype == "bf16":
         a = bf16_round(a)
+    elif dtype == "f16":
+        a = f16_round(a)
     return a
 
 
@@ -303,9 +324,26 @@ CONFIG_NAMES = {
 }
 
 
+def skewed_grid(n: int, dtype: str, *, seed: int = 0, keep_tiles: bool = False, budget: Optional[int] = None) -> Problem:
+    """The pages' variable-rank workload: dense C <- TLR x TLR on an 8 x 8 tile
+    grid, b = n / 8, every off-diagonal tile with its own rank drawn from a
+    skewed distribution on [b/32, b/16] ("Tile-Low-Rank GEMM: Designing Storage
+    Around the Contraction", section "Results"), dense diagonal tiles, factors
+    ~N(0,1)/sqrt(b), dense tiles ~N(0,1), alpha = 1, beta = 0.
+    """
+    if n % 8 or (n // 8) % 32:
+        raise ValueError("n must be a multiple of 256")
+    rng = np.random.default_rng(seed)
+    b = n // 8
+    rule = rank_skewed(b // 32, b // 16)
+    A = make_tlr(rng, n, b, rule, dtype, keep_tiles=keep_tiles)
+    Bm = make_tlr(rng, n, b, rule, dtype, keep_tiles=keep_tiles)
+    return Problem(f"skewed_8x8_{dtype}_N{n}", A, Bm, "N", "N", 1.0, 0.0, None, n, n, dtype, budget=budget)
+
+
 def problem(cfg, *, seed: int = 0, keep_tiles: bool = False, scale_down: int = 1,
             zero_diag: bool = False, zero_lowrank: bool = False, beta_override=None,
-            alpha_override=None) -> Problem:
+            alpha_override=None, dtype_override: Optional[str] = None) -> Problem:
     """Build one of the five graded workloads (or a smaller member of its family).
 
     ``cfg`` is 1..5. ``scale_down`` > 1 divides N (and for config 4 the dense
@@ -313,7 +351,8 @@ def problem(cfg, *, seed: int = 0, keep_tiles: bool = False, scale_down: int = 1
     remainder ratio) so the oracle can run the whole product. ``zero_diag`` and
     ``zero_lowrank`` build the term-isolated variants (dense tiles, or every
     low-rank factor, replaced by zeros after drawing, so that the other values
-    are the same seeded draws).
+    are the same seeded draws). ``dtype_override`` ("f16" for the bf16
+    workloads) draws the same distributions rounded to another 16-bit type.
     """
     rng = np.random.default_rng(seed)
     kt = keep_tiles
@@ -343,18 +382,24 @@ def problem(cfg, *, seed: int = 0, keep_tiles: bool = False, scale_down: int = 1
     elif cfg == 4:
         N, b, W = 16384 // scale_down, 1024 // scale_down, 4096 // scale_down
         lo, hi = (16, 256) if scale_down == 1 else (max(1, 16 // scale_down), max(2, 256 // scale_down))
-        A = make_tlr(rng, N, b, rank_uniform(lo, hi), "bf16", keep_tiles=kt)
-        Bm = make_dense(rng, N, W, "bf16")
-        p = Problem(CONFIG_NAMES[4], A, Bm, "N", "N", 1.0, 0.0, None, N, W, "bf16")
+        dt = dtype_override or "bf16"
+        A = make_tlr(rng, N, b, rank_uniform(lo, hi), dt, keep_tiles=kt)
+        Bm = make_dense(rng, N, W, dt)
+        p = Problem(CONFIG_NAMES[4], A, Bm, "N", "N", 1.0, 0.0, None, N, W, dt)
     elif cfg == 5:
         N, b = 32768 // scale_down, 1024 // scale_down
         rule = rank_exp_decay(256 / scale_down, 4.0, max(1, 8 // scale_down), 256 // scale_down)
-        A = make_tlr(rng, N, b, rule, "bf16", keep_tiles=kt)
-        Bm = make_tlr(rng, N, b, rule, "bf16", keep_tiles=kt)
+        dt = dtype_override or "bf16"
+        A = make_tlr(rng, N, b, rule, dt, keep_tiles=kt)
+        Bm = make_tlr(rng, N, b, rule, dt, keep_tiles=kt)
         budget = (2 << 30) // (scale_down * scale_down)
-        p = Problem(CONFIG_NAMES[5], A, Bm, "N", "N", 1.0, 0.0, None, N, N, "bf16", budget=budget)
+        p = Problem(CONFIG_NAMES[5], A, Bm, "N", "N", 1.0, 0.0, None, N, N, dt, budget=budget)
     else:
         raise ValueError(f"unknown config {cfg}")
+    if dtype_override is not None and cfg in (1, 2, 3):
+        raise ValueError("dtype_override applies to the 16-bit workloads (4, 5)")
+    if dtype_override is not None:
+        p.name = p.name.replace("bf16", dtype_override)
     if scale_down != 1:
         p.name += f"/scale{scale_down}"
     if zero_diag or zero_lowrank:
