@@ -336,9 +336,15 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 __device__ __forceinline__ uint16_t to16(float x, bool f16) {
   return f16 ? __half_as_ushort(__float2half_rn(x)) : __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
-// Two values as a packed pair of 16-bit floats (low half: a).
+// Two values as a packed pair of 16-bit floats (low half: a), one paired
+// conversion instruction either way.
 __device__ __forceinline__ uint32_t pack16x2(float a, float b, bool f16) {
-  return static_cast<uint32_t>(to16(a, f16)) | (static_cast<uint32_t>(to16(b, f16)) << 16);
+  if (f16) {
+    const __half2 h2 = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h2);
+  }
+  const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t *>(&h2);
 }
 
 __device__ __forceinline__ float round_tf32(float x) {
@@ -352,8 +358,12 @@ __device__ __forceinline__ float round_tf32(float x) {
 // 32 accumulator values of tile row 32q + l (columns c0 .. c0 + nc - 1 of the
 // output); `drow` is that row's destination (valid: the row is stored) and `stg`
 // is the warp's 2 KiB staging area in shared memory.
+// kRowIdx: rowd holds this lane's output rows for row-major 16-bit outputs
+// (resolved once per task); otherwise they are shuffled out per chunk.
+template <bool kRowIdx>
 __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, int64_t drow, bool valid,
-                                            const Params &p, const Out &o, int lane, uint8_t *stg) {
+                                            const Params &p, const Out &o, int lane, uint8_t *stg,
+                                            const int32_t (&rowd)[4], bool &bulk_live) {
   if (o.kind == kOutC) {
     // fp32 C through shared memory in two 16-column halves. The warp's block is
     // 32 rows x 16 columns of column-major C (tile rows are rows of C), or 16
@@ -376,9 +386,10 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
       for (int h = 0; h < 2; ++h) {
         const int nch = nc - 16 * h < 16 ? nc - 16 * h : 16;   // columns of this half
         if (nch <= 0) break;
-        if (p.cmap_ok) {   // an earlier bulk store may still be reading the staging area
+        if (bulk_live) {   // an earlier bulk store may still be reading the staging area
           if (lane == 0) bulk_wait_read();
           __syncwarp();
+          bulk_live = false;
         }
         if (!o.trans) {
 #pragma unroll
@@ -388,6 +399,7 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
             __syncwarp();
             if (lane == 0) tma_store_2d(&p.cmap[0], smem_u32(sf), static_cast<int32_t>(d0),
                                         static_cast<int32_t>(c0 + 16 * h), policy_evict_first());
+            bulk_live = true;
             continue;
           }
           __syncwarp();
@@ -416,6 +428,7 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
             __syncwarp();
             if (lane == 0) tma_store_2d(&p.cmap[1], smem_u32(stg), static_cast<int32_t>(c0 + 16 * h),
                                         static_cast<int32_t>(d0), policy_evict_first());
+            bulk_live = true;
             continue;
           }
           __syncwarp();
@@ -477,14 +490,19 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
     // 64 bytes (16-byte chunks XOR-swizzled by row pair, so neither the writes
     // nor the reads conflict on banks); then each store instruction writes
     // 8 rows x 64 contiguous bytes instead of 32 rows x 16 bytes.
-    uint16_t *W = static_cast<uint16_t *>(o.ptr);
-    if (p.cmap_ok) {   // an earlier bulk store may still be reading the staging area
+    if (bulk_live) {   // an earlier bulk store may still be reading the staging area
       if (lane == 0) bulk_wait_read();
       __syncwarp();
+      bulk_live = false;
     }
     uint32_t pk[16];
+    if (o.kind == kOutF16) {   // one conversion per branch, decided once per chunk
 #pragma unroll
-    for (int i = 0; i < 16; ++i) pk[i] = pack16x2(v[2 * i], v[2 * i + 1], o.kind == kOutF16);
+      for (int i = 0; i < 16; ++i) pk[i] = pack16x2(v[2 * i], v[2 * i + 1], true);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pk[i] = pack16x2(v[2 * i], v[2 * i + 1], false);
+    }
 #pragma unroll
     for (int c = 0; c < 4; ++c)
       *reinterpret_cast<uint4 *>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
@@ -495,10 +513,14 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
     for (int s = 0; s < 4; ++s) {
       const int r = 8 * s + (lane >> 2), c = lane & 3;
       const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
-      const int64_t d = __shfl_sync(0xffffffffu, valid ? drow : int64_t(-1), r);
-      // T is read by a later rectangle's final products, long after it would have
-      // left L2: its lines go first, ahead of the operands being reused now
-      if (d >= 0) st_global_evict_first(W + d * o.ld + c0 + 8 * c, val, pol);
+      // rowd[s]: output row of row 8s + lane/4 of this warp's block (-1: not
+      // stored), resolved once per task. T is read by a later rectangle's final
+      // products, long after it would have left L2: its lines go first, ahead
+      // of the operands being reused now.
+      int64_t d;
+      if constexpr (kRowIdx) d = rowd[s];
+      else d = __shfl_sync(0xffffffffu, valid ? drow : int64_t(-1), r);
+      if (d >= 0) st_global_evict_first(static_cast<uint16_t *>(o.ptr) + d * o.ld + c0 + 8 * c, val, pol);
     }
     __syncwarp();   // the staging area is reused by the next chunk
     return;
@@ -518,15 +540,22 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
     }
   } else if (half16) {
     uint16_t *W = static_cast<uint16_t *>(o.ptr);
-    const bool f16 = o.kind == kOutF16;
+    uint16_t h[32];
+    if (o.kind == kOutF16) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) h[i] = to16(v[i], true);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) h[i] = to16(v[i], false);
+    }
     if (o.trans) {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        if (i < nc) W[drow * o.ld + c0 + i] = to16(v[i], f16);
+        if (i < nc) W[drow * o.ld + c0 + i] = h[i];
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        if (i < nc) W[drow + (c0 + i) * o.ld] = to16(v[i], f16);
+        if (i < nc) W[drow + (c0 + i) * o.ld] = h[i];
     }
   } else {
     float *W = static_cast<float *>(o.ptr);
@@ -638,16 +667,33 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
     constexpr int kBatch = kTicketBatch;
     int n = 0;
     bool done = false;
+    // One CTA claims kBatch tickets at a time from the launch's counter. CTA
+    // pairs take their tickets in a fixed order: whole rounds of kBatch-ticket
+    // batches, then the remainder one ticket per pair in turn, so the pairs
+    // finish within about one task of each other (with batches throughout, the
+    // last round left half the pairs idle for up to kBatch final-product tiles).
+    const unsigned int ntasks = static_cast<unsigned int>(p.ntasks);
     for (uint32_t b = 0; !done; ++b) {
-      unsigned int t0 = 0;
+      unsigned int t0 = 0, cnt = kBatch;
       if (lane == 0) {
-        if constexpr (kPair == 1) t0 = atomicAdd(p.ticket, static_cast<unsigned int>(kBatch));
-        else t0 = static_cast<unsigned int>((blockIdx.x / 2 + static_cast<uint64_t>(b) * (gridDim.x / 2)) * kBatch);
+        if constexpr (kPair == 1) {
+          t0 = atomicAdd(p.ticket, cnt);
+        } else {
+          const unsigned int units = gridDim.x / 2, unit = blockIdx.x / 2;
+          const unsigned int rounds = ntasks / (kBatch * units);
+          if (b < rounds) {
+            t0 = (unit + b * units) * kBatch;
+          } else {
+            t0 = rounds * kBatch * units + unit + (b - rounds) * units;
+            cnt = 1;
+          }
+        }
       }
       t0 = __shfl_sync(0xffffffffu, t0, 0);
+      cnt = __shfl_sync(0xffffffffu, cnt, 0);
       Task mine;
-      if (lane < kBatch && t0 + lane < static_cast<unsigned int>(p.ntasks)) mine = p.tasks[t0 + lane];
-      for (int j = 0; j < kBatch; ++j, ++n) {
+      if (lane < static_cast<int>(cnt) && t0 + lane < ntasks) mine = p.tasks[t0 + lane];
+      for (int j = 0; j < static_cast<int>(cnt); ++j, ++n) {
         const int r = n % kRing;
         const uint32_t ph = (n / kRing) & 1;
         Slot &sl = ring[r];
@@ -878,6 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
     // A warp publishes what it holds before it would block (next task not yet
     // staged, accumulator not yet ready), when the counter changes, and every
     // kSignalBatch tasks, so a dependency on its tasks can always be met.
+    bool bulk_live = false;               // this warp has bulk stores that may still read its staging area
     int32_t pend = -1;
     uint32_t pend_n = 0;
     bool pend_writes = false;
@@ -919,6 +966,14 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       if (pend != signal || pend_n >= kSignalBatch) flush();   // the earlier stores have had time to drain
       const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                               static_cast<uint32_t>(acc * kMaxBN);
+      // row-major 16-bit outputs: the output rows of this lane's four 16-byte
+      // pieces of every chunk (workspace rows fit in 32 bits)
+      int32_t rowd[4] = {-1, -1, -1, -1};
+      if (kPair == 1 && (o.kind == kOutBF16 || o.kind == kOutF16) && o.trans) {
+        const int32_t dr = valid ? static_cast<int32_t>(drow) : -1;
+#pragma unroll
+        for (int s4 = 0; s4 < 4; ++s4) rowd[s4] = __shfl_sync(0xffffffffu, dr, 8 * s4 + (lane >> 2));
+      }
       for (int cc = 64 * grp; cc < ncols; cc += 64 * kEpiGroups) {
         float v64[64];
         if (has_acc) {
@@ -934,7 +989,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = v64[32 * h + i];
-          store_chunk(v, ncols - c < 32 ? ncols - c : 32, col0 + c, drow, valid, p, o, lane, stg);
+          store_chunk<kPair == 1>(v, ncols - c < 32 ? ncols - c : 32, col0 + c, drow, valid, p, o, lane, stg, rowd, bulk_live);
         }
       }
       // every lane's TMEM reads are complete; one arrival per warp hands the

@@ -1339,6 +1339,7 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
     const int i0 = r.left ? r.j0 : r.i0, i1 = r.left ? r.j1 : r.i1;
     const int j0 = r.left ? r.i0 : r.j0, j1 = r.left ? r.i1 : r.j1;
     RectLayout L = layout_rect(X, Y, i0, i1, j0, j1, es);
+    if (L.Trows >= INT32_MAX) return TLR_STATUS_UNSUPPORTED;   // the epilogue holds T rows in 32 bits
     const uint64_t arena = ws + static_cast<uint64_t>(pc.fixed + (static_cast<int64_t>(ri) % narenas) * arena_bytes);
     Builder B{X, Y, es, tf32, tb.bn, r.left, arena, &tb.maps, &tb.map_index, nullptr, &tb.segs, &tb.pieces, &tb.outs};
     B.f16 = pc.pv.dtype == TLR_F16;
