@@ -64,3 +64,33 @@ def test_skewed_grid_largest_fp16_sampled(oracle_lib, handle, n):
     err = rel(got, oracle_lib.gemm_problem(p, out_rows, out_cols))
     print(f"{p.name} sampled: {err:.3e}")
     assert np.isfinite(got).all() and err <= TOL["f16"], f"{p.name}: sampled rel Frobenius {err:.3e}"
+
+
+@pytest.mark.parametrize("opA,opB", [("N", "N"), ("N", "T"), ("T", "N"), ("T", "T")])
+def test_fp16_transposes_with_boundary(oracle_lib, handle, opA, opB):
+    """fp16 through every operand orientation, with a 72-wide boundary tile and beta != 0."""
+    rng = np.random.default_rng(31)
+    N, b = 456, 128
+    A = ti.make_tlr(rng, N, b, ti.rank_uniform(0, 40), "f16")
+    B = ti.make_tlr(rng, N, b, ti.rank_uniform(0, 40), "f16")
+    C = rng.standard_normal(N * N).astype(np.float32)
+    p = ti.Problem("transpose_f16", A, B, opA, opB, 0.75, -1.25, C, N, N, "f16")
+    out, _ = run(p, handle)
+    assert rel(out, oracle_lib.gemm_problem(p)) <= TOL["f16"]
+
+
+@pytest.mark.parametrize("left_dense", [True, False])
+def test_fp16_dense_operand(oracle_lib, handle, left_dense):
+    """A dense fp16 operand on either side of a TLR one (96-wide tiles, 72-wide boundary)."""
+    rng = np.random.default_rng(32)
+    if left_dense:
+        A = ti.make_dense(rng, 320, 456, "f16")
+        B = ti.make_tlr(rng, 456, 96, ti.rank_uniform(1, 48), "f16")
+        m, n = 320, 456
+    else:
+        A = ti.make_tlr(rng, 456, 96, ti.rank_uniform(1, 48), "f16")
+        B = ti.make_dense(rng, 456, 256, "f16")
+        m, n = 456, 256
+    p = ti.Problem("dense_tlr_f16", A, B, "N", "N", 1.0, 0.0, None, m, n, "f16")
+    out, _ = run(p, handle)
+    assert rel(out, oracle_lib.gemm_problem(p)) <= TOL["f16"]

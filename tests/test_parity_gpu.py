@@ -132,6 +132,22 @@ def test_small_budget_many_rectangles(oracle_lib, handle):
     assert rel(out, oracle_lib.gemm_problem(p)) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("runs", [1, 6])
+def test_merged_two_arena_schedule(oracle_lib, handle, monkeypatch, runs):
+    """The single merged launch of CTA pairs, where Stages 1-2 of rectangle r + 1 run
+    interleaved with the final products of rectangle r in a second arena."""
+    import gemm_tlr_gb300 as g
+    from gemm_tlr_gb300.device import host_descriptor
+    monkeypatch.setenv("TLR_HYBRID", "0")
+    p = ti.problem(5, scale_down=8)
+    A, ka = host_descriptor(p.A)
+    B, kb = host_descriptor(p.B)
+    budget = g.tlr_gemm_workspace_bytes(0, 0, 0, A, B, runs)
+    out, info = run(p, handle, budget=budget)
+    assert (info["runs"] == 1) == (runs == 1)
+    assert rel(out, oracle_lib.gemm_problem(p)) <= TOL["bf16"]
+
+
 @pytest.mark.parametrize("cfg,scale", [(5, 4), (3, 2), (2, 1)])
 def test_single_cta_tiles_match_oracle(oracle_lib, handle, monkeypatch, cfg, scale):
     """128-row tiles on single CTAs (cta_group::1) for products whose default is CTA pairs."""
