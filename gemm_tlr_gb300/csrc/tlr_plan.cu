@@ -40,6 +40,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <climits>
 #include <functional>
 #include <map>
 #include <new>
@@ -1322,6 +1323,33 @@ void interleave(const std::vector<Task> &a, const std::vector<Task> &b, const st
   }
 }
 
+// Counters whose waiting tasks all run in later launches than every task that
+// signals them: the kernel boundary already orders those stores before those
+// reads, so the signals (and their fences) and the waits are dropped.
+void drop_cross_launch_counters(Tables &tb) {
+  const size_t nc = tb.counter_counts.size();
+  if (nc == 0 || tb.launches.size() < 2) return;
+  std::vector<int> launch_of(tb.all.size(), 0);
+  for (size_t li = 0; li < tb.launches.size(); ++li)
+    for (int64_t t = tb.launches[li].t0; t < tb.launches[li].t1; ++t) launch_of[t] = static_cast<int>(li);
+  std::vector<int> last_sig(nc, -1), first_wait(nc, INT_MAX);
+  for (size_t ti = 0; ti < tb.all.size(); ++ti) {
+    const Task &t = tb.all[ti];
+    if (t.signal >= 0) last_sig[t.signal] = std::max(last_sig[t.signal], launch_of[ti]);
+    for (int d = 0; d < 2; ++d)
+      if (t.dep[d] >= 0) first_wait[t.dep[d]] = std::min(first_wait[t.dep[d]], launch_of[ti]);
+  }
+  std::vector<uint8_t> keep(nc);
+  for (size_t c = 0; c < nc; ++c) keep[c] = first_wait[c] <= last_sig[c];
+  for (Task &t : tb.all) {
+    if (t.signal >= 0 && !keep[t.signal]) { t.signal = -1; t.signal_writes = 0; }
+    for (int d = 0; d < 2; ++d)
+      if (t.dep[d] >= 0 && !keep[t.dep[d]]) { t.dep[d] = -1; t.dep_target[d] = 0; }
+  }
+  for (size_t c = 0; c < nc; ++c)
+    if (!keep[c]) tb.counter_counts[c] = 0;
+}
+
 tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, int narenas, uint64_t ws, bool dry,
                           Tables &tb) {
   const int es = elem_size(pc.pv.dtype);
@@ -1414,6 +1442,7 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
       }
       tb.all = stream;
       tb.task_rect = stream_rect;
+      drop_cross_launch_counters(tb);
       tb.narenas = narenas;
       tb.arena_bytes = arena_bytes;
       info.flops_executed = info.flops_stage1 + info.flops_stage2 + info.flops_stage3 + info.flops_dense_terms;
@@ -1438,6 +1467,7 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
     }
     tb.all = stream;
     tb.task_rect = stream_rect;
+    drop_cross_launch_counters(tb);
     tb.narenas = narenas;
     tb.arena_bytes = arena_bytes;
     info.flops_executed = info.flops_stage1 + info.flops_stage2 + info.flops_stage3 + info.flops_dense_terms;
@@ -1520,9 +1550,11 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
     if (!inside(regs, v.addr, span)) { snprintf(buf, sizeof buf, "map %zu: view outside every buffer", m); return buf; }
   }
   const int64_t Cm = pc.pv.Cm, Cn = pc.pv.Cn;
-  std::vector<int> task_pair(tb.all.size(), tb.pair);
-  for (const Launch &l : tb.launches)
-    for (int64_t ti = l.t0; ti < l.t1; ++ti) task_pair[ti] = l.pair;
+  std::vector<int> task_pair(tb.all.size(), tb.pair), task_launch(tb.all.size(), 0);
+  for (size_t li = 0; li < tb.launches.size(); ++li) {
+    const Launch &l = tb.launches[li];
+    for (int64_t ti = l.t0; ti < l.t1; ++ti) { task_pair[ti] = l.pair; task_launch[ti] = static_cast<int>(li); }
+  }
   std::set<std::pair<int64_t, int64_t>> ctiles;
   double carea = 0;
   for (size_t ti = 0; ti < tb.all.size(); ++ti) {
@@ -1593,6 +1625,12 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
       for (int d = 0; d < 2; ++d) {
         if (t.dep[d] < 0) continue;
         if (static_cast<size_t>(t.dep[d]) >= nc) { snprintf(buf, sizeof buf, "task %zu: bad counter", ti); return buf; }
+        // every wait is met inside its own launch (counters are not reset between launches,
+        // but a wait whose signals all came from earlier launches would only cost time)
+        if (last[t.dep[d]] < 0 || task_launch[last[t.dep[d]]] != task_launch[ti]) {
+          snprintf(buf, sizeof buf, "task %zu: waits for counter %d, last signalled outside its launch", ti, t.dep[d]);
+          return buf;
+        }
         if (t.dep_target[d] != tb.counter_counts[t.dep[d]] || cnt[t.dep[d]] != t.dep_target[d]) {
           snprintf(buf, sizeof buf, "task %zu: waits for counter %d before all %u signals have lower tickets",
                    ti, t.dep[d], t.dep_target[d]);
