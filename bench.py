@@ -41,9 +41,9 @@ WORKLOAD = "large_var_rank_bf16_N32768_b1024"
 # profiles/tlr_task_gemm_large_var_rank_N32768_launches.md). The figure belongs
 # to the kernel sources it was taken with: `sources_sha256` is their hash, and the
 # bench reports null traffic once the sources differ.
-TRAFFIC = {"sources_sha256": "5e90ccfe18a321c424ea7048d2f17d3969d7e2732b7f22be46cc71006085d3fe",
-           # final-product launch (CTA pairs), mean of four: 0.977 GB read + 1.022 GB written
-           "bytes_per_launch": 0.9771e9 + 1.0223e9,
+TRAFFIC = {"sources_sha256": "31ae23a7a23ed2ba937fc03e2001dc1e396450ed2a1d6a7727e4be09ada6665c",
+           # final-product launch (CTA pairs), mean of four: 0.976 GB read + 1.021 GB written
+           "bytes_per_launch": 0.9759e9 + 1.0213e9,
            # its operands once and C once: (T 3.354 + C 4.295 + U 0.105 + P^T 0.105 + Z 0.105
            # + dense tiles 0.134 GB) over the four rectangles of the product
            "algorithmic_bytes_per_launch": 8.098e9 / 4}
@@ -73,12 +73,25 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) during the timed region."""
+    """nvidia-smi samples (every 200 ms), kept when they fall inside the timed region.
+
+    The sampler is started, and its first sample awaited, before the region
+    opens; `mark()` brackets the region in host time, which ends after the
+    closing synchronize.
+    """
 
     def __init__(self, index: int):
         self.index = index
         self.samples = []
+        self.times = []
         self.proc = None
+        self.t0 = self.t1 = None
+
+    def mark(self, which: str):
+        if which == "start":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
 
     def __enter__(self):
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -90,12 +103,16 @@ class ClockSampler:
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t_wait = time.time()
+            while not self.samples and self.proc.poll() is None and time.time() - t_wait < 5.0:
+                time.sleep(0.02)
         except OSError:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
+            self.times.append(time.time())
             self.samples.append([x.strip() for x in line.split(",")])
 
     def __exit__(self, *exc):
@@ -108,6 +125,10 @@ class ClockSampler:
         return False
 
     def summary(self):
+        if self.t0 is not None and self.t1 is not None:
+            inside = [s for s, t in zip(self.samples, self.times) if self.t0 <= t <= self.t1]
+            if inside:
+                self.samples = inside
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         sm = sorted(float(s[1]) for s in self.samples if len(s) > 2 and s[1].replace(".", "").isdigit())
@@ -191,7 +212,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
@@ -262,11 +283,13 @@ def main():
     barrier()
     with ClockSampler(local) as clk:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clk.mark("start")
         e0.record(stream)
         for _ in range(args.steps):
             dp.run()
         e1.record(stream)
         barrier()
+        clk.mark("end")
     g.tlr_set_timing(h, False)
     ms_total = max_over_ranks(e0.elapsed_time(e1))
     ms_step = ms_total / args.steps
