@@ -52,6 +52,14 @@ TRAFFIC = {"sources_sha256": "31ae23a7a23ed2ba937fc03e2001dc1e396450ed2a1d6a7727
 ALGORITHMIC_BYTES = 12.100e9
 
 
+def recorded_traffic(main_workload: bool, scale_down: int):
+    """The recorded DRAM bytes per final-product launch, or None unless they were
+    captured on this workload with the kernel sources as they are now."""
+    if not main_workload or scale_down != 1 or sources_sha256() != TRAFFIC["sources_sha256"]:
+        return None
+    return TRAFFIC["bytes_per_launch"]
+
+
 def sources_sha256() -> str:
     import hashlib
     root = os.path.join(ROOT, "gemm_tlr_gb300", "csrc")
@@ -333,7 +341,7 @@ def main():
     names = {5: f"tlr_task_gemm<{et}>: Stages 1-3 and the dense-tile terms of a product in one persistent launch",
              2: f"tlr_task_gemm<{et}, CTA pairs>: final products (Stage 3 and the dense-tile segment) of a rectangle",
              1: f"tlr_task_gemm<{et}, single CTAs>: Stages 1-2 and the dense precomputes of a rectangle",
-             0: f"tlr_task_gemm<{et}>: Stage 1"}
+             0: f"tlr_task_gemm<{et}>: Stage 1 and the dense precomputes in a launch of their own"}
     dom = max((k for k in (5, 2, 1, 0) if kern[k][1]), key=lambda k: kern[k][0], default=None)
     roof = None
     if dom is not None:
@@ -342,9 +350,8 @@ def main():
         per_launch_flops = class_flops[dom] / launches_per_step
         avg_ms = k_ms / k_n
         achieved = per_launch_flops / (avg_ms * 1e-3) / 1e12
-        same = main_workload and args.scale_down == 1 and sources_sha256() == TRAFFIC["sources_sha256"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": achieved / peak_sus, "traffic": TRAFFIC["bytes_per_launch"] if same else None,
+                "frac": achieved / peak_sus, "traffic": recorded_traffic(main_workload, args.scale_down),
                 "traffic_unit": "bytes per launch (DRAM read + write)",
                 "algorithmic_bytes": TRAFFIC["algorithmic_bytes_per_launch"] if main_workload else None,
                 "kernel": names[dom] + " (executed FLOPs per launch / mean launch time)",

@@ -437,6 +437,7 @@ struct Builder {
   int bm = kBM;                         // output tile rows of the final products: 128, or 256 for a CTA pair
   int pair = 1;                         // CTAs per final-product tile (each epilogue warp of each signals)
   int prep_bm = kBM, prep_pair = 1;     // the same for Stages 1-2 and the dense precomputes
+  int l1_bm = kBM, l1_pair = 1;         // Stage 1 and the dense precomputes (may run on pairs)
   int cur_pair = 1;                     // of the list being built
   // Dependency counters of the merged launch (see Task in tlr_tables.h).
   std::vector<uint32_t> *counts = nullptr;              // signals each counter receives so far
@@ -697,8 +698,8 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
   const LOp &X = B.X;
   const LOp &Y = B.Y;
   const int es = B.es, bn = B.bn;
-  int64_t BM = B.prep_bm;              // rows of an output tile (256 for a CTA pair)
-  B.cur_pair = B.prep_pair;
+  int64_t BM = B.l1_bm;                // rows of an output tile (256 for a CTA pair)
+  B.cur_pair = B.l1_pair;
   const int i0 = L.i0, i1 = L.i1, j0 = L.j0, j1 = L.j1;
   const uint64_t T = B.ws + static_cast<uint64_t>(L.Toffset);
   const int outT = B.out_ws(T, L.Tld, L.Trow);
@@ -802,6 +803,8 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
   const double before2 = B.fl_s2;
   // ---------------- L2: Stage 2, T_i[k, j] = S_ikj Z_kj^T fused over i
   B.tasks = &l2;
+  BM = B.prep_bm;
+  B.cur_pair = B.prep_pair;
   if (!Y.dense)
     for (int k = 0; k < X.nc; ++k) {
       const int64_t sig = L.Ssig[k];
@@ -1209,6 +1212,20 @@ int choose_prep_pair(const PlanCore &pc, int bn, int pair) {
   return 1;
 }
 
+// CTAs per tile for Stage 1 and the dense precomputes when Stage 2 runs on
+// single CTAs. A product with a dense operand has no Stage 2: its first-stage
+// tiles (K = one tile of the contraction, 256 wide) run on CTA pairs, in a launch
+// of their own before the final products (one TLR 16384^2 operand times a dense
+// 16384 x 4096: 0.195 vs 0.243 ms for that launch). A TLR x TLR product keeps
+// them with Stage 2 on single CTAs (large product: 0.49 ms on pairs in a launch
+// of their own plus 0.85 for Stage 2, against 1.30 for the two together).
+// TLR_L1_PAIR=0/1 overrides.
+int choose_l1_pair(const PlanCore &pc, int prep_pair, int pair) {
+  if (prep_pair == pair) return prep_pair;
+  if (const char *e = getenv("TLR_L1_PAIR")) return atoi(e) == 1 ? pair : prep_pair;
+  return (pc.pv.dense_left || pc.pv.dense_right) ? pair : prep_pair;
+}
+
 bool plan_split(const PlanCore &pc, int64_t budget, tlr_order_t force, int es, std::vector<Rect> &rects,
                 int &narenas) {
   const int64_t avail = budget - pc.fixed;
@@ -1279,6 +1296,7 @@ struct Tables {
   int bn = 256;
   int pair = 1;
   int prep_pair = 1;
+  int l1_pair = 1;                          // Stage 1 and the dense precomputes
   std::vector<CUtensorMap> maps;
   std::map<std::tuple<uint64_t, int64_t, int64_t, int64_t, int>, int> map_index;
   std::vector<Task> all;
@@ -1378,6 +1396,8 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
     B.bm = kBM * tb.pair;
     B.prep_pair = tb.prep_pair;
     B.prep_bm = kBM * tb.prep_pair;
+    B.l1_pair = tb.l1_pair;
+    B.l1_bm = kBM * tb.l1_pair;
     // counters: S_k per contraction tile, "T and P ready", "Stage 3 done"
     B.counts = &tb.counter_counts;
     B.cS0 = static_cast<int32_t>(tb.counter_counts.size());
@@ -1432,7 +1452,7 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
         std::vector<Task> a(prep[ri].begin(), prep[ri].begin() + n1), b(prep[ri].begin() + n1, prep[ri].end());
         const std::vector<Task> *lists[3] = {&a, &b, &fin[ri]};
         const int kinds[3] = {kKindStage1, kKindStage2, kKindStage3};
-        const int pairs[3] = {tb.prep_pair, tb.prep_pair, tb.pair};
+        const int pairs[3] = {tb.l1_pair, tb.prep_pair, tb.pair};
         for (int q = 0; q < 3; ++q) {
           if (lists[q]->empty()) continue;
           const int64_t t0 = static_cast<int64_t>(stream.size());
@@ -1456,6 +1476,19 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
     // launch only waits for counters of its own lower tickets; everything an
     // earlier launch signals is complete before the next one starts.
     for (size_t ri = 0; ri < nr; ++ri) {
+      if (tb.l1_pair != tb.prep_pair) {   // Stage 1 and the dense precomputes in a launch of their own
+        const size_t n1 = prep[ri].size() - l2count[ri];
+        std::vector<Task> a(prep[ri].begin(), prep[ri].begin() + n1), b(prep[ri].begin() + n1, prep[ri].end());
+        const std::vector<Task> *lists[3] = {&a, &b, &fin[ri]};
+        const int kinds[3] = {kKindStage1, kKindPrep, kKindFinal}, pairs[3] = {tb.l1_pair, tb.prep_pair, tb.pair};
+        for (int q = 0; q < 3; ++q) {
+          if (lists[q]->empty()) continue;
+          const int64_t t0 = static_cast<int64_t>(stream.size());
+          push(*lists[q], static_cast<int>(ri));
+          tb.launches.push_back(Launch{kinds[q], t0, static_cast<int64_t>(stream.size()), pairs[q]});
+        }
+        continue;
+      }
       const std::vector<Task> *lists[2] = {&prep[ri], &fin[ri]};
       const int kinds[2] = {kKindPrep, kKindFinal}, pairs[2] = {tb.prep_pair, tb.pair};
       for (int q = 0; q < 2; ++q) {
@@ -1920,6 +1953,7 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
   tb.bn = p->bn;
   tb.pair = p->pair = choose_pair(pc, p->bn);
   tb.prep_pair = choose_prep_pair(pc, p->bn, tb.pair);
+  tb.l1_pair = choose_l1_pair(pc, tb.prep_pair, tb.pair);
   st = build_tables(pc, rects, narenas, ws, false, tb);
   if (st) { delete p; return st; }
   p->launches = tb.launches;
@@ -2002,6 +2036,7 @@ tlr_status_t tlr_debug_check_plan(tlr_op_t opA, tlr_op_t opB, const tlr_operand_
   tb.bn = choose_bn(pc);
   tb.pair = choose_pair(pc, tb.bn);
   tb.prep_pair = choose_prep_pair(pc, tb.bn, tb.pair);
+  tb.l1_pair = choose_l1_pair(pc, tb.prep_pair, tb.pair);
   st = build_tables(pc, rects, narenas, ws, true, tb);
   if (st) return st;
   const int64_t need = pc.fixed + narenas * align_up(max_rect_bytes(pc, rects, es), 256);
@@ -2158,6 +2193,7 @@ tlr_status_t tlr_gemm_static_scratch(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB,
   tb.bn = p.bn;
   tb.pair = p.pair = choose_pair(pc, p.bn);
   tb.prep_pair = choose_prep_pair(pc, p.bn, tb.pair);
+  tb.l1_pair = choose_l1_pair(pc, tb.prep_pair, tb.pair);
   st = build_tables(pc, rects, narenas, ws, false, tb);
   if (st) return st;
   p.launches = tb.launches;

@@ -218,9 +218,10 @@ tlr_status_t tlr_get_device_status(tlr_handle_t handle);
  * dense precomputes, 2 the launch of its final products (products whose final
  * tiles run on CTA pairs use these two launches per rectangle); 5 a whole
  * product in one launch (every other product); 3 the fp32 rounding and
- * transpose pre-pass; 4 the alpha == 0 scale-only kernel; 0 Stage 1 alone
- * (only with the per-stage diagnostic schedule, which also splits 1 into
- * Stage 2 alone). */
+ * transpose pre-pass; 4 the alpha == 0 scale-only kernel; 0 Stage 1 and the
+ * dense precomputes in a launch of their own (products with a dense operand,
+ * where they run on CTA pairs before the final products; also the per-stage
+ * diagnostic schedule, which then leaves Stage 2 alone in class 1). */
 tlr_status_t tlr_set_timing(tlr_handle_t handle, int enabled);
 tlr_status_t tlr_get_timing(tlr_handle_t handle, int kind, double *ms, int64_t *launches);
 tlr_status_t tlr_reset_timing(tlr_handle_t handle);

