@@ -12,15 +12,20 @@
 // "One product, three stages" and "Where fusion stops"; the dense-diagonal
 // terms follow "TLR Matrix Multiplication", section "Regular TLR GEMM").
 //
-// Roles (224 threads, one CTA per SM):
-//   warp 0       TMA producer: 4-stage shared-memory ring, 128-byte swizzle
-//   warp 1       tcgen05.mma issuer (M = 128, N = BN, fp32 accumulators in TMEM,
+// Roles (352 threads, one CTA per SM; instantiated for single CTAs, M = 128, and
+// for CTA pairs, cta_group::2 with M = 256 across the two SMs):
+//   warp 0       TMA producer: shared-memory ring of 4 stages (48 KiB) on a
+//                single CTA or 6 stages (32 KiB) per CTA of a pair, 128-byte swizzle
+//   warp 1       tcgen05.mma issuer (N = BN <= 256, fp32 accumulators in TMEM,
 //                two accumulators so the epilogue of tile t overlaps tile t+1)
-//   warp 2       descriptors: stages each task's segments, output descriptor and
-//                per-row destinations in a shared-memory ring, kRing tasks ahead
-//   warps 3..    epilogue, kEpiGroups groups of four warps: tcgen05.ld, alpha/beta,
-//                coalesced column-major stores; group g takes 32-column chunks
-//                g, g + kEpiGroups, ... so more stores are in flight per SM
+//   warp 2       descriptors: claims tickets, stages each task's segments, output
+//                descriptor and per-row destinations in a shared-memory ring,
+//                kRing tasks ahead
+//   warps 3..10  epilogue, kEpiGroups groups of four warps (one per TMEM lane
+//                quarter): tcgen05.ld, alpha/beta, stores staged through shared
+//                memory (bulk tensor stores of C when beta == 0, 16-byte stores
+//                of row-major 16-bit workspaces); group g takes the 64-column
+//                blocks g, g + kEpiGroups, ... of the tile
 // Every mbarrier wait is bounded (globaltimer); on timeout the CTA raises a flag
 // in the device error word, drains its own copies and MMAs, frees TMEM, exits.
 #include <cuda.h>
@@ -514,9 +519,9 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
       const int r = 8 * s + (lane >> 2), c = lane & 3;
       const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
       // rowd[s]: output row of row 8s + lane/4 of this warp's block (-1: not
-      // stored), resolved once per task. T is read by a later rectangle's final
-      // products, long after it would have left L2: its lines go first, ahead
-      // of the operands being reused now.
+      // stored), resolved once per task. A rectangle's T is larger than L2 and
+      // is read back only by its final products, after every Stage-2 tile of
+      // the rectangle: its lines go first, ahead of the operands being reused now.
       int64_t d;
       if constexpr (kRowIdx) d = rowd[s];
       else d = __shfl_sync(0xffffffffu, valid ? drow : int64_t(-1), r);

@@ -27,7 +27,7 @@ constexpr int kStageBytes = kSmemA + kSmemB;
 #ifndef TLR_EPI_GROUPS
 #define TLR_EPI_GROUPS 2
 #endif
-constexpr int kEpiGroups = TLR_EPI_GROUPS;   // epilogue warp groups; each stores every kEpiGroups-th 32-column chunk
+constexpr int kEpiGroups = TLR_EPI_GROUPS;   // epilogue warp groups; each stores every kEpiGroups-th 64-column block
 constexpr int kEpiThreads = 128 * kEpiGroups;
 constexpr int kThreads = 96 + kEpiThreads;   // warp 0 TMA, warp 1 MMA, warp 2 descriptors, then the epilogue
 constexpr int kTmemCols = 512;      // two accumulators of up to 256 fp32 columns
