@@ -151,6 +151,21 @@ class ClockSampler:
                 "samples": len(self.samples)}
 
 
+def reduce_max(x: float, dist=None, device: str = "cuda") -> float:
+    """The largest of every rank's x (the slowest replica sets the step time)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_replica_step: float, ms_per_step: float) -> float:
+    """Replicas only: every rank runs the whole product, so the job does world x the FLOPs."""
+    return world * flops_per_replica_step / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -168,26 +183,32 @@ def sample_rc(n, b, per_tile, seed):
     return np.array(sorted(idx))
 
 
-def cpu_baseline(p, flops_total, target_s=10.0):
-    """Time the fp64 oracle on a bounded sample of C's entries, scaled to the metric."""
+def cpu_baseline(p, flops_total, target_s=10.0, per_tile=None):
+    """Time the fp64 oracle on a bounded sample of C's entries, scaled to the metric.
+
+    Without `per_tile` the sample grows (rows and columns per tile doubling)
+    until one evaluation takes a quarter of `target_s`; with it, one evaluation
+    of that sample is timed. Returns the baseline record, the seconds of the
+    timed evaluation and the sample size used."""
     import numpy as np
     import oracle
     oracle.build()
-    per_tile = 4
+    grow = per_tile is None
+    per_tile = per_tile or 4
     while True:
         rows = sample_rc(p.m, p.A.b, per_tile, 1)
         cols = sample_rc(p.n, p.A.b, per_tile, 2)
         t0 = time.perf_counter()
         oracle.gemm_problem(p, rows, cols)
         dt = time.perf_counter() - t0
-        if dt >= target_s / 4 or per_tile >= 64:
+        if not grow or dt >= target_s / 4 or per_tile >= 64:
             break
         per_tile *= 2
     frac = (len(rows) * len(cols)) / float(p.m * p.n)
     tflops = flops_total * frac / dt / 1e12
     return {"value": tflops, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{len(rows)} rows x {len(cols)} columns of C ({frac:.2e} of the entries), "
-                      f"{dt:.2f} s; executed FLOPs scaled by that fraction"}, dt
+                      f"{dt:.2f} s; executed FLOPs scaled by that fraction"}, dt, per_tile
 
 
 def run_reference(args):
@@ -198,11 +219,14 @@ def run_reference(args):
     from gemm_tlr_gb300 import flops as fl
     p = tlr_inputs.problem(5)
     total = fl.executed_flops(p, "R")["total"]
+    # one sample size for every step, chosen so the whole run stays near two minutes
+    per_step_s = min(4.0, max(0.1, 120.0 / max(1, args.steps + args.warmup)))
+    _, _, per_tile = cpu_baseline(p, total, target_s=4 * per_step_s)
     for _ in range(args.warmup):
-        cpu_baseline(p, total, target_s=2.0)
+        cpu_baseline(p, total, per_tile=per_tile)
     vals, times = [], []
     for _ in range(args.steps):
-        cb, dt = cpu_baseline(p, total, target_s=4.0)
+        cb, dt, _ = cpu_baseline(p, total, per_tile=per_tile)
         vals.append(cb["value"])
         times.append(dt)
     value = sum(vals) / len(vals)
@@ -277,11 +301,7 @@ def main():
         torch.cuda.synchronize()
 
     def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, dist, "cuda")
 
     # ---- device-resident timing (value)
     for _ in range(args.warmup):
@@ -303,7 +323,7 @@ def main():
     ms_step = ms_total / args.steps
     status = g.tlr_get_device_status(h)
     kern = {k: g.tlr_get_timing(h, k) for k in range(6)}
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops_step, ms_step)
 
     # ---- end-to-end through the same entry point, host buffers in and out
     C_host = torch.empty(p.m * p.n, dtype=torch.float32).pin_memory()
@@ -323,7 +343,7 @@ def main():
     f1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1)) / args.e2e_steps
-    e2e_value = world * flops_step / (e2e_ms * 1e-3) / 1e12
+    e2e_value = whole_job_tflops(world, flops_step, e2e_ms)
 
     peaks, peak_src = _peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
@@ -386,7 +406,7 @@ def main():
         "device_status": g.tlr_status_string(status),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"], _ = cpu_baseline(p, flops_step)
+        line["cpu_baseline"], _, _ = cpu_baseline(p, flops_step)
     dp.close()
     g.tlr_destroy(h)
     if rank == 0:
