@@ -1917,6 +1917,26 @@ tlr_status_t tlr_gemm_workspace_bytes(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB
   return TLR_STATUS_OK;
 }
 
+// Buffers the kernels read or write through TMA must be device memory
+// (cudaMalloc or managed); a host pointer, pinned or not, is refused before any
+// table is built or kernel launched.
+bool device_memory(const void *ptr) {
+  if (!ptr) return true;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+bool operand_on_device(const tlr_operand_t *X) {
+  if (X->kind == TLR_KIND_DENSE) return device_memory(X->data);
+  for (const void *q : {X->U, X->V, X->D, X->bu_U, X->bu_V, X->bv_U, X->bv_V, X->gamma})
+    if (!device_memory(q)) return false;
+  return true;
+}
+
 tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A,
                              const tlr_operand_t *B, void *workspace, size_t workspace_bytes,
                              tlr_order_t order, tlr_plan_t *plan_out) {
@@ -1928,6 +1948,7 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
   PlanCore pc;
   tlr_status_t st = core_init(pc, opA, opB, A, B, true, ws ? ws : 256);
   if (st) return st;
+  if (!operand_on_device(A) || !operand_on_device(B) || !device_memory(workspace)) return TLR_STATUS_INVALID_ARG;
   const int es = elem_size(pc.pv.dtype);
   const bool tf32 = pc.pv.dtype == TLR_F32;
   std::vector<Rect> rects;
@@ -2080,6 +2101,7 @@ tlr_status_t tlr_plan_execute(tlr_plan_t p, float alpha, float beta, float *C, i
   if (!p || !C) return TLR_STATUS_INVALID_ARG;
   if (ldc < p->Cm || (ldc % 4)) return ldc < p->Cm ? TLR_STATUS_INVALID_ARG : TLR_STATUS_ALIGNMENT;
   if (!aligned16(C)) return TLR_STATUS_ALIGNMENT;
+  if (!device_memory(C)) return TLR_STATUS_INVALID_ARG;
   tlr_handle_t h = p->h;
   const int sms = device_sms();
   std::pair<cudaEvent_t, cudaEvent_t> ev;
@@ -2171,6 +2193,7 @@ tlr_status_t tlr_gemm_static_scratch(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB,
   st = core_init(pc, opA, opB, A, B, true, ws);
   if (st) return st;
   if (ldc < pc.pv.Cm) return TLR_STATUS_INVALID_ARG;
+  if (!operand_on_device(A) || !operand_on_device(B) || !device_memory(C)) return TLR_STATUS_INVALID_ARG;
   const int es = elem_size(pc.pv.dtype);
   std::vector<Rect> rects;
   int narenas = 1;

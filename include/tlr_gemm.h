@@ -33,8 +33,11 @@
  *
  * Conventions for every entry point:
  *   - All numeric buffers are DEVICE pointers owned by the caller; the library
- *     never frees or reallocates them. Rank and offset arrays are HOST pointers,
- *     read during the call (a plan keeps its own copy).
+ *     never frees or reallocates them. Device means cudaMalloc or managed
+ *     memory: a host pointer (pinned or not) for an operand, the workspace or C
+ *     gets TLR_STATUS_INVALID_ARG before any table is built or kernel launched.
+ *     Rank and offset arrays are HOST pointers, read during the call (a plan
+ *     keeps its own copy).
  *   - Element types: fp32 (run on TF32 tensor cores, inputs rounded to nearest
  *     TF32 first), bf16 or fp16 (tensor cores, fp32 accumulation; the
  *     intermediate S, T and P products are kept in the input type, rounded to

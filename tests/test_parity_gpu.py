@@ -233,6 +233,33 @@ def test_one_shot_entry_point(oracle_lib, handle, torch_cuda):
     assert rel(dp.result(), oracle_lib.gemm_problem(p)) <= TOL["f32"]
 
 
+def test_host_buffers_are_refused_before_any_launch(handle, torch_cuda):
+    """Operands, workspace and C must be device memory; a pinned host buffer is
+    refused by plan creation or execution on the host (nothing is launched)."""
+    import gemm_tlr_gb300 as g
+    from gemm_tlr_gb300._abi import TLRError
+    from gemm_tlr_gb300.device import DeviceProblem
+    p = ti.problem(1)
+    dp = DeviceProblem(p)
+    try:
+        host_u = dp.A.host["U"].pin_memory()
+        saved = dp.A.desc.U
+        dp.A.desc.U = host_u.data_ptr()
+        with pytest.raises(TLRError) as e:
+            dp.make_plan(handle)
+        assert e.value.code == 1
+        dp.A.desc.U = saved
+        dp.make_plan(handle)
+        host_c = torch_cuda.empty(p.m * p.n, dtype=torch_cuda.float32).pin_memory()
+        with pytest.raises(TLRError) as e:
+            g.tlr_plan_execute(dp.plan, p.alpha, p.beta, host_c.data_ptr(), p.m)
+        assert e.value.code == 1
+        dp.run()
+        assert g.tlr_get_device_status(handle) == 0
+    finally:
+        dp.close()
+
+
 def test_bounded_wait_reports_timeout_and_recovers(oracle_lib, handle):
     import gemm_tlr_gb300 as g
     g.tlr_set_wait_limit_us(handle, 200_000)
