@@ -8,6 +8,7 @@ oracle's own metadata definitions on random rank maps. The table validator
 output writes stay inside their buffers and that every dependency is satisfied.
 """
 import ctypes
+import functools
 import json
 import os
 
@@ -203,3 +204,31 @@ def test_fp16_descriptors_plan_and_check_like_bf16(g):
         ws = p.budget or g.tlr_gemm_workspace_bytes(0, 0, 0, Ad, Bd, 1)
         st, msg, info = g.tlr_debug_check_plan(0, 0, Ad, Bd, ws)
         assert st == 0, (p.name, msg)
+
+
+@functools.lru_cache(maxsize=None)
+def _problem(cfg, scale):
+    return ti.problem(cfg, scale_down=scale)
+
+
+SCHEDULES = [{}, {"TLR_HYBRID": "0"}, {"TLR_SPLIT_LAUNCHES": "1"}, {"TLR_L1_PAIR": "1"},
+             {"TLR_L1_PAIR": "0"}, {"TLR_PAIR": "1"}, {"TLR_ARENAS": "1", "TLR_HYBRID": "0"}]
+
+
+@pytest.mark.parametrize("env", SCHEDULES, ids=lambda e: ",".join(f"{k}={v}" for k, v in e.items()) or "default")
+@pytest.mark.parametrize("cfg,scale", [(5, 1), (5, 4), (4, 1), (3, 2)])
+def test_every_schedule_variant_validates(g, monkeypatch, env, cfg, scale):
+    """Each launch schedule the planner can build (defaults and tuning overrides)
+    passes the host validator: views and writes in bounds, C covered once, T
+    covered, and every dependency wait met by lower tickets of its own launch."""
+    from gemm_tlr_gb300.device import fake_descriptor
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    p = _problem(cfg, scale)
+    A, ka = fake_descriptor(p.A, 1 << 40)
+    B, kb = fake_descriptor(p.B, 1 << 41)
+    opA = 1 if p.opA == "T" else 0
+    budget = p.budget or g.tlr_gemm_workspace_bytes(0, opA, 0, A, B, 1)
+    st, msg, info = g.tlr_debug_check_plan(opA, 0, A, B, budget)
+    assert st == 0, msg
+    assert info["launches"] >= 1
