@@ -252,10 +252,11 @@ def main():
     ap.add_argument("--scale-down", type=int, default=1,
                     help="profile a smaller member of the workload family (N/s, b/s, budget/s^2); "
                          "bench lines are taken at 1")
-    ap.add_argument("--workload", default="large_var_rank", choices=["large_var_rank", "skewed8x8"],
+    ap.add_argument("--workload", default="large_var_rank", choices=["large_var_rank", "skewed8x8", "var_rank"],
                     help="skewed8x8: the pages' variable-rank 8 x 8 grid (b = N/8, ranks on [b/32, b/16]), "
-                         "a second measurement beside the metric's workload")
-    ap.add_argument("--n", type=int, default=65536, help="order of the skewed8x8 workload")
+                         "a second measurement beside the metric's workload; var_rank: the large product's "
+                         "tiles and rank rule at order --n (smaller cases for profiling)")
+    ap.add_argument("--n", type=int, default=65536, help="order of the skewed8x8 or var_rank workload")
     ap.add_argument("--dtype", default="f16", choices=["f16", "bf16", "f32"], help="element type of skewed8x8")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -283,6 +284,9 @@ def main():
     main_workload = args.workload == "large_var_rank"
     if main_workload:
         p = tlr_inputs.problem(5, scale_down=args.scale_down)
+    elif args.workload == "var_rank":
+        p = tlr_inputs.var_rank_grid(args.n)
+        args.no_cpu_baseline = True
     else:
         p = tlr_inputs.skewed_grid(args.n, args.dtype)
         args.no_cpu_baseline = True

@@ -32,3 +32,16 @@ def test_traffic_is_reported_only_for_the_sources_it_was_captured_with(monkeypat
     assert bench.recorded_traffic(False, 1) is None and bench.recorded_traffic(True, 2) is None
     monkeypatch.setitem(bench.TRAFFIC, "sources_sha256", "0" * 64)
     assert bench.recorded_traffic(True, 1) is None
+
+
+def test_var_rank_grid_keeps_the_large_products_tiles():
+    import numpy as np
+    import tlr_inputs as ti
+    p = ti.var_rank_grid(4096)
+    assert p.A.b == 1024 and p.m == p.n == 4096 and p.budget == (2 << 30) // 64
+    r = np.asarray(p.A.ranks).reshape(4, 4)
+    for i in range(4):
+        for j in range(4):
+            if i != j:
+                want = min(256, max(8, int(np.floor(256 * np.exp(-abs(i - j) / 4.0) + 0.5))))
+                assert r[i, j] == want

@@ -40,7 +40,7 @@ from typing import Callable, Dict, Optional, Tuple
 import numpy as np
 
 __all__ = [
-    "bf16_round", "f16_round", "bf16_bits", "TLRMatrix", "DenseMatrix", "Problem",
+    "var_rank_grid", "bf16_round", "f16_round", "bf16_bits", "TLRMatrix", "DenseMatrix", "Problem",
     "make_tlr", "make_dense", "problem", "CONFIG_NAMES", "tile_dims",
     "rank_fixed", "rank_uniform", "rank_inverse_distance", "rank_exp_decay", "rank_skewed",
     "skewed_grid",
@@ -322,6 +322,24 @@ CONFIG_NAMES = {
     4: "one_tlr_bf16_16384x16384_b1024_x_16384x4096",
     5: "large_var_rank_bf16_N32768_b1024",
 }
+
+
+def var_rank_grid(n: int, *, b: int = 1024, dtype: str = "bf16", seed: int = 0,
+                  budget: Optional[int] = None) -> Problem:
+    """The large variable-rank family at another order: b = 1024 tiles with the
+    same rank rule, clamp(round(256 exp(-|i-j|/4)), 8, 256), so every tile has
+    the large product's shape and only the grid (n / b tiles a side) changes.
+    A budget of 2 GiB scaled by (n / 32768)^2 unless given.
+    """
+    if n % b:
+        raise ValueError("n must be a multiple of b")
+    rng = np.random.default_rng(seed)
+    rule = rank_exp_decay(256, 4.0, 8, 256)
+    A = make_tlr(rng, n, b, rule, dtype)
+    Bm = make_tlr(rng, n, b, rule, dtype)
+    if budget is None:
+        budget = int((2 << 30) * (n / 32768) ** 2)
+    return Problem(f"var_rank_{dtype}_N{n}_b{b}", A, Bm, "N", "N", 1.0, 0.0, None, n, n, dtype, budget=budget)
 
 
 def skewed_grid(n: int, dtype: str, *, seed: int = 0, keep_tiles: bool = False, budget: Optional[int] = None) -> Problem:
