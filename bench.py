@@ -384,13 +384,15 @@ def main():
                                + ("; tf32 = bf16 x 1.1/2.25" if p.dtype == "f32" else ""),
                 "frac_of_burst": achieved / peak_burst}
     line = {
-        "metric": METRIC if main_workload else "TLR GEMM executed TFLOP/s (pages' skewed-rank 8x8 grid)",
+        "metric": METRIC if main_workload else (
+            "TLR GEMM executed TFLOP/s (variable-rank grid, b = 1024)" if args.workload == "var_rank"
+            else "TLR GEMM executed TFLOP/s (pages' skewed-rank 8x8 grid)"),
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": p.dtype, "data": "synthetic",
         "config": {"workload": WORKLOAD if main_workload and args.scale_down == 1 else p.name, "N": p.m, "b": p.A.b,
                    "tile_grid": [p.m // p.A.b, p.n // p.A.b],
-                   "ranks": "clamp(round(256 exp(-|i-j|/4)), 8, 256)" if main_workload else
+                   "ranks": "clamp(round(256 exp(-|i-j|/4)), 8, 256)" if args.workload != "skewed8x8" else
                             "b/32 + floor((b/32 + 1) u^2), u ~ U[0,1), on [b/32, b/16]",
                    "alpha": p.alpha, "beta": p.beta,
                    "workspace_budget_bytes": p.budget, "runs": info["runs"], "order": order,
