@@ -12,13 +12,14 @@
 //   - C is split into rectangles of output tiles that fit the workspace:
 //     widest feasible block of tile columns first, then the longest runs of tile
 //     rows; each rectangle holds the full reduction over k and takes the cheaper
-//     feasible order; rectangles run in sequence over one arena.
+//     feasible order; rectangles run in sequence over one arena (two when one
+//     launch overlaps the stages of consecutive rectangles).
 // The left order is evaluated as the right order of the transposed product
 // C^T = op(B)^T op(A)^T with a transposed store of the output tile, so both
 // orders share one kernel path.
 //
-// Per rectangle three launches of the task kernel (section "One product, three
-// stages"):
+// Per rectangle three classes of tasks for the one task kernel (section "One
+// product, three stages"):
 //   L1  Stage 1 S_k = V_{:,k}^T W_{k,:} per contraction tile k (fused over i
 //       and j), plus P_i = D_ii W_{i,:} (first half of D_A O_B) and the k=j block
 //       V_ij^T D_jj of T_i (O_A D_B), both from "TLR Matrix Multiplication",
@@ -31,6 +32,11 @@
 //       accumulator, so every element of C is read and written once.
 // One-TLR-operand products (dense B) skip Stage 2: L1 writes T_i rows
 // V_{:,k}^T B_k directly, and L3 adds the segment D_ii B_i.
+// Launches: with 256-wide final tiles, L1 and L2 of a rectangle run in one launch
+// on single CTAs and L3 in the next on CTA pairs (L1 on pairs, in a launch of its
+// own, for a product with a dense operand); otherwise one launch runs every
+// class of every rectangle in order, L1-L2 of rectangle r + 1 mixed with L3 of
+// r when there are two arenas.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
