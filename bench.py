@@ -37,10 +37,9 @@ WORKLOAD = "large_var_rank_bf16_N32768_b1024"
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # dominant kernel on this workload (the final-product launch), from one ncu
-# capture (summary and command in
-# profiles/tlr_task_gemm_large_var_rank_N32768_launches.md). The figure belongs
-# to the kernel sources it was taken with: `sources_sha256` is their hash, and the
-# bench reports null traffic once the sources differ.
+# capture. The figure belongs to the kernel sources it was taken with:
+# `sources_sha256` is their hash, and the bench reports null traffic once the
+# sources differ.
 TRAFFIC = {"sources_sha256": "7d38f860b2d7edfc28c55b7bb7bfc3aa9d36a058ba21a865e54d411ace4d66d8",
            # final-product launch (CTA pairs), mean of four: 0.976 GB read + 1.022 GB written
            "bytes_per_launch": 0.9764e9 + 1.0221e9,
@@ -206,9 +205,14 @@ def cpu_baseline(p, flops_total, target_s=10.0, per_tile=None):
         per_tile *= 2
     frac = (len(rows) * len(cols)) / float(p.m * p.n)
     tflops = flops_total * frac / dt / 1e12
+    # the oracle's own arithmetic: a dense dot product of length K per sampled entry
+    K = p.A.cols if p.opA == "N" else p.A.rows
+    own = 2.0 * len(rows) * len(cols) * K / dt / 1e12
     return {"value": tflops, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "value_own_flops": own,
             "sample": f"{len(rows)} rows x {len(cols)} columns of C ({frac:.2e} of the entries), "
-                      f"{dt:.2f} s; executed FLOPs scaled by that fraction"}, dt, per_tile
+                      f"{dt:.2f} s; value: the method's executed FLOPs scaled by that fraction; "
+                      f"value_own_flops: the oracle's own 2 K FLOPs per sampled entry (K = {K})"}, dt, per_tile
 
 
 def run_reference(args):
@@ -241,14 +245,160 @@ def run_reference(args):
     return 0
 
 
+# Nominal dense tensor-core peaks of one GB300 (TFLOP/s): bf16/fp16 2250, tf32 1100.
+NOMINAL_TFLOPS = {"bf16": 2250.0, "f16": 2250.0, "f32": 1100.0}
+
+
+def dtype_peaks(dtype: str, peaks: dict):
+    """(burst, sustained) TFLOP/s for the tensor-core type a product runs on: the
+    measured bf16 figures, times the nominal tf32/bf16 ratio for fp32 inputs."""
+    scale = NOMINAL_TFLOPS[dtype] / NOMINAL_TFLOPS["bf16"]
+    burst = float(peaks.get("bf16_tflops")) * scale
+    sus = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))) * scale
+    return burst, sus
+
+
+def peak_choice(region_ms: float) -> str:
+    """The measured peak a timed region is compared with: the burst figure for a
+    region shorter than three seconds (the power cap has not settled), else the
+    sustained one."""
+    return "burst" if region_ms < 3000.0 else "sustained"
+
+
+def gpu_local_cpus(index: int):
+    """CPUs the kernel lists as local to GPU `index` (its PCI device's
+    local_cpulist), restricted to this process's affinity; None if unknown."""
+    try:
+        out = subprocess.run(["nvidia-smi", f"--id={index}", "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.strip()
+        dom, rest = out.split(":", 1)
+        sysid = "%04x:%s" % (int(dom, 16), rest.lower())
+        text = open(f"/sys/bus/pci/devices/{sysid}/local_cpulist").read().strip()
+    except (OSError, ValueError, subprocess.SubprocessError):
+        return None
+    cpus = set()
+    for part in text.split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    mine = os.sched_getaffinity(0)
+    local = sorted(cpus & mine)
+    return local if local and len(local) < len(mine) else None
+
+
+class near_gpu:
+    """Runs the block with this thread bound to the GPU's local CPUs, so that host
+    memory it allocates and first touches (the pinned staging buffers) lands on
+    the GPU's NUMA node; the previous affinity comes back afterwards."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.cpus = None
+
+    def __enter__(self):
+        self.saved = os.sched_getaffinity(0)
+        self.cpus = gpu_local_cpus(self.index)
+        if self.cpus:
+            os.sched_setaffinity(0, self.cpus)
+        return self
+
+    def __exit__(self, *exc):
+        os.sched_setaffinity(0, self.saved)
+        return False
+
+
+def input_bytes(p) -> int:
+    es = 4 if p.dtype == "f32" else 2
+    n = 0
+    for X in (p.A, p.B):
+        if X.kind == "dense":
+            n += X.data.size * es
+        else:
+            n += X.nbytes_device()
+    return n
+
+
+def algorithmic_bytes(p) -> int:
+    """Every input once, C written once (and read once when beta != 0)."""
+    return input_bytes(p) + p.m * p.n * 4 * (2 if p.beta != 0.0 else 1)
+
+
+def per_config_timings(h, stream, local: int, peaks: dict, cfgs=(1, 2, 3, 4)) -> dict:
+    """The other four workloads at full size: per config the mean product time
+    (CUDA events around each product on the library's stream, L2 flushed by a
+    256 MiB write before every timed product, 10 untimed products first; at
+    least 100 timed products for configs 1-2 and 20 for 3-4, and at least 0.5 s
+    of them), executed TFLOP/s, tensor-core and HBM fractions, and the SM clock."""
+    import torch
+    import gemm_tlr_gb300 as g
+    import tlr_inputs
+    from gemm_tlr_gb300 import flops as fl
+    from gemm_tlr_gb300.device import DeviceProblem
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    out = {}
+    for cfg in cfgs:
+        p = tlr_inputs.problem(cfg)
+        dp = DeviceProblem(p)
+        try:
+            dp.make_plan(h)
+            info = dp.info()
+            rects = g.tlr_plan_rects(dp.plan)
+            flops = info["flops_executed"]
+            counted = fl.executed_flops_rects(p, rects)["total"]
+            assert abs(counted - flops) <= 1e-9 * flops, (cfg, counted, flops)
+            for _ in range(10):
+                dp.run()
+            torch.cuda.synchronize()
+            min_iters = 100 if cfg in (1, 2) else 20
+            evs = []
+            with ClockSampler(local) as clk:
+                clk.mark("start")
+                t_start = time.time()
+                while len(evs) < min_iters or time.time() - t_start < 0.5:
+                    flush.fill_(len(evs) & 255)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    dp.run()
+                    b.record(stream)
+                    evs.append((a, b))
+                    if len(evs) % 64 == 0:
+                        torch.cuda.synchronize()
+                    if len(evs) >= 20000:
+                        break
+                torch.cuda.synchronize()
+                clk.mark("end")
+            assert g.tlr_get_device_status(h) == 0
+            ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+            burst, sus = dtype_peaks(p.dtype, peaks)
+            tflops = flops / (ms * 1e-3) / 1e12
+            ab = algorithmic_bytes(p)
+            out[str(cfg)] = {
+                "workload": p.name, "dtype": p.dtype, "ms": ms, "runs_timed": len(evs),
+                "flops_executed": flops, "executed_tflops": tflops,
+                "tensor_frac_of_burst": tflops / burst, "tensor_peak_burst_tflops": burst,
+                "algorithmic_bytes": ab, "hbm_gbs": ab / (ms * 1e-3) / 1e9,
+                "hbm_frac": ab / (ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
+                "rects": len(rects), "orders": "".join(r[4] for r in rects),
+                "clocks": clk.summary(),
+            }
+        finally:
+            dp.close()
+    del flush
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=0,
+                    help="end-to-end steps (0: as many as fill one second, at least 3)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the timings of the other four workloads")
     ap.add_argument("--scale-down", type=int, default=1,
                     help="profile a smaller member of the workload family (N/s, b/s, budget/s^2); "
                          "bench lines are taken at 1")
@@ -258,6 +408,8 @@ def main():
                          "tiles and rank rule at order --n (smaller cases for profiling)")
     ap.add_argument("--n", type=int, default=65536, help="order of the skewed8x8 or var_rank workload")
     ap.add_argument("--dtype", default="f16", choices=["f16", "bf16", "f32"], help="element type of skewed8x8")
+    ap.add_argument("--order", default="auto", choices=["auto", "right", "left", "triple"],
+                    help="association order of the plan: per rectangle (auto), forced, or per tile triple")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -290,14 +442,20 @@ def main():
     else:
         p = tlr_inputs.skewed_grid(args.n, args.dtype)
         args.no_cpu_baseline = True
-    dp = DeviceProblem(p, pinned=True)
-    dp.make_plan(h)
+    # pinned host copies of the inputs (end-to-end timing) on the GPU's NUMA node
+    with near_gpu(local) as numa:
+        dp = DeviceProblem(p, pinned=True)
+        C_host = torch.empty(p.m * p.n, dtype=torch.float32).pin_memory()
+        C_host.zero_()
+    dp.make_plan(h, order={"auto": 0, "right": 1, "left": 2, "triple": 3}[args.order])
     info = dp.info()
-    order = "L" if info["runs_left"] == info["runs"] else ("R" if info["runs_left"] == 0 else "mixed")
-    py_flops = fl.executed_flops(p, "R")["total"] if order == "R" else None
+    order = ("per-triple" if info["runs_triple"] == info["runs"] else
+             "L" if info["runs_left"] == info["runs"] else ("R" if info["runs_left"] == 0 else "mixed"))
     flops_step = info["flops_executed"]
-    if py_flops is not None:
-        assert abs(py_flops - flops_step) <= 1e-9 * flops_step, (py_flops, flops_step)
+    # the planner's count, recounted from the ranks rectangle by rectangle with each one's order
+    rects = g.tlr_plan_rects(dp.plan)
+    counted = fl.executed_flops_rects(p, rects)["total"]
+    assert abs(counted - flops_step) <= 1e-9 * flops_step, (counted, flops_step)
 
     def barrier():
         if dist is not None:
@@ -330,30 +488,44 @@ def main():
     value = whole_job_tflops(world, flops_step, ms_step)
 
     # ---- end-to-end through the same entry point, host buffers in and out
-    C_host = torch.empty(p.m * p.n, dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in dp.A.host.values()) + \
         sum(t.numel() * t.element_size() for t in dp.B.host.values())
     d2h = C_host.numel() * 4
-    for _ in range(1):
-        dp.A.upload(); dp.B.upload(); dp.run(); C_host.copy_(dp.C, non_blocking=True)
-    barrier()
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(args.e2e_steps):
+
+    def e2e_step():
         dp.A.upload()
         dp.B.upload()
         dp.run()
         C_host.copy_(dp.C, non_blocking=True)
+
+    # link rates of the same buffers, copies alone (for the expected end-to-end time)
+    e2e_step()
+    barrier()
+    l0, l1, l2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    l0.record(stream)
+    dp.A.upload()
+    dp.B.upload()
+    l1.record(stream)
+    C_host.copy_(dp.C, non_blocking=True)
+    l2.record(stream)
+    barrier()
+    h2d_ms, d2h_ms = l0.elapsed_time(l1), l1.elapsed_time(l2)
+    e2e_steps = args.e2e_steps or max(3, math.ceil(1000.0 / max(1e-3, h2d_ms + d2h_ms + ms_step)))
+    e2e_steps = int(max_over_ranks(float(e2e_steps)))   # every rank runs the same number
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
     f1.record(stream)
     barrier()
-    e2e_ms = max_over_ranks(f0.elapsed_time(f1)) / args.e2e_steps
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1)) / e2e_steps
     e2e_value = whole_job_tflops(world, flops_step, e2e_ms)
 
     peaks, peak_src = _peaks()
-    peak_sus = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    peak_burst = float(peaks.get("bf16_tflops"))
-    if p.dtype == "f32":   # TF32 runs at half the bf16 rate (nominal 1.1 vs 2.25 PFLOP/s dense)
-        peak_sus, peak_burst = peak_sus / 2, peak_burst / 2
+    peak_burst, peak_sus = dtype_peaks(p.dtype, peaks)
+    peak_nominal = NOMINAL_TFLOPS[p.dtype]
+    which = peak_choice(ms_total)
+    peak_used = peak_burst if which == "burst" else peak_sus
     # dominant kernel: the launch class with the most time. Classes: 5 = a whole
     # product in one launch; 1 = Stages 1-2 of a rectangle and 2 = its final
     # products (two launches per rectangle); 0 = Stage 1 alone (diagnostic split).
@@ -374,15 +546,16 @@ def main():
         per_launch_flops = class_flops[dom] / launches_per_step
         avg_ms = k_ms / k_n
         achieved = per_launch_flops / (avg_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": achieved / peak_sus, "traffic": recorded_traffic(main_workload, args.scale_down),
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak_used, "unit": "TFLOP/s",
+                "frac": achieved / peak_used, "traffic": recorded_traffic(main_workload, args.scale_down),
                 "traffic_unit": "bytes per launch (DRAM read + write)",
                 "algorithmic_bytes": TRAFFIC["algorithmic_bytes_per_launch"] if main_workload else None,
                 "kernel": names[dom] + " (executed FLOPs per launch / mean launch time)",
                 "launches_per_step": launches_per_step,
-                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside back-to-back steps)"
-                               + ("; tf32 = bf16 x 1.1/2.25" if p.dtype == "f32" else ""),
-                "frac_of_burst": achieved / peak_burst}
+                "peak_source": f"{peak_src} bf16 {which} (timed region {ms_total / 1e3:.2f} s: burst below 3 s, "
+                               f"sustained from 3 s)" + ("; tf32 = bf16 x 1.1/2.25" if p.dtype == "f32" else ""),
+                "frac_of_burst": achieved / peak_burst, "frac_of_sustained": achieved / peak_sus,
+                "frac_of_nominal": achieved / peak_nominal, "nominal_peak": peak_nominal}
     line = {
         "metric": METRIC if main_workload else (
             "TLR GEMM executed TFLOP/s (variable-rank grid, b = 1024)" if args.workload == "var_rank"
@@ -399,18 +572,27 @@ def main():
                    "l2": f"inputs larger than L2 (C alone is {p.m * p.n * 4 / 1e9:.1f} GB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": {"burst": value / world / peak_burst, "sustained": value / world / peak_sus,
-                        "source": peak_src},
+                        "nominal": value / world / peak_nominal, "used": which,
+                        "source": f"{peak_src} bf16 (torch.matmul 8192^3 burst and 4 s loop); nominal "
+                                  f"{peak_nominal:.0f} TFLOP/s dense",
+                        "target": "whole product >= 0.70 of the tensor-core peak"},
         "flops_per_step": flops_step,
         "kernel_ms_per_step": {name: kern[k][0] / args.steps for k, name in
                                enumerate(["stage1", "stages1_2" if os.environ.get("TLR_SPLIT_LAUNCHES") != "1"
                                           else "stage2", "final", "round", "scale", "tasks"]) if kern[k][1]},
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms, "steps": e2e_steps,
+                "link_gbs": {"h2d": h2d / (h2d_ms * 1e-3) / 1e9, "d2h": d2h / (d2h_ms * 1e-3) / 1e9},
+                "expected_ms": h2d_ms + ms_step + d2h_ms,
+                "host_buffers": (f"pinned, allocated on CPUs {numa.cpus[0]}-{numa.cpus[-1]} local to the GPU"
+                                 if numa.cpus else "pinned, default placement (GPU-local CPUs unknown)")},
         "clocks": clk.summary(),
         "gpu_launches": int(sum(v[1] for v in kern.values())),
         "device_status": g.tlr_status_string(status),
     }
+    if main_workload and args.scale_down == 1 and world == 1 and not args.no_per_config:
+        line["per_config"] = per_config_timings(h, stream, local, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"], _, _ = cpu_baseline(p, flops_step)
     dp.close()

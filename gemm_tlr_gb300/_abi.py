@@ -18,7 +18,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "tlr_gemm.h")
 TLR_OP_N, TLR_OP_T = 0, 1
 TLR_F32, TLR_BF16, TLR_F16 = 0, 1, 2
 TLR_KIND_TLR, TLR_KIND_DENSE = 0, 1
-TLR_ORDER_AUTO, TLR_ORDER_RIGHT, TLR_ORDER_LEFT = 0, 1, 2
+TLR_ORDER_AUTO, TLR_ORDER_RIGHT, TLR_ORDER_LEFT, TLR_ORDER_TRIPLE = 0, 1, 2, 3
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "ALIGNMENT", 3: "WORKSPACE_TOO_SMALL", 4: "UNSUPPORTED",
           5: "CUDA_ERROR", 6: "TIMEOUT", 7: "NOT_INITIALIZED"}
 KIND_STAGE1, KIND_STAGE2, KIND_STAGE3, KIND_ROUND, KIND_SCALE = 0, 1, 2, 3, 4
@@ -46,13 +46,18 @@ class tlr_operand_t(ctypes.Structure):
 class tlr_plan_info_t(ctypes.Structure):
     _fields_ = [
         ("runs", ctypes.c_int32), ("runs_right", ctypes.c_int32), ("runs_left", ctypes.c_int32),
-        ("launches", ctypes.c_int64),
+        ("runs_triple", ctypes.c_int32), ("launches", ctypes.c_int64),
         ("flops_executed", ctypes.c_double), ("flops_stage1", ctypes.c_double),
         ("flops_stage2", ctypes.c_double), ("flops_stage3", ctypes.c_double),
         ("flops_dense_terms", ctypes.c_double), ("flops_right_final", ctypes.c_double),
         ("flops_left_final", ctypes.c_double), ("workspace_bytes", ctypes.c_size_t),
         ("tasks", ctypes.c_int64), ("flops_launch", ctypes.c_double * 3),
     ]
+
+
+class tlr_rect_t(ctypes.Structure):
+    _fields_ = [("i0", ctypes.c_int32), ("i1", ctypes.c_int32), ("j0", ctypes.c_int32), ("j1", ctypes.c_int32),
+                ("order", ctypes.c_int32)]
 
 
 class tlr_analysis_t(ctypes.Structure):
@@ -80,6 +85,10 @@ _SIGS = {
     "tlr_plan_create": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _OP, _OP, _P, ctypes.c_size_t,
                                        ctypes.c_int, ctypes.POINTER(_P)]),
     "tlr_plan_info": (ctypes.c_int, [_P, ctypes.POINTER(tlr_plan_info_t)]),
+    "tlr_plan_rects": (ctypes.c_int, [_P, ctypes.POINTER(tlr_rect_t), ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
+    "tlr_debug_plan_rects": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _OP, _OP, ctypes.c_size_t, ctypes.c_int,
+                                            ctypes.POINTER(tlr_rect_t), ctypes.c_int32,
+                                            ctypes.POINTER(ctypes.c_int32)]),
     "tlr_plan_execute": (ctypes.c_int, [_P, ctypes.c_float, ctypes.c_float, _P, ctypes.c_int64]),
     "tlr_plan_destroy": (ctypes.c_int, [_P]),
     "tlr_gemm": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.c_float, _OP, _OP, ctypes.c_float,
@@ -189,6 +198,27 @@ def tlr_plan_info(p: int) -> dict:
     i = tlr_plan_info_t()
     check(lib().tlr_plan_info(_P(p), ctypes.byref(i)), "tlr_plan_info")
     return _info_dict(i)
+
+
+def _rects(call, what: str) -> list:
+    n = ctypes.c_int32()
+    check(call(None, 0, ctypes.byref(n)), what)
+    arr = (tlr_rect_t * max(1, n.value))()
+    check(call(arr, n.value, ctypes.byref(n)), what)
+    names = {TLR_ORDER_RIGHT: "R", TLR_ORDER_LEFT: "L", TLR_ORDER_TRIPLE: "P"}
+    return [(r.i0, r.i1, r.j0, r.j1, names.get(r.order, r.order)) for r in arr[:n.value]]
+
+
+def tlr_plan_rects(p: int) -> list:
+    """[(i0, i1, j0, j1, order)] of a plan, order "R", "L" or "P" (per tile triple)."""
+    return _rects(lambda a, c, n: lib().tlr_plan_rects(_P(p), a, c, n), "tlr_plan_rects")
+
+
+def tlr_debug_plan_rects(opA: int, opB: int, A: tlr_operand_t, B: tlr_operand_t, ws_bytes: int,
+                         order: int = TLR_ORDER_AUTO) -> list:
+    """The rectangles a plan for this budget would use (host only, no device)."""
+    return _rects(lambda a, c, n: lib().tlr_debug_plan_rects(opA, opB, ctypes.byref(A), ctypes.byref(B), ws_bytes,
+                                                             order, a, c, n), "tlr_debug_plan_rects")
 
 
 def tlr_plan_execute(p: int, alpha: float, beta: float, C: int, ldc: int) -> None:

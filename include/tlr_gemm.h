@@ -78,7 +78,12 @@ typedef enum {
 typedef enum { TLR_OP_N = 0, TLR_OP_T = 1 } tlr_op_t;
 typedef enum { TLR_F32 = 0, TLR_BF16 = 1, TLR_F16 = 2 } tlr_dtype_t;
 typedef enum { TLR_KIND_TLR = 0, TLR_KIND_DENSE = 1 } tlr_kind_t;
-typedef enum { TLR_ORDER_AUTO = 0, TLR_ORDER_RIGHT = 1, TLR_ORDER_LEFT = 2 } tlr_order_t;
+/* Association order of the low-rank products (page 1, "Association order and
+ * workspace"; page 2, "The O_A O_B terms"): AUTO takes the cheaper of RIGHT
+ * U (S Z^T) and LEFT (U S) Z^T per output rectangle; TRIPLE decides per tile
+ * triple (i, k, j) by min(r_ik, r_kj) after S_ikj = V_ik^T W_kj (two TLR
+ * operands with a 16-bit element type; otherwise TLR_STATUS_UNSUPPORTED). */
+typedef enum { TLR_ORDER_AUTO = 0, TLR_ORDER_RIGHT = 1, TLR_ORDER_LEFT = 2, TLR_ORDER_TRIPLE = 3 } tlr_order_t;
 
 /* One operand. Fields not used by its kind must be zero / NULL. */
 typedef struct tlr_operand {
@@ -110,6 +115,7 @@ typedef struct tlr_plan_s *tlr_plan_t;
 typedef struct tlr_plan_info {
     int32_t runs;                 /* output rectangles executed in sequence */
     int32_t runs_right, runs_left;/* rectangles using each association order */
+    int32_t runs_triple;          /* rectangles with the order chosen per tile triple */
     int64_t launches;             /* kernel launches per execution */
     double flops_executed;        /* every product the plan runs */
     double flops_stage1, flops_stage2, flops_stage3, flops_dense_terms;
@@ -119,6 +125,16 @@ typedef struct tlr_plan_info {
     double flops_launch[3];       /* per execution, by launch class: [0] Stage 1 with the
                                      dense-tile precomputes, [1] Stage 2, [2] Stage 3 */
 } tlr_plan_info_t;
+
+/* One output rectangle of a plan: tile rows [i0, i1) and tile columns [j0, j1)
+ * of C's tile grid, evaluated with association order `order` (tlr_order_t:
+ * TLR_ORDER_RIGHT U (S Z^T), TLR_ORDER_LEFT (U S) Z^T (page 1, "Association
+ * order and workspace"), or TLR_ORDER_TRIPLE, the order taken per tile triple
+ * (page 2, "The O_A O_B terms")). Rectangles run in the order listed. */
+typedef struct tlr_rect {
+    int32_t i0, i1, j0, j1;
+    int32_t order;
+} tlr_rect_t;
 
 /* Metadata of a TLR x TLR product computed from ranks alone (no device use).
  * Arrays are caller-owned with the stated lengths. */
@@ -170,6 +186,11 @@ tlr_status_t tlr_plan_create(tlr_handle_t handle, tlr_op_t opA, tlr_op_t opB,
                              void *workspace, size_t workspace_bytes,
                              tlr_order_t order, tlr_plan_t *plan);
 tlr_status_t tlr_plan_info(tlr_plan_t plan, tlr_plan_info_t *info);
+/* The plan's output rectangles (host copy): at most `capacity` are written to
+ * `rects` (caller-owned; NULL when capacity is 0) and *count receives how many
+ * the plan has, so a first call with capacity 0 sizes the array. Lets a
+ * caller recount the plan's executed FLOPs from the ranks on its own. */
+tlr_status_t tlr_plan_rects(tlr_plan_t plan, tlr_rect_t *rects, int32_t capacity, int32_t *count);
 /* Run a planned product into C (device, fp32, column-major, leading dimension ldc). */
 tlr_status_t tlr_plan_execute(tlr_plan_t plan, float alpha, float beta, float *C, int64_t ldc);
 tlr_status_t tlr_plan_destroy(tlr_plan_t plan);
@@ -193,8 +214,10 @@ tlr_status_t tlr_gemm(tlr_handle_t handle, tlr_op_t opA, tlr_op_t opB, float alp
  * that must not stall on allocation).
  *   Setup: the first call on each device (that device current) looks up the
  *   array's device address with cudaGetSymbolAddress and keeps it; make that
- *   first call before any stream capture. The current device must be the
- *   handle's device.
+ *   first call before any stream capture. After the device's context has been
+ *   destroyed and re-created (cudaDeviceReset), the next call looks the
+ *   address up again. The current device must be the handle's device (the one
+ *   current at tlr_create), else TLR_STATUS_INVALID_ARG.
  *   Sharing: every call on a device, from any handle or thread, uses the same
  *   array. Calls must be ordered (one stream, or events between streams);
  *   overlapping calls race on the workspace and the counters and give wrong
@@ -239,6 +262,13 @@ tlr_status_t tlr_reset_timing(tlr_handle_t handle);
 tlr_status_t tlr_debug_check_plan(tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A,
                                   const tlr_operand_t *B, size_t workspace_bytes, tlr_order_t order,
                                   tlr_plan_info_t *info, char *msg, size_t msg_len);
+
+/* Host-only: the rectangles tlr_plan_create would choose for these operands,
+ * budget and order (same split, same per-rectangle order), without device use;
+ * pointer fields of A and B are not read. Array protocol as tlr_plan_rects. */
+tlr_status_t tlr_debug_plan_rects(tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A,
+                                  const tlr_operand_t *B, size_t workspace_bytes, tlr_order_t order,
+                                  tlr_rect_t *rects, int32_t capacity, int32_t *count);
 
 /* Test hook: device wait limit in microseconds for this handle's kernels
  * (default 2,000,000). Used by the bounded-wait test, which gives a kernel a

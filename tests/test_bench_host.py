@@ -45,3 +45,34 @@ def test_var_rank_grid_keeps_the_large_products_tiles():
             if i != j:
                 want = min(256, max(8, int(np.floor(256 * np.exp(-abs(i - j) / 4.0) + 0.5))))
                 assert r[i, j] == want
+
+
+def test_peak_follows_the_length_of_the_timed_region():
+    """Burst peak for a region shorter than three seconds, sustained from three on;
+    fp32 products are compared with the tf32 peak (bf16 x 1.1 / 2.25)."""
+    assert bench.peak_choice(74.0) == "burst" and bench.peak_choice(2999.0) == "burst"
+    assert bench.peak_choice(3000.0) == "sustained"
+    peaks = {"bf16_tflops": 1878.3, "bf16_tflops_sustained": 1704.2, "hbm_gbs": 6784.5}
+    assert bench.dtype_peaks("bf16", peaks) == (1878.3, 1704.2)
+    b, s = bench.dtype_peaks("f32", peaks)
+    assert abs(b - 1878.3 * 1.1 / 2.25) < 1e-9 and abs(s - 1704.2 * 1.1 / 2.25) < 1e-9
+
+
+def test_algorithmic_bytes_count_inputs_once_and_c_once_or_twice():
+    import tlr_inputs as ti
+    p = ti.problem(2, scale_down=4)                     # beta != 0: C read and written
+    assert bench.algorithmic_bytes(p) == bench.input_bytes(p) + 2 * p.m * p.n * 4
+    q = ti.problem(1)                                   # beta == 0: C written only
+    assert bench.algorithmic_bytes(q) == bench.input_bytes(q) + q.m * q.n * 4
+    assert bench.input_bytes(q) == q.A.nbytes_device() + q.B.nbytes_device()
+
+
+def test_near_gpu_restores_the_affinity(monkeypatch):
+    before = os.sched_getaffinity(0)
+    monkeypatch.setattr(bench, "gpu_local_cpus", lambda i: sorted(before)[:1])
+    with bench.near_gpu(0) as n:
+        assert os.sched_getaffinity(0) == set(sorted(before)[:1]) and n.cpus == sorted(before)[:1]
+    assert os.sched_getaffinity(0) == before
+    monkeypatch.setattr(bench, "gpu_local_cpus", lambda i: None)
+    with bench.near_gpu(0) as n:
+        assert n.cpus is None and os.sched_getaffinity(0) == before

@@ -11,10 +11,16 @@ import numpy as np
 import pytest
 
 import tlr_inputs as ti
+from parity_check import check, interior_extents, tile_size
 from test_parity_gpu import TOL as _TOL, handle, rel, run, sample_indices, torch_cuda  # noqa: F401
 
 pytestmark = pytest.mark.gpu
 TOL = dict(_TOL, f16=2.5e-3)
+
+
+def check_p(out, ref, p, rows=None, cols=None):
+    """Whole, per-tile and per-region parity at this element type's tolerance."""
+    return check(out, ref, TOL[p.dtype], tile_size(p), rows, cols, regions=interior_extents(p), what=p.name)
 
 
 @pytest.mark.parametrize("cfg,scale", [(4, 8), (4, 4), (5, 8), (5, 4)])
@@ -27,9 +33,8 @@ def test_fp16_workloads_match_oracle(oracle_lib, handle, cfg, scale, variant):
         kw = dict(zero_lowrank=True)
     p = ti.problem(cfg, scale_down=scale, dtype_override="f16", **kw)
     out, info = run(p, handle)
-    err = rel(out, oracle_lib.gemm_problem(p))
-    print(f"{p.name} {variant}: {err:.3e}")
-    assert np.isfinite(out).all() and err <= TOL["f16"], f"{p.name}: rel Frobenius {err:.3e}"
+    res = check_p(out, oracle_lib.gemm_problem(p), p)
+    print(f"{p.name} {variant}: {res}")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
@@ -37,9 +42,8 @@ def test_fp16_workloads_match_oracle(oracle_lib, handle, cfg, scale, variant):
 def test_skewed_grid_matches_oracle(oracle_lib, handle, dtype, n):
     p = ti.skewed_grid(n, dtype)
     out, info = run(p, handle)
-    err = rel(out, oracle_lib.gemm_problem(p))
-    print(f"{p.name}: {err:.3e}")
-    assert np.isfinite(out).all() and err <= TOL[dtype], f"{p.name}: rel Frobenius {err:.3e}"
+    res = check_p(out, oracle_lib.gemm_problem(p), p)
+    print(f"{p.name}: {res}")
 
 
 @pytest.mark.parametrize("n", [65536])
@@ -61,9 +65,8 @@ def test_skewed_grid_largest_fp16_sampled(oracle_lib, handle, n):
         got = sub.double().cpu().numpy().T
     finally:
         dp.close()
-    err = rel(got, oracle_lib.gemm_problem(p, out_rows, out_cols))
-    print(f"{p.name} sampled: {err:.3e}")
-    assert np.isfinite(got).all() and err <= TOL["f16"], f"{p.name}: sampled rel Frobenius {err:.3e}"
+    res = check_p(got, oracle_lib.gemm_problem(p, out_rows, out_cols), p, out_rows, out_cols)
+    print(f"{p.name} sampled: {res}")
 
 
 @pytest.mark.parametrize("opA,opB", [("N", "N"), ("N", "T"), ("T", "N"), ("T", "T")])
@@ -76,7 +79,7 @@ def test_fp16_transposes_with_boundary(oracle_lib, handle, opA, opB):
     C = rng.standard_normal(N * N).astype(np.float32)
     p = ti.Problem("transpose_f16", A, B, opA, opB, 0.75, -1.25, C, N, N, "f16")
     out, _ = run(p, handle)
-    assert rel(out, oracle_lib.gemm_problem(p)) <= TOL["f16"]
+    check_p(out, oracle_lib.gemm_problem(p), p)
 
 
 @pytest.mark.parametrize("left_dense", [True, False])
@@ -93,4 +96,4 @@ def test_fp16_dense_operand(oracle_lib, handle, left_dense):
         m, n = 456, 256
     p = ti.Problem("dense_tlr_f16", A, B, "N", "N", 1.0, 0.0, None, m, n, "f16")
     out, _ = run(p, handle)
-    assert rel(out, oracle_lib.gemm_problem(p)) <= TOL["f16"]
+    check_p(out, oracle_lib.gemm_problem(p), p)

@@ -3,7 +3,8 @@
 `tlr_gemm_static_scratch` keeps workspace, tables and counters in a static
 device array instead of allocating; these tests run it twice in a row (the
 counters must be re-zeroed and the tables re-uploaded each call) and compare
-each result with `tlr_gemm` on the same inputs, at the parity tolerances.
+each result with `tlr_gemm` on the same inputs and with the fp64 oracle, at the
+parity tolerances (whole C and every output tile).
 The file is named to be collected last, so it also runs after every other GPU
 test has used the library in the same process.
 """
@@ -11,6 +12,7 @@ import numpy as np
 import pytest
 
 import tlr_inputs as ti
+from parity_check import check, interior_extents, tile_size
 
 pytestmark = pytest.mark.gpu
 TOL = {"f32": 2e-3, "bf16": 1e-2}
@@ -37,7 +39,7 @@ def rel(a, b):
 
 
 @pytest.mark.parametrize("cfg,scale", [(1, 1), (5, 8), (3, 4), (2, 2)])
-def test_static_scratch_matches_workspace_entry_point(handle, torch_cuda, cfg, scale):
+def test_static_scratch_matches_workspace_entry_point(oracle_lib, handle, torch_cuda, cfg, scale):
     import gemm_tlr_gb300 as g
     from gemm_tlr_gb300.device import DeviceProblem
     p = ti.problem(cfg, scale_down=scale)
@@ -51,6 +53,7 @@ def test_static_scratch_matches_workspace_entry_point(handle, torch_cuda, cfg, s
         assert g.tlr_get_device_status(handle) == 0
         want = dp.result()
         del ws
+        ref = oracle_lib.gemm_problem(p)
         for call in range(2):
             dp.reset_c()
             g.tlr_gemm_static_scratch(handle, dp.opA, dp.opB, p.alpha, dp.A.desc, dp.B.desc, p.beta,
@@ -59,7 +62,9 @@ def test_static_scratch_matches_workspace_entry_point(handle, torch_cuda, cfg, s
             got = dp.result()
             assert np.isfinite(got).all()
             err = rel(got, want)
-            assert err <= TOL[p.dtype], f"{p.name} call {call}: rel Frobenius {err:.3e}"
+            assert err <= TOL[p.dtype], f"{p.name} call {call}: rel Frobenius {err:.3e} against tlr_gemm"
+            check(got, ref, TOL[p.dtype], tile_size(p), regions=interior_extents(p),
+                  what=f"{p.name} call {call} against the oracle")
     finally:
         dp.close()
 
