@@ -577,7 +577,7 @@ struct Slot {
   int32_t pad_[4];
   Seg segs[kMaxSegs];        // at 96
   int64_t pad2_[4];
-  int64_t rowdst[kBM];       // at 256: output row of each tile row, -1 when the row is not stored
+  int64_t rowdst[kBM];       // at 384: output row of each tile row, -1 when the row is not stored
 };
 static_assert(sizeof(Slot) <= kSlotBytes, "slot size");
 

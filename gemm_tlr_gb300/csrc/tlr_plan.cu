@@ -399,6 +399,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct Rect {
   int i0, i1, j0, j1;
   bool left;
+  bool triple = false;   // per-triple order (left ignored)
 };
 
 struct Launch {
@@ -908,6 +909,478 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
   B.fl_launch[2] += B.fl_s3 + B.fl_dense - before3;
 }
 
+// ------------------------------------------------------------------ per-triple order
+// "TLR Matrix Multiplication", section "The O_A O_B terms": once the coupling
+// product S_ikj = V_ik^T W_kj is formed, each tile triple (i, k, j) takes the
+// cheaper of the two remaining contractions, decided by min(r_ik, r_kj):
+//   right  T^R_ikj = S_ikj Z_kj^T (r_ik x d_j), then C_ij += U_ik T^R_ikj   (r_ik <= r_kj)
+//   left   T^L_ikj = U_ik S_ikj   (d_i x r_kj), then C_ij += T^L_ikj Z_kj^T (r_kj <  r_ik)
+// so the final product of a pair (i, j) runs over K = sum_k min(r_ik, r_kj)
+// instead of rho_i (or gamma_j). The dense-tile terms take a fixed side: the
+// k = j block V_ij^T D_jj is a right block (K = r_ij), the k = i block
+// D_ii W_ij is a left block (P_ij, K = r_ij), and D_ii D_ii is a segment of its own.
+//
+// Storage (one rectangle of output tiles): the coupling products S_k^T as in the
+// per-rectangle orders (one Stage-1 product per k, shared by both sides); the
+// right blocks of a pair (i, j), in ascending k, form a matrix T^R_ij of
+// sum r_ik rows and d_j columns, the left blocks (transposed, T^L_ikj^T, r_kj x d_i)
+// a matrix T^L_ij; all of them are packed into two row-major buffers with one
+// leading dimension, so nothing is stored for a block the pair does not use.
+// Stage 2 of the right side is fused over i (one product per (k, j), rows of
+// S_k^T for the tile rows that take the right side), that of the left side over j
+// (one product per (k, i): T^L^T = S^T U_ik^T). The final product of a tile of C
+// is one K-loop over the runs of consecutive right blocks (U_i panel against
+// T^R_ij) and of left blocks (T^L_ij against the Z_j panel).
+//
+// A task's K-loop takes at most kMaxSegs operand segments. When the sides of a
+// pair alternate so often that its runs need more, the run whose side change
+// costs the fewest extra final-product FLOPs is given the other side, until the
+// tile fits (never needed for rank maps that decay with |i - j|).
+
+enum : uint8_t { kSideNone = 0, kSideRight = 1, kSideLeft = 2 };
+
+struct TripleLayout {
+  int i0 = 0, i1 = 0, j0 = 0, j1 = 0, nk = 0;
+  std::vector<int64_t> Soff, Sld, Ssig;        // per k, as RectLayout
+  std::vector<std::vector<int64_t>> Srow;      // per k, per j: first row of block j in S_k^T
+  std::vector<uint8_t> side;                   // per (i, j, k): kSide*
+  std::vector<int64_t> trow;                   // per (i, j, k): row of the block in its buffer, -1
+  std::vector<int64_t> tR0, tRn, tL0, tLn;     // per (i, j): first row and rows of T^R_ij, T^L_ij
+  int64_t ldT = 0, TRoff = 0, TLoff = 0, TRrows = 0, TLrows = 0;
+  int64_t bytes = 0;
+  size_t ij(int i, int j) const { return static_cast<size_t>(i - i0) * (j1 - j0) + (j - j0); }
+  size_t ijk(int i, int j, int k) const { return ij(i, j) * nk + k; }
+};
+
+// Operand segments of the final product of pair (i, j) under `side`, in K-loop
+// order: right runs over the U_i panel parts, then left runs over the Z_j panel
+// parts. Each entry: (panel part view restricted to the run, first block k, run width).
+struct TripleRun {
+  bool right;
+  View panel;          // U_i columns (right) or Z_j columns (left) of the run
+  int k_first;
+  int64_t width;
+};
+
+std::vector<TripleRun> triple_runs(const LOp &X, const LOp &Y, const TripleLayout &L, int i, int j, int es) {
+  std::vector<TripleRun> out;
+  // right: U_i panel, tiles k of op(A)'s row i in panel order
+  for (const Part &p : X.rowp[i]) {
+    bool open = false;
+    int64_t c0 = 0, c1 = 0;
+    int kf = -1;
+    for (int k = p.t0; k < p.t1; ++k) {
+      if (X.rpos[i][k] < 0) continue;
+      const int64_t r = X.r(i, k);
+      if (r == 0) continue;
+      const bool in = L.side[L.ijk(i, j, k)] == kSideRight;
+      const int64_t lc = X.rpos[i][k] - p.col0;
+      if (in && !open) { open = true; c0 = lc; kf = k; }
+      if (in) c1 = lc + r;
+      if (!in && open) { out.push_back(TripleRun{true, sub_cols(p.v, c0, c1, es), kf, c1 - c0}); open = false; }
+    }
+    if (open) out.push_back(TripleRun{true, sub_cols(p.v, c0, c1, es), kf, c1 - c0});
+  }
+  // left: Z_j panel, tiles k of op(B)'s column j in panel order
+  for (const Part &p : Y.colp[j]) {
+    bool open = false;
+    int64_t c0 = 0, c1 = 0;
+    int kf = -1;
+    for (int k = p.t0; k < p.t1; ++k) {
+      if (Y.cpos[j][k] < 0) continue;
+      const int64_t r = Y.r(k, j);
+      if (r == 0) continue;
+      const bool in = L.side[L.ijk(i, j, k)] == kSideLeft;
+      const int64_t lc = Y.cpos[j][k] - p.col0;
+      if (in && !open) { open = true; c0 = lc; kf = k; }
+      if (in) c1 = lc + r;
+      if (!in && open) { out.push_back(TripleRun{false, sub_cols(p.v, c0, c1, es), kf, c1 - c0}); open = false; }
+    }
+    if (open) out.push_back(TripleRun{false, sub_cols(p.v, c0, c1, es), kf, c1 - c0});
+  }
+  return out;
+}
+
+// Side of every (i, k, j) of the rectangle by min(r_ik, r_kj) (tie: right), the
+// fixed sides of the dense-tile blocks, and the coarsening that keeps every
+// output tile within kMaxSegs segments.
+void triple_sides(const LOp &X, const LOp &Y, TripleLayout &L, int es) {
+  const int nk = X.nc;
+  L.side.assign(static_cast<size_t>(L.i1 - L.i0) * (L.j1 - L.j0) * nk, kSideNone);
+  for (int i = L.i0; i < L.i1; ++i)
+    for (int j = L.j0; j < L.j1; ++j) {
+      for (int k = 0; k < nk; ++k) {
+        uint8_t sd = kSideNone;
+        if (X.dt(i, k)) {                       // k = i: D_ii B_ij
+          if (!Y.dt(k, j) && Y.r(k, j) > 0) sd = kSideLeft;        // P_ij = D_ii W_ij
+        } else if (Y.dt(k, j)) {                // k = j: A_ij D_jj
+          if (X.r(i, k) > 0) sd = kSideRight;                       // V_ij^T D_jj
+        } else if (X.r(i, k) > 0 && Y.r(k, j) > 0) {
+          sd = X.r(i, k) <= Y.r(k, j) ? kSideRight : kSideLeft;
+        }
+        L.side[L.ijk(i, j, k)] = sd;
+      }
+      const bool dd = X.dt(i, i) && i < Y.nr && Y.dt(i, j);   // D_ii D_ii segment
+      const size_t cap = static_cast<size_t>(kMaxSegs - (dd ? 1 : 0));
+      std::vector<uint8_t> locked(nk, 0);                       // a block changes side at most once
+      for (;;) {
+        std::vector<TripleRun> runs = triple_runs(X, Y, L, i, j, es);
+        if (runs.size() <= cap) break;
+        // cheapest run to give the other side (dense-tile blocks keep theirs)
+        double best = 1e300;
+        int bk0 = -1, bk1 = -1;
+        bool bright = true;
+        for (const TripleRun &ru : runs) {
+          // the run's blocks: consecutive ks from k_first covering `width` columns
+          double extra = 0;
+          int64_t w = 0;
+          int k = ru.k_first, klast = ru.k_first;
+          bool fixed = false;
+          for (; k < nk && w < ru.width; ++k) {
+            const uint8_t sd = L.side[L.ijk(i, j, k)];
+            if (sd != (ru.right ? kSideRight : kSideLeft)) continue;
+            if (X.dt(i, k) || Y.dt(k, j) || locked[k]) { fixed = true; break; }
+            const int64_t ra = X.r(i, k), rb = Y.r(k, j);
+            w += ru.right ? ra : rb;
+            extra += 2.0 * static_cast<double>(X.rd[i]) * static_cast<double>(Y.cd[j]) *
+                     static_cast<double>(ru.right ? rb - ra : ra - rb);
+            klast = k;
+          }
+          if (fixed) continue;
+          if (extra < best) { best = extra; bk0 = ru.k_first; bk1 = klast; bright = ru.right; }
+        }
+        if (bk0 < 0) {
+          // nothing left to move run by run: one side for every block that can take
+          // either (the cheaper one for the pair), which leaves a run per panel part
+          double fr = 0, fl = 0;
+          for (int k = 0; k < nk; ++k)
+            if (!X.dt(i, k) && !Y.dt(k, j) && L.side[L.ijk(i, j, k)] != kSideNone) { fr += X.r(i, k); fl += Y.r(k, j); }
+          for (int k = 0; k < nk; ++k)
+            if (!X.dt(i, k) && !Y.dt(k, j) && L.side[L.ijk(i, j, k)] != kSideNone)
+              L.side[L.ijk(i, j, k)] = fr <= fl ? kSideRight : kSideLeft;
+          break;
+        }
+        for (int k = bk0; k <= bk1; ++k) {
+          uint8_t &sd = L.side[L.ijk(i, j, k)];
+          if (sd == (bright ? kSideRight : kSideLeft) && !X.dt(i, k) && !Y.dt(k, j)) {
+            sd = bright ? kSideLeft : kSideRight;
+            locked[k] = 1;
+          }
+        }
+      }
+    }
+}
+
+TripleLayout layout_triple(const LOp &X, const LOp &Y, int i0, int i1, int j0, int j1, int es) {
+  TripleLayout L;
+  L.i0 = i0; L.i1 = i1; L.j0 = j0; L.j1 = j1;
+  L.nk = X.nc;
+  const int nk = X.nc;
+  int64_t off = 0;
+  L.Soff.assign(nk, -1); L.Sld.assign(nk, 0); L.Ssig.assign(nk, 0); L.Srow.assign(nk, {});
+  for (int k = 0; k < nk; ++k) {
+    int64_t sig = 0;
+    for (int i = i0; i < i1; ++i) if (!X.dt(i, k)) sig += X.r(i, k);
+    L.Ssig[k] = sig;
+    L.Srow[k].assign(j1 - j0, -1);
+    int64_t g = 0;
+    for (int j = j0; j < j1; ++j)
+      if (!Y.dt(k, j) && Y.r(k, j) > 0) { L.Srow[k][j - j0] = g; g += align_up(Y.r(k, j), 8); }
+    if (sig == 0 || g == 0) continue;
+    L.Sld[k] = g;
+    L.Soff[k] = off;
+    off = align_up(off + g * sig * es, 256);
+  }
+  triple_sides(X, Y, L, es);
+  int64_t dmax = 8;
+  for (int j = j0; j < j1; ++j) dmax = std::max(dmax, Y.cd[j]);
+  for (int i = i0; i < i1; ++i) dmax = std::max(dmax, X.rd[i]);
+  L.ldT = align_up(dmax, 8);
+  const size_t npair = static_cast<size_t>(i1 - i0) * (j1 - j0);
+  L.tR0.assign(npair, 0); L.tRn.assign(npair, 0); L.tL0.assign(npair, 0); L.tLn.assign(npair, 0);
+  L.trow.assign(npair * nk, -1);
+  int64_t rr = 0, rl = 0;
+  for (int i = i0; i < i1; ++i)
+    for (int j = j0; j < j1; ++j) {
+      const size_t q = L.ij(i, j);
+      L.tR0[q] = rr;
+      L.tL0[q] = rl;
+      for (int k = 0; k < nk; ++k) {
+        const uint8_t sd = L.side[L.ijk(i, j, k)];
+        if (sd == kSideRight) { L.trow[L.ijk(i, j, k)] = rr; rr += X.r(i, k); }
+        else if (sd == kSideLeft) { L.trow[L.ijk(i, j, k)] = rl; rl += Y.r(k, j); }
+      }
+      L.tRn[q] = rr - L.tR0[q];
+      L.tLn[q] = rl - L.tL0[q];
+      rr = align_up(rr, 8);
+      rl = align_up(rl, 8);
+    }
+  L.TRrows = std::max<int64_t>(rr, 8);
+  L.TLrows = std::max<int64_t>(rl, 8);
+  L.TRoff = off;
+  off = align_up(off + L.TRrows * L.ldT * es, 256);
+  L.TLoff = off;
+  off = align_up(off + L.TLrows * L.ldT * es, 256);
+  L.bytes = off;
+  return L;
+}
+
+// Final-stage FLOPs of the per-triple order over a rectangle (right blocks
+// K = r_ik, left blocks K = r_kj, the dense-tile blocks included).
+double triple_final_cost(const LOp &X, const LOp &Y, const TripleLayout &L) {
+  double f = 0;
+  for (int i = L.i0; i < L.i1; ++i)
+    for (int j = L.j0; j < L.j1; ++j)
+      for (int k = 0; k < L.nk; ++k) {
+        const uint8_t sd = L.side[L.ijk(i, j, k)];
+        if (sd == kSideNone) continue;
+        const double K = sd == kSideRight ? X.r(i, k) : Y.r(k, j);
+        f += 2.0 * static_cast<double>(X.rd[i]) * static_cast<double>(Y.cd[j]) * K;
+      }
+  return f;
+}
+
+void build_rect_triple(Builder &B, const TripleLayout &L, std::vector<Task> &l1, std::vector<Task> &l2,
+                       std::vector<Task> &l3) {
+  const LOp &X = B.X;
+  const LOp &Y = B.Y;
+  const int es = B.es, bn = B.bn;
+  const int i0 = L.i0, i1 = L.i1, j0 = L.j0, j1 = L.j1, nk = L.nk;
+  const uint64_t TR = B.ws + static_cast<uint64_t>(L.TRoff), TL = B.ws + static_cast<uint64_t>(L.TLoff);
+  const int outR = B.out_ws(TR, L.ldT, true), outL = B.out_ws(TL, L.ldT, true);
+  auto xcol = [&X](int k) { return [&X, k](int i) { return static_cast<int64_t>(X.r(i, k)); }; };
+  auto yrow = [&Y](int k) { return [&Y, k](int j) { return static_cast<int64_t>(Y.r(k, j)); }; };
+  int64_t BM = B.l1_bm;
+  B.cur_pair = B.l1_pair;
+
+  // ---------------- L1: Stage 1 (shared), V_ij^T D_jj into T^R, D_ii W_ij (transposed) into T^L
+  B.tasks = &l1;
+  for (int k = 0; k < nk; ++k) {
+    std::vector<RPart> Ap = restrict_panel(X.colp[k], X.cpos[k], i0, i1, xcol(k), es);
+    if (Ap.empty()) continue;
+    if (L.Soff[k] >= 0) {
+      B.deps(B.cS0 >= 0 ? B.cS0 + k : -1, 1, B.war, -1);
+      const uint64_t S = B.ws + static_cast<uint64_t>(L.Soff[k]);
+      const int outS = B.out_ws(S, L.Sld[k]);
+      std::vector<RPart> Bp = restrict_panel(Y.rowp[k], Y.rpos[k], j0, j1, yrow(k), es);
+      for (const RPart &bp : Bp) {
+        const ORef am = B.input(bp.v, false);
+        for (int64_t mt = 0; mt < ceil_div(bp.v.cols, BM); ++mt) {
+          const int64_t rows = std::min<int64_t>(BM, bp.v.cols - mt * BM);
+          auto pc = pieces_for(bp, 0, mt * BM, rows, [&](int j) { return L.Srow[k][j - j0]; });
+          int64_t ra = 0;
+          for (const RPart &ap : Ap) {
+            const ORef bm = B.input(ap.v, false);
+            for (int64_t nt = 0; nt < ceil_div(ap.v.cols, bn); ++nt)
+              B.emit(outS, 0, ra + nt * bn, rows, std::min<int64_t>(bn, ap.v.cols - nt * bn),
+                     {Builder::seg(am, bm, mt * BM, nt * bn, X.cd[k])}, pc);
+            ra += ap.v.cols;
+          }
+        }
+        for (const RPart &ap : Ap) B.fl_s1 += 2.0 * ap.v.cols * static_cast<double>(bp.v.cols) * X.cd[k];
+      }
+    }
+    // k = j: T^R_ij block k=j = V_ij^T D_jj for the tile rows i of the rectangle
+    if (k >= j0 && k < j1 && k < Y.nr && Y.dt(k, k)) {
+      B.deps(B.cPrep, 1, B.war, -1);
+      const ORef bm = B.input(Y.diag[k], Y.diag_trans);
+      for (const RPart &ap : Ap) {
+        const ORef am = B.input(ap.v, false);
+        for (int64_t mt = 0; mt < ceil_div(ap.v.cols, BM); ++mt) {
+          const int64_t rows = std::min<int64_t>(BM, ap.v.cols - mt * BM);
+          auto pc = pieces_for(ap, 0, mt * BM, rows, [&](int i) { return L.trow[L.ijk(i, k, k)]; });
+          for (int64_t nt = 0; nt < ceil_div(Y.cd[k], bn); ++nt)
+            B.emit(outR, 0, nt * bn, rows, std::min<int64_t>(bn, Y.cd[k] - nt * bn),
+                   {Builder::seg(am, bm, mt * BM, nt * bn, Y.rd[k])}, pc);
+        }
+        B.fl_dense += 2.0 * ap.v.cols * static_cast<double>(Y.cd[k]) * Y.rd[k];
+      }
+    }
+  }
+  // k = i: T^L_ij block k=i = (D_ii W_ij)^T = W_ij^T D_ii^T, for the tile columns j
+  for (int i = i0; i < i1; ++i) {
+    if (!(i < X.nc && X.dt(i, i))) continue;
+    std::vector<RPart> Bp = restrict_panel(Y.rowp[i], Y.rpos[i], j0, j1, yrow(i), es);
+    if (Bp.empty()) continue;
+    B.deps(B.cPrep, 1, B.war, -1);
+    const ORef dm = B.input(X.diag[i], !X.diag_trans);
+    for (const RPart &bp : Bp) {
+      const ORef am = B.input(bp.v, false);
+      for (int64_t mt = 0; mt < ceil_div(bp.v.cols, BM); ++mt) {
+        const int64_t rows = std::min<int64_t>(BM, bp.v.cols - mt * BM);
+        auto pc = pieces_for(bp, 0, mt * BM, rows, [&](int j) { return L.trow[L.ijk(i, j, i)]; });
+        for (int64_t nt = 0; nt < ceil_div(X.rd[i], bn); ++nt)
+          B.emit(outL, 0, nt * bn, rows, std::min<int64_t>(bn, X.rd[i] - nt * bn),
+                 {Builder::seg(am, dm, mt * BM, nt * bn, X.cd[i])}, pc);
+      }
+      B.fl_dense += 2.0 * X.rd[i] * static_cast<double>(bp.v.cols) * X.cd[i];
+    }
+  }
+  B.fl_launch[0] += B.fl_s1 + B.fl_dense;
+
+  // ---------------- L2: Stage 2 of both sides
+  const double before2 = B.fl_s2;
+  B.tasks = &l2;
+  BM = B.prep_bm;
+  B.cur_pair = B.prep_pair;
+  for (int k = 0; k < nk; ++k) {
+    if (L.Soff[k] < 0) continue;
+    const uint64_t S = B.ws + static_cast<uint64_t>(L.Soff[k]);
+    B.deps(B.cPrep, 1, B.cS0 >= 0 ? B.cS0 + k : -1, B.war);
+    std::vector<RPart> Ap = restrict_panel(X.colp[k], X.cpos[k], i0, i1, xcol(k), es);
+    // rows of S_k^T's columns: tile row i of the rectangle at sigma position
+    std::vector<std::pair<int, int64_t>> ipos;   // (i, column of block i in S_k^T)
+    {
+      int64_t acc = 0;
+      for (const RPart &ap : Ap) {
+        for (size_t q = 0; q < ap.tiles.size(); ++q) ipos.push_back({ap.tiles[q].first, acc + ap.tiles[q].second});
+        acc += ap.v.cols;
+      }
+    }
+    // right: per j, T^R rows S_ikj Z_kj^T for the i that take the right side (fused over i)
+    for (int j = j0; j < j1; ++j) {
+      if (Y.dt(k, j) || Y.r(k, j) <= 0) continue;
+      const int64_t r = Y.r(k, j);
+      // runs of consecutive tile rows (in S_k^T column order) on the right side
+      std::vector<std::pair<int64_t, int64_t>> mr;   // [m0, m1) in S_k^T columns
+      std::vector<std::vector<std::pair<int, int64_t>>> mi;
+      for (auto &ip : ipos) {
+        const int i = ip.first;
+        const int64_t w = X.r(i, k);
+        if (w == 0) continue;
+        const bool in = L.side[L.ijk(i, j, k)] == kSideRight;
+        if (!in) continue;
+        if (!mr.empty() && mr.back().second == ip.second) { mr.back().second += w; mi.back().push_back(ip); }
+        else { mr.push_back({ip.second, ip.second + w}); mi.push_back({ip}); }
+      }
+      if (mr.empty()) continue;
+      const ORef am = B.work(View{S + static_cast<uint64_t>(L.Srow[k][j - j0] * es), r, L.Ssig[k], L.Sld[k]});
+      const ORef bm = B.input(Y.inner[static_cast<size_t>(k) * Y.nc + j], true);
+      for (size_t q = 0; q < mr.size(); ++q) {
+        const int64_t m0 = mr[q].first, mlen = mr[q].second - mr[q].first;
+        B.fl_s2 += 2.0 * mlen * static_cast<double>(Y.cd[j]) * r;
+        for (int64_t mt = 0; mt < ceil_div(mlen, BM); ++mt) {
+          const int64_t rows = std::min<int64_t>(BM, mlen - mt * BM);
+          std::vector<Piece> pc;
+          for (auto &ip : mi[q]) {
+            const int64_t s = ip.second - m0, e = s + X.r(ip.first, k);
+            const int64_t a = std::max(s, mt * BM), b2 = std::min(e, mt * BM + rows);
+            if (a >= b2) continue;
+            Piece pe;
+            pe.src0 = static_cast<int32_t>(a - mt * BM);
+            pe.len = static_cast<int32_t>(b2 - a);
+            pe.dst0 = L.trow[L.ijk(ip.first, j, k)] + (a - s);
+            pc.push_back(pe);
+          }
+          for (int64_t nt = 0; nt < ceil_div(Y.cd[j], bn); ++nt)
+            B.emit(outR, 0, nt * bn, rows, std::min<int64_t>(bn, Y.cd[j] - nt * bn),
+                   {Builder::seg(am, bm, m0 + mt * BM, nt * bn, r)}, pc);
+        }
+      }
+    }
+    // left: per i, T^L rows (U_ik S_ikj)^T = S_ikj^T U_ik^T for the j that take the left side (fused over j)
+    for (auto &ip : ipos) {
+      const int i = ip.first;
+      const int64_t r = X.r(i, k);
+      if (r == 0) continue;
+      std::vector<std::pair<int64_t, int64_t>> mr;   // [m0, m1) in S_k^T rows
+      std::vector<std::vector<int>> mj;
+      for (int j = j0; j < j1; ++j) {
+        if (Y.dt(k, j) || Y.r(k, j) <= 0) continue;
+        if (L.side[L.ijk(i, j, k)] != kSideLeft) continue;
+        const int64_t s = L.Srow[k][j - j0], e = s + Y.r(k, j);
+        // consecutive S_k^T row blocks (padding rows between them are computed, not stored)
+        if (!mr.empty() && align_up(mr.back().second, 8) == s) { mr.back().second = e; mj.back().push_back(j); }
+        else { mr.push_back({s, e}); mj.push_back({j}); }
+      }
+      if (mr.empty()) continue;
+      // A = S_k^T columns of block i, read MN-major (M = rows of S_k^T, K = r_ik)
+      const ORef am = ORef{B.map_of(View{S + static_cast<uint64_t>(ip.second * L.Sld[k] * es), L.Sld[k], r, L.Sld[k]}, true), true};
+      const ORef bm = B.input(X.outer[static_cast<size_t>(i) * X.nc + k], true);
+      for (size_t q = 0; q < mr.size(); ++q) {
+        const int64_t m0 = mr[q].first, mlen = mr[q].second - mr[q].first;
+        for (int j : mj[q]) B.fl_s2 += 2.0 * Y.r(k, j) * static_cast<double>(X.rd[i]) * r;
+        for (int64_t mt = 0; mt < ceil_div(mlen, BM); ++mt) {
+          const int64_t rows = std::min<int64_t>(BM, mlen - mt * BM);
+          std::vector<Piece> pc;
+          for (int j : mj[q]) {
+            const int64_t s = L.Srow[k][j - j0] - m0, e = s + Y.r(k, j);
+            const int64_t a = std::max(s, mt * BM), b2 = std::min(e, mt * BM + rows);
+            if (a >= b2) continue;
+            Piece pe;
+            pe.src0 = static_cast<int32_t>(a - mt * BM);
+            pe.len = static_cast<int32_t>(b2 - a);
+            pe.dst0 = L.trow[L.ijk(i, j, k)] + (a - s);
+            pc.push_back(pe);
+          }
+          if (pc.empty()) continue;
+          for (int64_t nt = 0; nt < ceil_div(X.rd[i], bn); ++nt)
+            B.emit(outL, 0, nt * bn, rows, std::min<int64_t>(bn, X.rd[i] - nt * bn),
+                   {Builder::seg(am, bm, m0 + mt * BM, nt * bn, r)}, pc);
+        }
+      }
+    }
+  }
+  B.fl_launch[1] += B.fl_s2 - before2;
+
+  // ---------------- L3: C[i, j] = alpha (right runs + left runs + D_ii D_ii) + beta C
+  const double before3 = B.fl_s3 + B.fl_dense;
+  B.tasks = &l3;
+  BM = B.bm;
+  B.cur_pair = B.pair;
+  const int outC = B.out_c();
+  B.deps(B.cL3, 0, B.cPrep, -1);
+  for (int i = i0; i < i1; ++i)
+    for (int j = j0; j < j1; ++j) {
+      const size_t q = L.ij(i, j);
+      std::vector<TripleRun> runs = triple_runs(X, Y, L, i, j, es);
+      struct SegOps { ORef a, b; int64_t k; bool a_is_pair_rows; };
+      std::vector<SegOps> ops;
+      for (const TripleRun &ru : runs) {
+        const int64_t row0 = L.trow[L.ijk(i, j, ru.k_first)];
+        if (ru.right) {
+          // A = U_i run (MN-major), B = T^R_ij rows (row-major: MN-major B)
+          const ORef a = B.input(ru.panel, true);
+          const ORef b = ORef{B.map_of(View{TR + static_cast<uint64_t>(row0 * L.ldT * es), Y.cd[j], ru.width, L.ldT}, true), true};
+          ops.push_back(SegOps{a, b, ru.width, false});
+        } else {
+          // A = T^L_ij rows (transposed blocks: MN-major A), B = Z_j run (MN-major)
+          const ORef a = ORef{B.map_of(View{TL + static_cast<uint64_t>(row0 * L.ldT * es), X.rd[i], ru.width, L.ldT}, true), true};
+          const ORef b = B.input(ru.panel, true);
+          ops.push_back(SegOps{a, b, ru.width, true});
+        }
+      }
+      // FLOPs: every block of the pair (the k = i block counts as a dense-tile term)
+      for (int k = 0; k < nk; ++k) {
+        const uint8_t sd = L.side[L.ijk(i, j, k)];
+        if (sd == kSideNone) continue;
+        const double f = 2.0 * static_cast<double>(X.rd[i]) * static_cast<double>(Y.cd[j]) *
+                         (sd == kSideRight ? X.r(i, k) : Y.r(k, j));
+        if (X.dt(i, k)) B.fl_dense += f; else B.fl_s3 += f;
+      }
+      ORef da, db;
+      int64_t dk = 0;
+      if (X.dt(i, i) && i < Y.nr && Y.dt(i, j)) {
+        da = B.input(X.diag[i], !X.diag_trans);
+        db = B.input(Y.diag[i], Y.diag_trans);
+        dk = X.cd[i];
+        B.fl_dense += 2.0 * X.rd[i] * static_cast<double>(Y.cd[j]) * dk;
+      }
+      (void)q;
+      const int64_t nnt = ceil_div(Y.cd[j], bn), nmt = ceil_div(X.rd[i], BM);
+      for (int64_t nt0 = 0; nt0 < nnt; nt0 += kTicketBatch)
+        for (int64_t mt = 0; mt < nmt; ++mt)
+          for (int64_t nt = nt0; nt < std::min<int64_t>(nnt, nt0 + kTicketBatch); ++nt) {
+            std::vector<Seg> sg;
+            for (const SegOps &o : ops) sg.push_back(Builder::seg(o.a, o.b, mt * BM, nt * bn, o.k));
+            if (dk > 0) sg.push_back(Builder::seg(da, db, mt * BM, nt * bn, dk));
+            B.emit(outC, X.ro[i] + mt * BM, Y.co[j] + nt * bn, std::min<int64_t>(BM, X.rd[i] - mt * BM),
+                   std::min<int64_t>(bn, Y.cd[j] - nt * bn), sg, {});
+          }
+    }
+  B.fl_launch[2] += B.fl_s3 + B.fl_dense - before3;
+}
+
 // Sort a launch's tasks by decreasing K so the persistent CTAs finish together.
 void sort_by_work(std::vector<Task> &v, const std::vector<Seg> &segs) {
   std::stable_sort(v.begin(), v.end(), [&](const Task &a, const Task &b) {
@@ -933,6 +1406,7 @@ int device_sms() {
 // ------------------------------------------------------------------ handle / plan
 struct tlr_handle_s {
   cudaStream_t stream = nullptr;
+  int device = -1;                      // device current at tlr_create
   unsigned int *d_err = nullptr;
   bool timing = false;
   std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> ev_used;
@@ -956,6 +1430,7 @@ struct tlr_plan_s {
   const Piece *d_pieces = nullptr;
   const Out *d_outs = nullptr;
   std::vector<Launch> launches;
+  std::vector<tlr_rect_t> rects;          // output rectangles in execution order
   std::vector<const float *> round_src;
   std::vector<float *> round_dst;
   std::vector<int64_t> round_n;
@@ -1122,6 +1597,17 @@ tlr_status_t core_init(PlanCore &pc, tlr_op_t opA, tlr_op_t opB, const tlr_opera
 }
 
 // Workspace bytes of rectangle (rows [i0,i1), cols [j0,j1) of C) under an order.
+// Workspace bytes of a per-triple rectangle (the right-order operands X = op(A), Y = op(B)).
+int64_t rect_bytes_triple(const PlanCore &pc, int i0, int i1, int j0, int j1, int es) {
+  return layout_triple(pc.XR, pc.YR, i0, i1, j0, j1, es).bytes;
+}
+
+// The per-triple order needs two TLR operands and a 16-bit element type (its
+// left-side Stage 2 reads the coupling products MN-major).
+bool can_triple(const PlanCore &pc) {
+  return pc.can_right && pc.can_left && pc.pv.dtype != TLR_F32;
+}
+
 int64_t rect_bytes(const PlanCore &pc, int i0, int i1, int j0, int j1, bool left, int es) {
   if (!left) return layout_rect(pc.XR, pc.YR, i0, i1, j0, j1, es).bytes;
   return layout_rect(pc.XL, pc.YL, j0, j1, i0, i1, es).bytes;
@@ -1140,6 +1626,8 @@ double rect_cost(const PlanCore &pc, int i0, int i1, int j0, int j1, bool left) 
 
 // Order for a rectangle: cheaper feasible one (tie: right); -1 if none fits.
 int choose(const PlanCore &pc, int i0, int i1, int j0, int j1, int64_t arena, tlr_order_t force, int es) {
+  if (force == TLR_ORDER_TRIPLE)
+    return can_triple(pc) && rect_bytes_triple(pc, i0, i1, j0, j1, es) <= arena ? 2 : -1;
   const bool r_ok = pc.can_right && force != TLR_ORDER_LEFT && rect_bytes(pc, i0, i1, j0, j1, false, es) <= arena;
   const bool l_ok = pc.can_left && force != TLR_ORDER_RIGHT && rect_bytes(pc, i0, i1, j0, j1, true, es) <= arena;
   if (r_ok && l_ok) return rect_cost(pc, i0, i1, j0, j1, true) < rect_cost(pc, i0, i1, j0, j1, false) ? 1 : 0;
@@ -1172,7 +1660,7 @@ bool split(const PlanCore &pc, int64_t arena, tlr_order_t force, int es, std::ve
              choose(pc, i0, i1 + 1, j0, j1, arena, force, es) >= 0)
         ++i1;
       const int o = choose(pc, i0, i1, j0, j1, arena, force, es);
-      rects.push_back(Rect{i0, i1, j0, j1, o == 1});
+      rects.push_back(Rect{i0, i1, j0, j1, o == 1, o == 2});
       i0 = i1;
     }
   }
@@ -1236,6 +1724,7 @@ bool plan_split(const PlanCore &pc, int64_t budget, tlr_order_t force, int es, s
                 int &narenas) {
   const int64_t avail = budget - pc.fixed;
   if (avail < 0) return false;
+  if (force == TLR_ORDER_TRIPLE && !can_triple(pc)) return false;
   {
     const int bn = choose_bn(pc), pair = choose_pair(pc, bn);
     if (choose_prep_pair(pc, bn, pair) != pair) {
@@ -1247,7 +1736,10 @@ bool plan_split(const PlanCore &pc, int64_t budget, tlr_order_t force, int es, s
       // (16384 x 16384 TLR times a dense 16384 x 4096: 0.54 ms in one, 0.66 in four).
       narenas = 1;
       const bool dense_operand = pc.pv.dense_left || pc.pv.dense_right;
-      return split(pc, avail, force, es, rects, dense_operand ? 0 : pipeline_rows(pc));
+      // per-triple plans also take the fewest rectangles (large product: 2.41 ms
+      // in one, 2.64 in four): their terminal blocks are small and the order no
+      // longer depends on the rectangle
+      return split(pc, avail, force, es, rects, dense_operand || force == TLR_ORDER_TRIPLE ? 0 : pipeline_rows(pc));
     }
   }
   const int cap = pipeline_rows(pc);
@@ -1272,7 +1764,9 @@ bool plan_split(const PlanCore &pc, int64_t budget, tlr_order_t force, int es, s
 
 int64_t max_rect_bytes(const PlanCore &pc, const std::vector<Rect> &rects, int es) {
   int64_t m = 0;
-  for (const Rect &r : rects) m = std::max(m, rect_bytes(pc, r.i0, r.i1, r.j0, r.j1, r.left, es));
+  for (const Rect &r : rects)
+    m = std::max(m, r.triple ? rect_bytes_triple(pc, r.i0, r.i1, r.j0, r.j1, es)
+                             : rect_bytes(pc, r.i0, r.i1, r.j0, r.j1, r.left, es));
   return m;
 }
 
@@ -1318,6 +1812,8 @@ struct Tables {
   std::vector<uint64_t> rect_arena;         // arena base of each rectangle
   std::vector<RectLayout> layouts;          // per rectangle (in the order it was built)
   std::vector<uint8_t> rect_left;
+  std::vector<uint8_t> rect_triple;
+  std::vector<TripleLayout> tlayouts;       // per rectangle (empty unless per-triple)
   tlr_plan_info_t info{};
 };
 
@@ -1386,14 +1882,22 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
   std::vector<int32_t> cl3(rects.size(), -1);
   for (size_t ri = 0; ri < rects.size(); ++ri) {
     const Rect &r = rects[ri];
-    const LOp &X = r.left ? pc.XL : pc.XR;
-    const LOp &Y = r.left ? pc.YL : pc.YR;
-    const int i0 = r.left ? r.j0 : r.i0, i1 = r.left ? r.j1 : r.i1;
-    const int j0 = r.left ? r.i0 : r.j0, j1 = r.left ? r.i1 : r.j1;
-    RectLayout L = layout_rect(X, Y, i0, i1, j0, j1, es);
-    if (L.Trows >= INT32_MAX) return TLR_STATUS_UNSUPPORTED;   // the epilogue holds T rows in 32 bits
+    const bool lft = r.left && !r.triple;
+    const LOp &X = lft ? pc.XL : pc.XR;
+    const LOp &Y = lft ? pc.YL : pc.YR;
+    const int i0 = lft ? r.j0 : r.i0, i1 = lft ? r.j1 : r.i1;
+    const int j0 = lft ? r.i0 : r.j0, j1 = lft ? r.i1 : r.j1;
+    RectLayout L;
+    TripleLayout TL3;
+    if (r.triple) {
+      TL3 = layout_triple(X, Y, i0, i1, j0, j1, es);
+      if (TL3.TRrows >= INT32_MAX || TL3.TLrows >= INT32_MAX) return TLR_STATUS_UNSUPPORTED;
+    } else {
+      L = layout_rect(X, Y, i0, i1, j0, j1, es);
+      if (L.Trows >= INT32_MAX) return TLR_STATUS_UNSUPPORTED;   // the epilogue holds T rows in 32 bits
+    }
     const uint64_t arena = ws + static_cast<uint64_t>(pc.fixed + (static_cast<int64_t>(ri) % narenas) * arena_bytes);
-    Builder B{X, Y, es, tf32, tb.bn, r.left, arena, &tb.maps, &tb.map_index, nullptr, &tb.segs, &tb.pieces, &tb.outs};
+    Builder B{X, Y, es, tf32, tb.bn, lft, arena, &tb.maps, &tb.map_index, nullptr, &tb.segs, &tb.pieces, &tb.outs};
     B.f16 = pc.pv.dtype == TLR_F16;
     B.dry = dry;
     B.views = &tb.views;
@@ -1421,7 +1925,8 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
       B.war_tgt = tb.counter_counts[B.war];
     }
     std::vector<Task> l1, l2, l3;
-    build_rect(B, L, l1, l2, l3);
+    if (r.triple) build_rect_triple(B, TL3, l1, l2, l3);
+    else build_rect(B, L, l1, l2, l3);
     if (B.status) return B.status;
     l2count[ri] = l2.size();
     sort_by_work(l1, tb.segs);
@@ -1430,10 +1935,14 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
     prep[ri].insert(prep[ri].end(), l2.begin(), l2.end());
     fin[ri] = l3;
     tb.layouts.push_back(L);
-    tb.rect_left.push_back(r.left ? 1 : 0);
+    tb.tlayouts.push_back(TL3);
+    tb.rect_left.push_back(lft ? 1 : 0);
+    tb.rect_triple.push_back(r.triple ? 1 : 0);
     tb.rect_arena.push_back(arena);
     info.runs += 1;
-    if (r.left) info.runs_left += 1; else info.runs_right += 1;
+    if (r.triple) info.runs_triple += 1;
+    else if (r.left) info.runs_left += 1;
+    else info.runs_right += 1;
     info.flops_stage1 += B.fl_s1;
     info.flops_stage2 += B.fl_s2;
     info.flops_stage3 += B.fl_s3;
@@ -1535,6 +2044,25 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
   tb.arena_bytes = arena_bytes;
   info.flops_executed = info.flops_stage1 + info.flops_stage2 + info.flops_stage3 + info.flops_dense_terms;
   info.tasks = static_cast<int64_t>(tb.all.size());
+  return TLR_STATUS_OK;
+}
+
+// Rectangles as the ABI reports them: tile ranges of C and the order used.
+std::vector<tlr_rect_t> abi_rects(const std::vector<Rect> &rects) {
+  std::vector<tlr_rect_t> out;
+  for (const Rect &r : rects) {
+    tlr_rect_t x;
+    x.i0 = r.i0; x.i1 = r.i1; x.j0 = r.j0; x.j1 = r.j1;
+    x.order = r.triple ? TLR_ORDER_TRIPLE : (r.left ? TLR_ORDER_LEFT : TLR_ORDER_RIGHT);
+    out.push_back(x);
+  }
+  return out;
+}
+
+tlr_status_t copy_rects(const std::vector<tlr_rect_t> &v, tlr_rect_t *rects, int32_t capacity, int32_t *count) {
+  if (!count || capacity < 0 || (capacity > 0 && !rects)) return TLR_STATUS_INVALID_ARG;
+  *count = static_cast<int32_t>(v.size());
+  for (int32_t q = 0; q < capacity && q < *count; ++q) rects[q] = v[q];
   return TLR_STATUS_OK;
 }
 
@@ -1685,8 +2213,73 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
     for (size_t c = 0; c < nc; ++c)
       if (cnt[c] != tb.counter_counts[c]) return "counter counts differ";
   }
+  // per-triple rectangles: every terminal-buffer element a final product reads
+  // was written exactly once (by the launches before it)
+  for (size_t ri = 0; ri < tb.layouts.size(); ++ri) {
+    if (!tb.rect_triple[ri]) continue;
+    const TripleLayout &L = tb.tlayouts[ri];
+    const uint64_t bufs[2] = {tb.rect_arena[ri] + static_cast<uint64_t>(L.TRoff),
+                              tb.rect_arena[ri] + static_cast<uint64_t>(L.TLoff)};
+    const int64_t nrows[2] = {L.TRrows, L.TLrows};
+    const int64_t rowb = L.ldT * es;
+    std::vector<std::vector<std::pair<int32_t, int32_t>>> wr[2];
+    for (int q = 0; q < 2; ++q) wr[q].assign(static_cast<size_t>(nrows[q]), {});
+    std::vector<size_t> finals;
+    for (size_t ti = 0; ti < tb.all.size(); ++ti) {
+      if (tb.task_rect[ti] != static_cast<int>(ri)) continue;
+      const Task &t = tb.all[ti];
+      const Out &o = tb.outs[t.out];
+      if (o.kind == kOutC) { finals.push_back(ti); continue; }
+      const uint64_t base = reinterpret_cast<uint64_t>(o.ptr);
+      const int q = base == bufs[0] ? 0 : (base == bufs[1] ? 1 : -1);
+      if (q < 0) continue;
+      auto add = [&](int64_t r0, int64_t n) {
+        for (int64_t r = r0; r < r0 + n; ++r)
+          if (r >= 0 && r < nrows[q]) wr[q][r].push_back({static_cast<int32_t>(t.col0), static_cast<int32_t>(t.col0 + t.cols)});
+      };
+      if (t.npiece == 0) add(t.row0, t.rows);
+      for (int pq = 0; pq < t.npiece; ++pq) add(tb.pieces[t.piece0 + pq].dst0, tb.pieces[t.piece0 + pq].len);
+    }
+    for (int q = 0; q < 2; ++q)
+      for (auto &v : wr[q]) {
+        std::sort(v.begin(), v.end());
+        for (size_t x = 1; x < v.size(); ++x)
+          if (v[x].first < v[x - 1].second) { snprintf(buf, sizeof buf, "rect %zu: terminal element written twice", ri); return buf; }
+      }
+    auto covered = [&](int q, int64_t r, int64_t c0, int64_t c1) {
+      if (r < 0 || r >= nrows[q]) return false;
+      int64_t c = c0;
+      for (auto &iv : wr[q][r]) {
+        if (iv.first > c) break;
+        if (iv.second > c) c = iv.second;
+        if (c >= c1) return true;
+      }
+      return c >= c1;
+    };
+    for (size_t ti : finals) {
+      const Task &t = tb.all[ti];
+      for (int sq = 0; sq < t.nseg; ++sq) {
+        const Seg &g = tb.segs[t.seg0 + sq];
+        for (int side = 0; side < 2; ++side) {
+          const View &v = tb.views[side == 0 ? g.a_map : g.b_map].first;
+          for (int q = 0; q < 2; ++q) {
+            if (v.addr < bufs[q] || v.addr >= bufs[q] + static_cast<uint64_t>(nrows[q] * rowb)) continue;
+            const int64_t r0 = static_cast<int64_t>(v.addr - bufs[q]) / rowb;
+            const int64_t c0 = side == 0 ? g.a_x : g.b_x;
+            const int64_t c1 = c0 + (side == 0 ? t.rows : t.cols);
+            for (int64_t r = r0; r < r0 + g.k_len; ++r)
+              if (!covered(q, r, c0, c1)) {
+                snprintf(buf, sizeof buf, "rect %zu: final product reads terminal row %lld not written", ri, (long long)r);
+                return buf;
+              }
+          }
+        }
+      }
+    }
+  }
   // T coverage per rectangle
   for (size_t ri = 0; ri < tb.layouts.size(); ++ri) {
+    if (tb.rect_triple[ri]) continue;
     const RectLayout &L = tb.layouts[ri];
     const bool left = tb.rect_left[ri] != 0;
     const LOp &X = left ? pc.XL : pc.XR;
@@ -1767,24 +2360,57 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
-void *g_static_ptr[kMaxDevices] = {};
+struct StaticSlot {
+  unsigned long long ctx_id = 0;   // context the address was looked up in (0: never)
+  void *ptr = nullptr;
+};
+StaticSlot g_static_slot[kMaxDevices];
 
-// Device address of g_static_scratch on the current device, looked up once per
-// device. The host never takes the symbol itself as a device address.
+// Unique id of the calling thread's current context (cuCtxGetId ids are never
+// reused within a process, unlike context handles); 0 when it cannot be read.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static bool looked = false;
+  if (!looked) {
+    void *a = nullptr, *b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 4000, cudaEnableDefault, &qa) == cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(a);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+        qb == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(b);
+    looked = true;
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_cur || !get_id || get_cur(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_static_scratch on the current device. The lookup runs
+// once per device and context: the first call on a device does it, and a call
+// after that device's context was destroyed and re-created (cudaDeviceReset)
+// does it again, so a stale address is never used. The host never takes the
+// symbol itself as a device address.
 tlr_status_t static_scratch_ptr(void **out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return TLR_STATUS_CUDA_ERROR; }
   if (dev < 0 || dev >= kMaxDevices) return TLR_STATUS_UNSUPPORTED;
+  const unsigned long long ctx = current_context_id();   // 0 until this thread has a current context
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_ptr[dev]) {
+  StaticSlot &sl = g_static_slot[dev];
+  if (!sl.ptr || ctx == 0 || sl.ctx_id != ctx) {
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) {
       cudaGetLastError();
       return TLR_STATUS_CUDA_ERROR;
     }
-    g_static_ptr[dev] = ptr;
+    sl.ptr = ptr;
+    sl.ctx_id = current_context_id();   // the lookup made the device's context current
   }
-  *out = g_static_ptr[dev];
+  *out = sl.ptr;
   return TLR_STATUS_OK;
 }
 
@@ -1815,6 +2441,7 @@ tlr_status_t tlr_create(tlr_handle_t *handle, void *stream) {
   tlr_handle_s *h = new (std::nothrow) tlr_handle_s();
   if (!h) return TLR_STATUS_INVALID_ARG;
   h->stream = static_cast<cudaStream_t>(stream);
+  if (cudaGetDevice(&h->device) != cudaSuccess) { cudaGetLastError(); delete h; return TLR_STATUS_NOT_INITIALIZED; }
   if (cudaMalloc(&h->d_err, 256) != cudaSuccess || cudaMemset(h->d_err, 0, 256) != cudaSuccess) {
     delete h;
     return TLR_STATUS_CUDA_ERROR;
@@ -1948,7 +2575,8 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
                              tlr_order_t order, tlr_plan_t *plan_out) {
   if (!h || !plan_out) return TLR_STATUS_INVALID_ARG;
   *plan_out = nullptr;
-  if (order != TLR_ORDER_AUTO && order != TLR_ORDER_RIGHT && order != TLR_ORDER_LEFT) return TLR_STATUS_INVALID_ARG;
+  if (order != TLR_ORDER_AUTO && order != TLR_ORDER_RIGHT && order != TLR_ORDER_LEFT && order != TLR_ORDER_TRIPLE)
+    return TLR_STATUS_INVALID_ARG;
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TLR_STATUS_ALIGNMENT;
   const uint64_t ws = reinterpret_cast<uint64_t>(workspace);
   PlanCore pc;
@@ -1959,6 +2587,7 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
   const bool tf32 = pc.pv.dtype == TLR_F32;
   std::vector<Rect> rects;
   int narenas = 1;
+  if (order == TLR_ORDER_TRIPLE && !can_triple(pc)) return TLR_STATUS_UNSUPPORTED;
   if (!plan_split(pc, static_cast<int64_t>(workspace_bytes), order, es, rects, narenas))
     return TLR_STATUS_WORKSPACE_TOO_SMALL;
   const int64_t need = pc.fixed + narenas * align_up(max_rect_bytes(pc, rects, es), 256);
@@ -1984,6 +2613,7 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
   st = build_tables(pc, rects, narenas, ws, false, tb);
   if (st) { delete p; return st; }
   p->launches = tb.launches;
+  p->rects = abi_rects(rects);
   p->info = tb.info;
   tlr_plan_info_t &info = p->info;
   info.workspace_bytes = static_cast<size_t>(need);
@@ -2057,6 +2687,7 @@ tlr_status_t tlr_debug_check_plan(tlr_op_t opA, tlr_op_t opB, const tlr_operand_
   const int es = elem_size(pc.pv.dtype);
   std::vector<Rect> rects;
   int narenas = 1;
+  if (order == TLR_ORDER_TRIPLE && !can_triple(pc)) return TLR_STATUS_UNSUPPORTED;
   if (!plan_split(pc, static_cast<int64_t>(workspace_bytes), order, es, rects, narenas))
     return TLR_STATUS_WORKSPACE_TOO_SMALL;
   Tables tb;
@@ -2082,6 +2713,27 @@ tlr_status_t tlr_plan_info(tlr_plan_t plan, tlr_plan_info_t *info) {
   if (!plan || !info) return TLR_STATUS_INVALID_ARG;
   *info = plan->info;
   return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_plan_rects(tlr_plan_t plan, tlr_rect_t *rects, int32_t capacity, int32_t *count) {
+  if (!plan) return TLR_STATUS_INVALID_ARG;
+  return copy_rects(plan->rects, rects, capacity, count);
+}
+
+tlr_status_t tlr_debug_plan_rects(tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A, const tlr_operand_t *B,
+                                  size_t workspace_bytes, tlr_order_t order, tlr_rect_t *rects, int32_t capacity,
+                                  int32_t *count) {
+  if (order != TLR_ORDER_AUTO && order != TLR_ORDER_RIGHT && order != TLR_ORDER_LEFT && order != TLR_ORDER_TRIPLE)
+    return TLR_STATUS_INVALID_ARG;
+  PlanCore pc;
+  tlr_status_t st = core_init(pc, opA, opB, A, B, false, 0x100000000000ull);
+  if (st) return st;
+  std::vector<Rect> rs;
+  int narenas = 1;
+  if (order == TLR_ORDER_TRIPLE && !can_triple(pc)) return TLR_STATUS_UNSUPPORTED;
+  if (!plan_split(pc, static_cast<int64_t>(workspace_bytes), order, elem_size(pc.pv.dtype), rs, narenas))
+    return TLR_STATUS_WORKSPACE_TOO_SMALL;
+  return copy_rects(abi_rects(rs), rects, capacity, count);
 }
 
 // Tensor maps of C for the epilogue's bulk stores (see Params::cmap). A map
@@ -2191,6 +2843,12 @@ tlr_status_t tlr_gemm_static_scratch(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB,
                                      int64_t ldc) {
   if (!h || !C) return TLR_STATUS_INVALID_ARG;
   if (!aligned16(C) || ldc % 4) return TLR_STATUS_ALIGNMENT;
+  {
+    // the scratch address is per device: the current one must be the handle's
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return TLR_STATUS_CUDA_ERROR; }
+    if (dev != h->device) return TLR_STATUS_INVALID_ARG;
+  }
   void *scratch = nullptr;
   tlr_status_t st = static_scratch_ptr(&scratch);
   if (st) return st;

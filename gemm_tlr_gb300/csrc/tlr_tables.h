@@ -31,7 +31,7 @@ constexpr int kEpiGroups = TLR_EPI_GROUPS;   // epilogue warp groups; each store
 constexpr int kEpiThreads = 128 * kEpiGroups;
 constexpr int kThreads = 96 + kEpiThreads;   // warp 0 TMA, warp 1 MMA, warp 2 descriptors, then the epilogue
 constexpr int kTmemCols = 512;      // two accumulators of up to 256 fp32 columns
-constexpr int kMaxSegs = 4;         // K segments per task
+constexpr int kMaxSegs = 8;         // K segments per task
 constexpr int kRing = 8;            // task descriptors staged ahead in shared memory
 constexpr int kTicketBatch = 4;     // consecutive tickets a CTA (or CTA pair) claims at once
 constexpr int kSlotBytes = 1536;    // one staged task: header, segments, per-row destinations

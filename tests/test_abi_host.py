@@ -232,3 +232,144 @@ def test_every_schedule_variant_validates(g, monkeypatch, env, cfg, scale):
     st, msg, info = g.tlr_debug_check_plan(opA, 0, A, B, budget)
     assert st == 0, msg
     assert info["launches"] >= 1
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_plan_flops_recounted_rectangle_by_rectangle(g, cfg):
+    """The planner's executed-FLOP figure equals an independent count from the
+    ranks (gemm_tlr_gb300.flops) over the rectangles it reports, each with its
+    own association order ("Tile-Low-Rank GEMM: Designing Storage Around the
+    Contraction", section "Association order and workspace": the cheaper order
+    per rectangle). The large product's 2 GiB plan mixes both orders."""
+    from gemm_tlr_gb300 import flops as fl
+    from gemm_tlr_gb300.device import fake_descriptor
+    p = ti.problem(cfg)
+    A, ka = fake_descriptor(p.A, 1 << 40)
+    B, kb = fake_descriptor(p.B, 1 << 42)
+    opA, opB = int(p.opA == "T"), int(p.opB == "T")
+    budget = p.budget or (1 << 40)
+    st, msg, info = g.tlr_debug_check_plan(opA, opB, A, B, budget)
+    assert st == 0, msg
+    rects = g.tlr_debug_plan_rects(opA, opB, A, B, budget)
+    assert len(rects) == info["runs"]
+    assert sum(r[4] == "L" for r in rects) == info["runs_left"]
+    counted = fl.executed_flops_rects(p, rects)
+    assert counted["total"] == pytest.approx(info["flops_executed"], rel=1e-12)
+    for k, name in (("stage1", "flops_stage1"), ("stage2", "flops_stage2"), ("stage3", "flops_stage3"),
+                    ("dense", "flops_dense_terms")):
+        assert counted[k] == pytest.approx(info[name], rel=1e-12, abs=1.0)
+    if cfg == 5:
+        # both orders over all of C give the right-order count of the survey table,
+        # 4.167e12; the mixed plan is cheaper, never dearer
+        assert {r[4] for r in rects} == {"R", "L"}
+        assert fl.executed_flops(p, "R")["total"] == pytest.approx(4.167e12, rel=1e-3)
+        assert fl.executed_flops(p, "L")["total"] == pytest.approx(4.167e12, rel=1e-3)
+        assert counted["total"] < fl.executed_flops(p, "R")["total"]
+        forced = g.tlr_debug_plan_rects(opA, opB, A, B, budget, g.TLR_ORDER_RIGHT)
+        assert {r[4] for r in forced} == {"R"}
+        assert fl.executed_flops_rects(p, forced)["total"] == pytest.approx(fl.executed_flops(p, "R")["total"],
+                                                                            rel=1e-12)
+
+
+def _fake(p):
+    from gemm_tlr_gb300.device import fake_descriptor
+    A, ka = fake_descriptor(p.A, 1 << 40)
+    B, kb = fake_descriptor(p.B, 1 << 42)
+    return A, B, (ka, kb), int(p.opA == "T"), int(p.opB == "T")
+
+
+TRIPLE_CASES = [("cfg5/8", lambda: ti.problem(5, scale_down=8), None),
+                ("cfg5", lambda: ti.problem(5), None),
+                ("asym", lambda: ti.asym_grid(2048, 256), None),
+                ("asym_split", lambda: ti.asym_grid(4096, 256), 12 << 20),
+                ("skewed", lambda: ti.skewed_grid(4096, "bf16"), None),
+                ("f16_boundary_TN", lambda: ti.Problem(
+                    "b", ti.make_tlr(np.random.default_rng(5), 456, 128, ti.rank_uniform(0, 40), "f16"),
+                    ti.make_tlr(np.random.default_rng(6), 456, 128, ti.rank_uniform(0, 40), "f16"),
+                    "T", "N", 1.0, 0.5, None, 456, 456, "f16"), None)]
+
+
+@pytest.mark.parametrize("name,make,budget", TRIPLE_CASES, ids=[c[0] for c in TRIPLE_CASES])
+def test_per_triple_plans_validate_and_count(g, name, make, budget):
+    """The per-triple order ("TLR Matrix Multiplication", section "The O_A O_B
+    terms": each (i, k, j) takes the side of min(r_ik, r_kj)) builds tables the
+    host validator accepts (every view inside its buffer, C covered once, every
+    terminal element a final product reads written exactly once), executes the
+    FLOPs an independent count from the ranks gives, and never more than the
+    per-rectangle plans."""
+    from gemm_tlr_gb300 import flops as fl
+    p = make()
+    A, B, keep, opA, opB = _fake(p)
+    budget = budget or p.budget or (1 << 40)
+    st, msg, info = g.tlr_debug_check_plan(opA, opB, A, B, budget, g.TLR_ORDER_TRIPLE)
+    assert st == 0, msg
+    assert info["runs_triple"] == info["runs"] >= 1
+    rects = g.tlr_debug_plan_rects(opA, opB, A, B, budget, g.TLR_ORDER_TRIPLE)
+    assert {r[4] for r in rects} == {"P"}
+    counted = fl.executed_flops_rects(p, rects)
+    assert counted["total"] == pytest.approx(info["flops_executed"], rel=1e-12)
+    assert counted["stage3"] == pytest.approx(info["flops_stage3"], rel=1e-12)
+    st2, _, auto = g.tlr_debug_check_plan(opA, opB, A, B, budget, g.TLR_ORDER_AUTO)
+    assert st2 == 0 and info["flops_executed"] <= auto["flops_executed"]
+    if name == "cfg5":
+        # the large product: final products 3.27e12 -> 1.59e12 FLOP
+        assert info["flops_stage3"] == pytest.approx(1.595e12, rel=1e-3)
+        assert auto["flops_stage3"] == pytest.approx(3.265e12, rel=1e-3)
+
+
+def test_four_orders_differ_on_the_asymmetric_workload(g):
+    """Right, left, per-rectangle (a budget that splits C) and per-triple plans
+    of the unlike-rank workload execute four different FLOP counts, each equal
+    to the independent count over the plan's rectangles."""
+    from gemm_tlr_gb300 import flops as fl
+    p = ti.asym_grid(4096, 256)
+    A, B, keep, opA, opB = _fake(p)
+    seen = {}
+    for budget in (1 << 40, 24 << 20, 12 << 20):
+        for order in (g.TLR_ORDER_RIGHT, g.TLR_ORDER_LEFT, g.TLR_ORDER_AUTO, g.TLR_ORDER_TRIPLE):
+            st, msg, info = g.tlr_debug_check_plan(opA, opB, A, B, budget, order)
+            if st == 3:
+                continue
+            assert st == 0, msg
+            rects = g.tlr_debug_plan_rects(opA, opB, A, B, budget, order)
+            assert fl.executed_flops_rects(p, rects)["total"] == pytest.approx(info["flops_executed"], rel=1e-12)
+            kinds = "".join(sorted({r[4] for r in rects}))
+            seen.setdefault(kinds, set()).add(round(info["flops_executed"]))
+    assert {"R", "L", "LR", "P"} <= set(seen), seen
+    per = {k: min(v) for k, v in seen.items()}
+    assert len(set(per.values())) == len(per)           # four different counts
+    assert per["P"] < min(per["R"], per["L"], per["LR"])
+
+
+def test_per_triple_order_needs_two_16_bit_tlr_operands(g):
+    rng = np.random.default_rng(7)
+    F = ti.make_tlr(rng, 256, 64, ti.rank_fixed(8), "f32")
+    from gemm_tlr_gb300.device import fake_descriptor
+    Fd, kf = fake_descriptor(F, 1 << 40)
+    assert g.tlr_debug_check_plan(0, 0, Fd, Fd, 1 << 30, g.TLR_ORDER_TRIPLE)[0] == 4
+    X = ti.make_tlr(rng, 256, 64, ti.rank_fixed(8), "bf16")
+    D = ti.make_dense(rng, 256, 128, "bf16")
+    Xd, kx = fake_descriptor(X, 1 << 40)
+    Dd, kd = fake_descriptor(D, 1 << 42)
+    assert g.tlr_debug_check_plan(0, 0, Xd, Dd, 1 << 30, g.TLR_ORDER_TRIPLE)[0] == 4
+
+
+def test_per_triple_segment_limit_on_alternating_ranks(g):
+    """Ranks that make the cheaper side alternate along k: every output tile's
+    K-loop still fits the kernel's segment limit (the validator checks it), the
+    plan stays correct in coverage, and its FLOPs are at least the rule's."""
+    from gemm_tlr_gb300 import flops as fl
+    n, b = 2048, 128
+    nt = n // b
+    ra = np.fromfunction(lambda i, k: np.where((k % 2) == 0, 8, 40), (nt, nt)).astype(np.int64)
+    rb = np.fromfunction(lambda k, j: np.where((k % 2) == 0, 40, 8), (nt, nt)).astype(np.int64)
+    rng = np.random.default_rng(8)
+    A = ti.make_tlr(rng, n, b, None, "bf16", ranks=ra)
+    B = ti.make_tlr(rng, n, b, None, "bf16", ranks=rb)
+    p = ti.Problem("alternating", A, B, "N", "N", 1.0, 0.0, None, n, n, "bf16")
+    Ad, Bd, keep, opA, opB = _fake(p)
+    st, msg, info = g.tlr_debug_check_plan(opA, opB, Ad, Bd, 1 << 40, g.TLR_ORDER_TRIPLE)
+    assert st == 0, msg
+    rule = fl.executed_flops_triple(p)["total"]
+    assert info["flops_executed"] >= rule
+    assert info["flops_executed"] < fl.executed_flops(p, "R")["total"]

@@ -43,7 +43,7 @@ __all__ = [
     "var_rank_grid", "bf16_round", "f16_round", "bf16_bits", "TLRMatrix", "DenseMatrix", "Problem",
     "make_tlr", "make_dense", "problem", "CONFIG_NAMES", "tile_dims",
     "rank_fixed", "rank_uniform", "rank_inverse_distance", "rank_exp_decay", "rank_skewed",
-    "skewed_grid",
+    "skewed_grid", "asym_grid", "rank_split_rows",
 ]
 
 
@@ -357,6 +357,33 @@ def skewed_grid(n: int, dtype: str, *, seed: int = 0, keep_tiles: bool = False, 
     A = make_tlr(rng, n, b, rule, dtype, keep_tiles=keep_tiles)
     Bm = make_tlr(rng, n, b, rule, dtype, keep_tiles=keep_tiles)
     return Problem(f"skewed_8x8_{dtype}_N{n}", A, Bm, "N", "N", 1.0, 0.0, None, n, n, dtype, budget=budget)
+
+
+def rank_split_rows(hi: int, scale: float, length: float, lo: int) -> Callable:
+    """Tile rows in the upper half at rank `hi` everywhere; the lower half
+    r_ik = clamp(round(scale exp(-|i-k| / length)), lo, hi)."""
+    def f(rng, nt_r, nt_c, rd, cd):
+        r = np.zeros((nt_r, nt_c), dtype=np.int64)
+        for i in range(nt_r):
+            for k in range(nt_c):
+                r[i, k] = hi if 2 * i < nt_r else min(hi, max(lo, _round_half_up(scale * math.exp(-abs(i - k) / length))))
+        return r
+    return f
+
+
+def asym_grid(n: int, b: int, dtype: str = "bf16", *, seed: int = 0, budget: Optional[int] = None) -> Problem:
+    """TLR x TLR with unlike rank maps, so that the right, left, per-rectangle and
+    per-triple orders all execute different FLOP counts: A's upper tile rows all
+    have rank b/4 and its lower ones decay away from the diagonal,
+    clamp(round(b/8 exp(-|i-k|/2)), 2, b/4); B's ranks are uniform on [b/32, b/8]
+    per tile. Factors ~N(0,1)/sqrt(b), dense diagonal tiles ~N(0,1), alpha = 1,
+    beta = 0 (a test and measurement workload, not one of the five)."""
+    if n % b:
+        raise ValueError("n must be a multiple of b")
+    rng = np.random.default_rng(seed)
+    A = make_tlr(rng, n, b, rank_split_rows(b // 4, b / 8, 2.0, 2), dtype)
+    Bm = make_tlr(rng, n, b, rank_uniform(max(1, b // 32), b // 8), dtype)
+    return Problem(f"asym_{dtype}_N{n}_b{b}", A, Bm, "N", "N", 1.0, 0.0, None, n, n, dtype, budget=budget)
 
 
 def problem(cfg, *, seed: int = 0, keep_tiles: bool = False, scale_down: int = 1,
