@@ -215,14 +215,50 @@ def cpu_baseline(p, flops_total, target_s=10.0, per_tile=None):
                       f"value_own_flops: the oracle's own 2 K FLOPs per sampled entry (K = {K})"}, dt, per_tile
 
 
+def default_plan_flops(p) -> float:
+    """Executed FLOPs of the default plan, counted from the ranks alone with the
+    default's rule (per-triple order when its final stage needs at most 90 % of
+    the cheaper single order's), so that both arms divide by the same count."""
+    from gemm_tlr_gb300 import flops as fl
+    if p.A.kind == "tlr" and p.B.kind == "tlr" and p.dtype != "f32":
+        tri = fl.executed_flops_triple(p)
+        single = min(fl.executed_flops(p, "R")["stage3"], fl.executed_flops(p, "L")["stage3"])
+        if tri["stage3"] <= 0.9 * single:
+            return tri["total"]
+    return fl.executed_flops(p, "R")["total"]
+
+
+def time_other_plan(g, h, dp, order: str, steps: int, stream) -> dict:
+    """The same product under another plan (same buffers and workspace), timed
+    like the main measurement over `steps` products."""
+    import torch
+    plan = g.tlr_plan_create(h, dp.opA, dp.opB, dp.A.desc, dp.B.desc, dp.ws.data_ptr(), dp.ws_bytes, ORDERS[order])
+    try:
+        info = g.tlr_plan_info(plan)
+        for _ in range(3):
+            g.tlr_plan_execute(plan, dp.p.alpha, dp.p.beta, dp.C.data_ptr(), dp.ldc)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            g.tlr_plan_execute(plan, dp.p.alpha, dp.p.beta, dp.C.data_ptr(), dp.ldc)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        return {"order": order, "ms_per_step": ms, "flops_per_step": info["flops_executed"],
+                "executed_tflops": info["flops_executed"] / (ms * 1e-3) / 1e12, "runs": info["runs"],
+                "runs_left": info["runs_left"], "runs_triple": info["runs_triple"], "steps": steps}
+    finally:
+        g.tlr_plan_destroy(plan)
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     import tlr_inputs
-    from gemm_tlr_gb300 import flops as fl
     p = tlr_inputs.problem(5)
-    total = fl.executed_flops(p, "R")["total"]
+    total = default_plan_flops(p)
     # one sample size for every step, chosen so the whole run stays near two minutes
     per_step_s = min(4.0, max(0.1, 120.0 / max(1, args.steps + args.warmup)))
     _, _, per_tile = cpu_baseline(p, total, target_s=4 * per_step_s)
@@ -244,6 +280,8 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
     return 0
 
+
+ORDERS = {"auto": 0, "right": 1, "left": 2, "triple": 3, "per_rect": 4}   # tlr_order_t
 
 # Nominal dense tensor-core peaks of one GB300 (TFLOP/s): bf16/fp16 2250, tf32 1100.
 NOMINAL_TFLOPS = {"bf16": 2250.0, "f16": 2250.0, "f32": 1100.0}
@@ -408,7 +446,9 @@ def main():
                          "tiles and rank rule at order --n (smaller cases for profiling)")
     ap.add_argument("--n", type=int, default=65536, help="order of the skewed8x8 or var_rank workload")
     ap.add_argument("--dtype", default="f16", choices=["f16", "bf16", "f32"], help="element type of skewed8x8")
-    ap.add_argument("--order", default="auto", choices=["auto", "right", "left", "triple"],
+    ap.add_argument("--budget-gib", type=float, default=None,
+                    help="workspace budget in GiB for the skewed8x8 / var_rank workloads (profiling)")
+    ap.add_argument("--order", default="auto", choices=["auto", "right", "left", "triple", "per_rect"],
                     help="association order of the plan: per rectangle (auto), forced, or per tile triple")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -442,12 +482,14 @@ def main():
     else:
         p = tlr_inputs.skewed_grid(args.n, args.dtype)
         args.no_cpu_baseline = True
+    if args.budget_gib is not None and not main_workload:
+        p.budget = int(args.budget_gib * (1 << 30))
     # pinned host copies of the inputs (end-to-end timing) on the GPU's NUMA node
     with near_gpu(local) as numa:
         dp = DeviceProblem(p, pinned=True)
         C_host = torch.empty(p.m * p.n, dtype=torch.float32).pin_memory()
         C_host.zero_()
-    dp.make_plan(h, order={"auto": 0, "right": 1, "left": 2, "triple": 3}[args.order])
+    dp.make_plan(h, order=ORDERS[args.order])
     info = dp.info()
     order = ("per-triple" if info["runs_triple"] == info["runs"] else
              "L" if info["runs_left"] == info["runs"] else ("R" if info["runs_left"] == 0 else "mixed"))
@@ -510,15 +552,19 @@ def main():
     l2.record(stream)
     barrier()
     h2d_ms, d2h_ms = l0.elapsed_time(l1), l1.elapsed_time(l2)
-    e2e_steps = args.e2e_steps or max(3, math.ceil(1000.0 / max(1e-3, h2d_ms + d2h_ms + ms_step)))
+    # steps for about two seconds: the host link of this machine has slow phases
+    # (copies at a fifth of their usual rate for a second or more), which a long
+    # region averages and the per-step spread below shows
+    e2e_steps = args.e2e_steps or max(3, math.ceil(2000.0 / max(1e-3, h2d_ms + d2h_ms + ms_step)))
     e2e_steps = int(max_over_ranks(float(e2e_steps)))   # every rank runs the same number
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(e2e_steps):
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
+    marks[0].record(stream)
+    for q in range(e2e_steps):
         e2e_step()
-    f1.record(stream)
+        marks[q + 1].record(stream)
     barrier()
-    e2e_ms = max_over_ranks(f0.elapsed_time(f1)) / e2e_steps
+    per_step = sorted(marks[q].elapsed_time(marks[q + 1]) for q in range(e2e_steps))
+    e2e_ms = max_over_ranks(marks[0].elapsed_time(marks[-1])) / e2e_steps
     e2e_value = whole_job_tflops(world, flops_step, e2e_ms)
 
     peaks, peak_src = _peaks()
@@ -583,6 +629,7 @@ def main():
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "steps": e2e_steps,
+                "step_ms": {"min": per_step[0], "median": per_step[len(per_step) // 2], "max": per_step[-1]},
                 "link_gbs": {"h2d": h2d / (h2d_ms * 1e-3) / 1e9, "d2h": d2h / (d2h_ms * 1e-3) / 1e9},
                 "expected_ms": h2d_ms + ms_step + d2h_ms,
                 "host_buffers": (f"pinned, allocated on CPUs {numa.cpus[0]}-{numa.cpus[-1]} local to the GPU"
@@ -591,6 +638,12 @@ def main():
         "gpu_launches": int(sum(v[1] for v in kern.values())),
         "device_status": g.tlr_status_string(status),
     }
+    if main_workload and args.scale_down == 1 and args.order == "auto":
+        # the per-rectangle plan of the same product, which the default gives up here
+        other = time_other_plan(g, h, dp, "per_rect", max(20, args.steps // 5), stream)
+        other["executed_tflops_frac_of_burst"] = other["executed_tflops"] / peak_burst
+        other["note"] = "same buffers and workspace budget; more executed FLOPs, more time"
+        line["other_plans"] = {"per_rect": other}
     if main_workload and args.scale_down == 1 and world == 1 and not args.no_per_config:
         line["per_config"] = per_config_timings(h, stream, local, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

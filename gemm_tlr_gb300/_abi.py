@@ -18,7 +18,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "tlr_gemm.h")
 TLR_OP_N, TLR_OP_T = 0, 1
 TLR_F32, TLR_BF16, TLR_F16 = 0, 1, 2
 TLR_KIND_TLR, TLR_KIND_DENSE = 0, 1
-TLR_ORDER_AUTO, TLR_ORDER_RIGHT, TLR_ORDER_LEFT, TLR_ORDER_TRIPLE = 0, 1, 2, 3
+TLR_ORDER_AUTO, TLR_ORDER_RIGHT, TLR_ORDER_LEFT, TLR_ORDER_TRIPLE, TLR_ORDER_PER_RECT = 0, 1, 2, 3, 4
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "ALIGNMENT", 3: "WORKSPACE_TOO_SMALL", 4: "UNSUPPORTED",
           5: "CUDA_ERROR", 6: "TIMEOUT", 7: "NOT_INITIALIZED"}
 KIND_STAGE1, KIND_STAGE2, KIND_STAGE3, KIND_ROUND, KIND_SCALE = 0, 1, 2, 3, 4
@@ -69,6 +69,7 @@ class tlr_analysis_t(ctypes.Structure):
         ("T_right_rows", ctypes.c_int64), ("T_right_cols", ctypes.c_int64),
         ("T_left_rows", ctypes.c_int64), ("T_left_cols", ctypes.c_int64),
         ("coupling_products", ctypes.c_int64), ("distinct_shapes", ctypes.c_int64),
+        ("F_P", ctypes.c_double),
     ]
 
 
@@ -82,6 +83,8 @@ _SIGS = {
     "tlr_analyze": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _OP, _OP, ctypes.POINTER(tlr_analysis_t)]),
     "tlr_gemm_workspace_bytes": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _OP, _OP, ctypes.c_int,
                                                 ctypes.POINTER(ctypes.c_size_t)]),
+    "tlr_gemm_workspace_bytes_for_order": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _OP, _OP, ctypes.c_int,
+                                                          ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
     "tlr_plan_create": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _OP, _OP, _P, ctypes.c_size_t,
                                        ctypes.c_int, ctypes.POINTER(_P)]),
     "tlr_plan_info": (ctypes.c_int, [_P, ctypes.POINTER(tlr_plan_info_t)]),
@@ -177,6 +180,14 @@ def tlr_gemm_workspace_bytes(h: int, opA: int, opB: int, A: tlr_operand_t, B: tl
     n = ctypes.c_size_t()
     check(lib().tlr_gemm_workspace_bytes(_P(h), opA, opB, ctypes.byref(A), ctypes.byref(B), runs,
                                          ctypes.byref(n)), "tlr_gemm_workspace_bytes")
+    return n.value
+
+
+def tlr_gemm_workspace_bytes_for_order(h: int, opA: int, opB: int, A: tlr_operand_t, B: tlr_operand_t, runs: int,
+                                       order: int) -> int:
+    n = ctypes.c_size_t()
+    check(lib().tlr_gemm_workspace_bytes_for_order(_P(h), opA, opB, ctypes.byref(A), ctypes.byref(B), runs, order,
+                                                   ctypes.byref(n)), "tlr_gemm_workspace_bytes_for_order")
     return n.value
 
 

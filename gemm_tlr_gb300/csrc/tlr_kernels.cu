@@ -169,6 +169,18 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
       : "memory");
 }
 
+// Pair mode with cluster multicast: the box lands at the same offset in every
+// CTA of `mask`, and each destination's bytes complete on the mbarrier at the
+// offset of `bar_cluster` in the leader CTA of that destination's pair.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void *tmap, int32_t x, int32_t y,
+                                                    uint32_t bar_cluster, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar_cluster), "h"(mask)
+      : "memory");
+}
+
 // L2 policy for data written once and not read again in the launch (C): its
 // lines are the first candidates for eviction, ahead of operands still in use.
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -290,9 +302,9 @@ __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a, uint64_t b
   }
 }
 
-// Commit for a pair: the mbarrier at the same offset in both CTAs gets one arrival.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
-  const uint16_t mask = 0x3;
+// Commit for a pair: the mbarrier at the same offset in every CTA of `mask`
+// (both CTAs of the pair by default) gets one arrival.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask = 0x3) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
       "h"(mask)
@@ -583,11 +595,19 @@ static_assert(sizeof(Slot) <= kSlotBytes, "slot size");
 
 template <bool kTF32, int kPair>
 __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_constant__ Params p) {
-  static_assert(kPair == 1 || kPair == 2, "one CTA or a CTA pair per output tile");
+  static_assert(kPair == 1 || kPair == 2 || kPair == 4, "one CTA, a CTA pair, or two pairs per cluster");
   // kPair == 2: the tile is 256 rows; each CTA of the pair holds 128 rows of A and
   // half of the columns of B; the leader issues cta_group::2 MMAs into both TMEMs.
-  constexpr int kSt = kPair == 2 ? 6 : kStages;          // pipeline stages
-  constexpr int kStB = kSmemA + kMaxBN / kPair * 128;     // bytes per stage in this CTA
+  // kPair == 4: a cluster of two such pairs working on tiles that share their B
+  // operand (tickets 8g..8g+3 for the first pair, 8g+4..8g+7 for the second, slot
+  // by slot with equal B segments): the first pair loads B once and multicasts it
+  // into the second pair's shared memory, so the cluster reads 3/4 of the operand
+  // bytes two separate pairs would.
+  constexpr bool kCG2 = kPair >= 2;                       // cta_group::2 MMAs over a CTA pair
+  constexpr bool kQuad = kPair == 4;
+  constexpr int kPairCTAs = kCG2 ? 2 : 1;                 // CTAs per output tile
+  constexpr int kSt = kCG2 ? 6 : kStages;                 // pipeline stages
+  constexpr int kStB = kSmemA + kMaxBN / kPairCTAs * 128; // bytes per stage in this CTA
   static_assert(kSt * kStB == kStages * kStageBytes, "same shared-memory footprint");
   constexpr int kElt = kTF32 ? 4 : 2;
   constexpr int kCH = 128 / kElt;     // elements per 128-byte row: MN chunk and K block
@@ -616,17 +636,19 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bn = p.bn;
-  const uint32_t rank = kPair == 2 ? cluster_rank() : 0u;   // 0: leader of the pair
+  const uint32_t crank = kCG2 ? cluster_rank() : 0u;      // rank in the cluster
+  const uint32_t rank = crank & 1u;                        // rank in the pair; 0: leader of the pair
+  const uint32_t lead_rank = crank & ~1u;                  // cluster rank of this pair's leader
   const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSt; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), kQuad ? 2 : 1);   // quad: both pairs' MMAs release a stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4 * kEpiGroups * kPair);   // one arrival per epilogue warp of the pair
+      mbar_init(tempty_bar(a), 4 * kEpiGroups * kPairCTAs);   // one arrival per epilogue warp of the pair
     }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(sfull_bar(r), 1);
@@ -638,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    if constexpr (kPair == 2) {
+    if constexpr (kCG2) {
       // one warp of each CTA of the pair allocates collectively
       asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                        smem_u32(tmem_holder)),
@@ -655,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (kPair == 2) cluster_sync_all();   // the peer's barriers exist before anyone signals them
+  if constexpr (kCG2) cluster_sync_all();   // the peers' barriers exist before anyone signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const char *maps = reinterpret_cast<const char *>(p.maps);
@@ -683,6 +705,11 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       if (lane == 0) {
         if constexpr (kPair == 1) {
           t0 = atomicAdd(p.ticket, cnt);
+        } else if constexpr (kQuad) {
+          // whole groups of 2 kBatch tickets per cluster in turn; the planner pads
+          // the launch to whole groups
+          const unsigned int units = gridDim.x / 4, unit = blockIdx.x / 4;
+          t0 = ((unit + b * units) * 2 + (crank >> 1)) * kBatch;
         } else {
           const unsigned int units = gridDim.x / 2, unit = blockIdx.x / 2;
           const unsigned int rounds = ntasks / (kBatch * units);
@@ -794,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
           // Box walk of each operand: MN-major boxes are kCH wide along MN (x) and
           // step K along y; K-major boxes are 64 rows along MN (y) and step K along x.
           const int32_t am0 = static_cast<int32_t>(rank) * kBM;   // this CTA's rows of A
-          const int bnc = bn / kPair;                             // this CTA's columns of B
+          const int bnc = bn / kPairCTAs;                         // this CTA's columns of B
           const int32_t bn0 = static_cast<int32_t>(rank) * bnc;
           const bool amn = (sg.flags & kSegAMN) != 0, bmn = (sg.flags & kSegBMN) != 0;
           int32_t ax = amn ? sg.a_x + am0 : sg.a_x, ay = amn ? sg.a_y : sg.a_y + am0;
@@ -809,17 +836,22 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
             const uint32_t fb = full_bar(stage);
             // one CTA: its own barrier; a pair: both CTAs' copies complete on the leader's
             // barrier, which the leader arms with the bytes of both
-            if (leader) mbar_expect_tx(fb, kPair * kSmemA + bn * 128);
-            const uint32_t fb_tma = kPair == 2 ? map_to_rank(fb, 0) : fb;
+            if (leader) mbar_expect_tx(fb, kPairCTAs * kSmemA + bn * 128);
+            const uint32_t fb_tma = kCG2 ? map_to_rank(fb, lead_rank) : fb;
             const uint32_t sa = base + stage * kStB;
             const uint32_t sb = sa + kSmemA;
             for (int c = 0; c < nba; ++c) {
-              if constexpr (kPair == 2) tma_load_2d_pair(sa + c * sta, ma, ax + c * adx, ay + c * ady, fb_tma);
+              if constexpr (kCG2) tma_load_2d_pair(sa + c * sta, ma, ax + c * adx, ay + c * ady, fb_tma);
               else tma_load_2d(sa + c * sta, ma, ax + c * adx, ay + c * ady, fb_tma);
             }
-            for (int c = 0; c < nbb; ++c) {
-              if constexpr (kPair == 2) tma_load_2d_pair(sb + c * stb, mb, bx + c * bdx, by + c * bdy, fb_tma);
-              else tma_load_2d(sb + c * stb, mb, bx + c * bdx, by + c * bdy, fb_tma);
+            if (!kQuad || crank < 2) {   // quad: the first pair's CTAs load B for both pairs
+              for (int c = 0; c < nbb; ++c) {
+                if constexpr (kQuad)
+                  tma_load_2d_pair_mc(sb + c * stb, mb, bx + c * bdx, by + c * bdy, fb_tma,
+                                      static_cast<uint16_t>((1u << crank) | (1u << (crank + 2))));
+                else if constexpr (kCG2) tma_load_2d_pair(sb + c * stb, mb, bx + c * bdx, by + c * bdy, fb_tma);
+                else tma_load_2d(sb + c * stb, mb, bx + c * bdx, by + c * bdy, fb_tma);
+              }
             }
             ax += akx; ay += aky; bx += bkx; by += bky;
             issued_mask |= 1u << stage;
@@ -850,18 +882,18 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
         const Slot &sl = ring[r];
         const int nseg = sl.task.nseg;
         if (nseg < 0) break;
-        if (kPair == 2 && !leader) {   // the peer's MMA warp only walks the ring
+        if (kCG2 && !leader) {   // the peer's MMA warp only walks the ring
           mbar_arrive(sempty_bar(r));
           continue;
         }
-        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p, 2, kPair == 2)) break;
+        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p, 2, kCG2)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kMaxBN);
         uint32_t accumulate = 0;
         for (int s = 0; ok && s < nseg; ++s) {
           const Seg sg = sl.segs[s];
           const bool a_mn = sg.flags & kSegAMN, b_mn = sg.flags & kSegBMN;
-          const uint32_t id = idesc(kTF32, p.f16 != 0, a_mn, b_mn, static_cast<uint32_t>(bn), kBM * kPair);
+          const uint32_t id = idesc(kTF32, p.f16 != 0, a_mn, b_mn, static_cast<uint32_t>(bn), kBM * kPairCTAs);
           const int nkb = (sg.k_len + kBK - 1) / kBK;
           // Descriptors of stage 0; a stage is kStB bytes further, an MMA step 32 bytes
           // (K-major: the next K slice of each 128-byte swizzled row) or kUK rows of
@@ -880,20 +912,21 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
             if (kleft >= kBK) {
 #pragma unroll
               for (int k = 0; k < kBK / kUK; ++k) {
-                if constexpr (kPair == 2) mma_pair<kTF32>(d_tmem, ad + k * da, bd + k * db, id, accumulate);
+                if constexpr (kCG2) mma_pair<kTF32>(d_tmem, ad + k * da, bd + k * db, id, accumulate);
                 else mma<kTF32>(d_tmem, ad + k * da, bd + k * db, id, accumulate);
                 accumulate = 1;
               }
             } else {
               const int nmma = (kleft + kUK - 1) / kUK;
               for (int k = 0; k < nmma; ++k) {
-                if constexpr (kPair == 2) mma_pair<kTF32>(d_tmem, ad + k * da, bd + k * db, id, accumulate);
+                if constexpr (kCG2) mma_pair<kTF32>(d_tmem, ad + k * da, bd + k * db, id, accumulate);
                 else mma<kTF32>(d_tmem, ad + k * da, bd + k * db, id, accumulate);
                 accumulate = 1;
               }
             }
-            // frees the stage (in both CTAs of a pair) once these MMAs have read it
-            if constexpr (kPair == 2) mma_commit_pair(empty_bar(stage));
+            // frees the stage (in both CTAs of a pair, in all four of a quad) once these MMAs have read it
+            if constexpr (kQuad) mma_commit_pair(empty_bar(stage), 0xF);
+            else if constexpr (kCG2) mma_commit_pair(empty_bar(stage));
             else mma_commit(empty_bar(stage));
             if (++stage == kSt) { stage = 0; phase ^= 1u; }
           }
@@ -901,17 +934,17 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
         mbar_arrive(sempty_bar(r));
         if (!ok) break;
         if (accumulate) {
-          if constexpr (kPair == 2) mma_commit_pair(tfull_bar(acc));
+          if constexpr (kCG2) mma_commit_pair(tfull_bar(acc), static_cast<uint16_t>(0x3u << lead_rank));
           else mma_commit(tfull_bar(acc));
         } else {
           mbar_arrive(tfull_bar(acc));
-          if constexpr (kPair == 2) mbar_arrive_remote(map_to_rank(tfull_bar(acc), 1));
+          if constexpr (kCG2) mbar_arrive_remote(map_to_rank(tfull_bar(acc), lead_rank + 1));
         }
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
       // All MMAs issued by this thread complete before TMEM is released.
       if (leader) {
-        if constexpr (kPair == 2) mma_commit_pair_local(drain_bar);
+        if constexpr (kCG2) mma_commit_pair_local(drain_bar);
         else mma_commit(drain_bar);
         wait_drain(drain_bar, 0, 200000000ull);
       }
@@ -946,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       pend_writes = false;
     };
     auto ready = [&](uint32_t bar, uint32_t parity) {
-      const uint32_t ok = lane == 0 ? (kPair == 2 ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) : 0u;
+      const uint32_t ok = lane == 0 ? (kCG2 ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) : 0u;
       return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
     for (int n = 0;; ++n) {
@@ -966,7 +999,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(sempty_bar(r));
       if (!ready(tfull_bar(acc), acc_phase)) flush();
-      if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p, 4, kPair == 2)) break;
+      if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p, 4, kCG2)) break;
       tc_fence_after();
       if (pend != signal || pend_n >= kSignalBatch) flush();   // the earlier stores have had time to drain
       const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -1003,7 +1036,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       __syncwarp();
       if (lane == 0) {
         if (leader) mbar_arrive(tempty_bar(acc));
-        else mbar_arrive_remote(map_to_rank(tempty_bar(acc), 0));
+        else mbar_arrive_remote(map_to_rank(tempty_bar(acc), lead_rank));
       }
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       if (signal >= 0) {
@@ -1019,10 +1052,10 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
 
   tc_fence_before();
   __syncthreads();
-  if constexpr (kPair == 2) cluster_sync_all();   // neither CTA leaves while the other may signal it
+  if constexpr (kCG2) cluster_sync_all();   // no CTA leaves while another may signal it
   tc_fence_after();
   if (warp == 1) {
-    if constexpr (kPair == 2)
+    if constexpr (kCG2)
       asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                    : "memory");
     else
@@ -1135,34 +1168,35 @@ cudaError_t launch_one(const Params &p, int grid, cudaStream_t stream) {
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = kPair;   // 2: one CTA pair; 4: two pairs
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, &tlr_task_gemm<kTF32, 2>, p);
+    return cudaLaunchKernelEx(&cfg, &tlr_task_gemm<kTF32, kPair>, p);
   }
 }
 
-// Pairs that can be resident at once (all must be, since tasks are assigned to pairs in turn).
-template <bool kTF32>
-int resident_pairs() {
+// Clusters (of kPair CTAs) that can be resident at once (all must be, since
+// tasks are assigned to clusters in turn).
+template <bool kTF32, int kPair>
+int resident_clusters() {
   static int n = -1;
   if (n < 0) {
-    cudaFuncSetAttribute(&tlr_task_gemm<kTF32, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaFuncSetAttribute(&tlr_task_gemm<kTF32, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
+    cfg.gridDim = dim3(kPair, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = kPair;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int c = 0;
-    if (cudaOccupancyMaxActiveClusters(&c, &tlr_task_gemm<kTF32, 2>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&c, &tlr_task_gemm<kTF32, kPair>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       c = 0;
     }
@@ -1171,9 +1205,11 @@ int resident_pairs() {
   return n;
 }
 
-int max_resident_pairs(bool tf32) { return tf32 ? resident_pairs<true>() : resident_pairs<false>(); }
+int max_resident_pairs(bool tf32) { return tf32 ? resident_clusters<true, 2>() : resident_clusters<false, 2>(); }
+int max_resident_quads(bool tf32) { return tf32 ? resident_clusters<true, 4>() : resident_clusters<false, 4>(); }
 
 cudaError_t launch_task_gemm(bool tf32, int pair, const Params &p, int grid, cudaStream_t stream) {
+  if (pair == 4) return tf32 ? launch_one<true, 4>(p, grid, stream) : launch_one<false, 4>(p, grid, stream);
   if (pair == 2) return tf32 ? launch_one<true, 2>(p, grid, stream) : launch_one<false, 2>(p, grid, stream);
   return tf32 ? launch_one<true, 1>(p, grid, stream) : launch_one<false, 1>(p, grid, stream);
 }

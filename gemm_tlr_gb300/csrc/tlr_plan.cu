@@ -62,6 +62,7 @@
 namespace tlr {
 cudaError_t launch_task_gemm(bool tf32, int pair, const Params &p, int grid, cudaStream_t stream);
 int max_resident_pairs(bool tf32);
+int max_resident_quads(bool tf32);
 cudaError_t launch_round_tf32(const float *const *src, float *const *dst, const int64_t *count, int n,
                               int grid, cudaStream_t stream);
 cudaError_t launch_scale_c(float *C, int64_t ldc, int64_t m, int64_t n, float beta, int grid,
@@ -1125,21 +1126,6 @@ TripleLayout layout_triple(const LOp &X, const LOp &Y, int i0, int i1, int j0, i
   return L;
 }
 
-// Final-stage FLOPs of the per-triple order over a rectangle (right blocks
-// K = r_ik, left blocks K = r_kj, the dense-tile blocks included).
-double triple_final_cost(const LOp &X, const LOp &Y, const TripleLayout &L) {
-  double f = 0;
-  for (int i = L.i0; i < L.i1; ++i)
-    for (int j = L.j0; j < L.j1; ++j)
-      for (int k = 0; k < L.nk; ++k) {
-        const uint8_t sd = L.side[L.ijk(i, j, k)];
-        if (sd == kSideNone) continue;
-        const double K = sd == kSideRight ? X.r(i, k) : Y.r(k, j);
-        f += 2.0 * static_cast<double>(X.rd[i]) * static_cast<double>(Y.cd[j]) * K;
-      }
-  return f;
-}
-
 void build_rect_triple(Builder &B, const TripleLayout &L, std::vector<Task> &l1, std::vector<Task> &l2,
                        std::vector<Task> &l3) {
   const LOp &X = B.X;
@@ -1720,10 +1706,43 @@ int choose_l1_pair(const PlanCore &pc, int prep_pair, int pair) {
   return (pc.pv.dense_left || pc.pv.dense_right) ? pair : prep_pair;
 }
 
+// Final-stage FLOPs of the per-triple order over all of C, on the same terms
+// as F_R and F_L: each low-rank triple's K is min(r_ik, r_kj), the k = j block
+// V_ij^T D_jj has K = r_ij, and the terms every order shares (D_ii W_ij Z_ij^T,
+// D_ii D_ii) are left out; before any regrouping for the segment limit.
+double triple_cost(const PlanCore &pc) {
+  const LOp &X = pc.XR, &Y = pc.YR;
+  double f = 0;
+  for (int i = 0; i < X.nr; ++i)
+    for (int j = 0; j < Y.nc; ++j) {
+      const double dd = 2.0 * static_cast<double>(X.rd[i]) * static_cast<double>(Y.cd[j]);
+      for (int k = 0; k < X.nc; ++k) {
+        if (X.dt(i, k)) continue;
+        if (Y.dt(k, j)) { f += dd * X.r(i, k); continue; }
+        if (X.r(i, k) > 0 && Y.r(k, j) > 0) f += dd * std::min(X.r(i, k), Y.r(k, j));
+      }
+    }
+  return f;
+}
+
+// TLR_ORDER_AUTO takes the per-triple order for the whole product when it is
+// available and its final stage needs at most 90 % of the FLOPs of the cheaper
+// single order (the large variable-rank product: 1.60e12 against 3.44e12
+// FLOPs, 2.38 against 3.70 ms); otherwise the per-rectangle choice stays.
+// TLR_TRIPLE=0/1 overrides (tuning).
+tlr_order_t resolve_order(const PlanCore &pc, tlr_order_t order) {
+  if (order != TLR_ORDER_AUTO) return order;
+  if (!can_triple(pc)) return TLR_ORDER_PER_RECT;
+  if (const char *e = getenv("TLR_TRIPLE")) return atoi(e) ? TLR_ORDER_TRIPLE : TLR_ORDER_PER_RECT;
+  const double single = std::min(rect_cost(pc, 0, pc.nI, 0, pc.nJ, false), rect_cost(pc, 0, pc.nI, 0, pc.nJ, true));
+  return triple_cost(pc) <= 0.9 * single ? TLR_ORDER_TRIPLE : TLR_ORDER_PER_RECT;
+}
+
 bool plan_split(const PlanCore &pc, int64_t budget, tlr_order_t force, int es, std::vector<Rect> &rects,
                 int &narenas) {
   const int64_t avail = budget - pc.fixed;
   if (avail < 0) return false;
+  force = resolve_order(pc, force);
   if (force == TLR_ORDER_TRIPLE && !can_triple(pc)) return false;
   {
     const int bn = choose_bn(pc), pair = choose_pair(pc, bn);
@@ -1841,6 +1860,70 @@ void interleave(const std::vector<Task> &a, const std::vector<Task> &b, const st
     if (take_a) { ca += task_cost(a[ia], segs, outs, bn); out.push_back(a[ia++]); from_a.push_back(1); }
     else { cb += task_cost(b[ib], segs, outs, bn); out.push_back(b[ib++]); from_a.push_back(0); }
   }
+}
+
+// Final-product tasks regrouped for clusters of two CTA pairs that share their
+// B operand (the kernel's quad mode): groups of 2 x kTicketBatch tickets, the
+// first kTicketBatch for the first pair and the rest for the second, slot q of
+// one pair and slot q of the other with equal B-side segments. The builder
+// emits a pair's batch as one row tile against up to kTicketBatch column tiles,
+// and the next batch as the next row tile against the same column tiles, so
+// consecutive batches pair up; a batch without a partner gets a copy of itself
+// that stores nothing (rows = 0), and short batches are padded with tasks that
+// have no segments and store nothing.
+bool same_b_side(const Task &a, const Task &b, const std::vector<Seg> &segs) {
+  if (a.nseg != b.nseg || a.cols != b.cols || a.col0 != b.col0) return false;
+  for (int q = 0; q < a.nseg; ++q) {
+    const Seg &x = segs[a.seg0 + q], &y = segs[b.seg0 + q];
+    if (x.b_map != y.b_map || x.b_x != y.b_x || x.b_y != y.b_y || x.k_len != y.k_len || x.flags != y.flags) return false;
+  }
+  return true;
+}
+
+Task silent_copy(const Task &t, bool keep_segments) {
+  Task n = t;
+  n.rows = 0;
+  if (!keep_segments) n.nseg = 0;
+  n.signal = -1;
+  n.signal_writes = 0;
+  n.dep[0] = n.dep[1] = -1;
+  n.dep_target[0] = n.dep_target[1] = 0;
+  return n;
+}
+
+std::vector<Task> quad_regroup(const std::vector<Task> &fin, const std::vector<Seg> &segs) {
+  std::vector<std::pair<size_t, size_t>> batches;
+  for (size_t q = 0; q < fin.size();) {
+    size_t e = q + 1;
+    while (e < fin.size() && e - q < static_cast<size_t>(kTicketBatch) && fin[e].row0 == fin[q].row0 &&
+           fin[e].out == fin[q].out)
+      ++e;
+    batches.push_back({q, e});
+    q = e;
+  }
+  std::vector<Task> out;
+  for (size_t bi = 0; bi < batches.size();) {
+    const size_t a0 = batches[bi].first, n = batches[bi].second - a0;
+    bool paired = bi + 1 < batches.size() && batches[bi + 1].second - batches[bi + 1].first == n;
+    const size_t b0 = paired ? batches[bi + 1].first : 0;
+    for (size_t k = 0; paired && k < n; ++k)
+      if (!same_b_side(fin[a0 + k], fin[b0 + k], segs)) paired = false;
+    for (size_t k = 0; k < static_cast<size_t>(kTicketBatch); ++k)
+      out.push_back(k < n ? fin[a0 + k] : silent_copy(fin[a0], false));
+    for (size_t k = 0; k < static_cast<size_t>(kTicketBatch); ++k) {
+      if (k >= n) out.push_back(silent_copy(fin[a0], false));
+      else out.push_back(paired ? fin[b0 + k] : silent_copy(fin[a0 + k], true));
+    }
+    bi += paired ? 2 : 1;
+  }
+  return out;
+}
+
+// Quad mode (two CTA pairs per cluster sharing B) for the final-product launches
+// of the two-launch schedule. TLR_QUAD=0/1 overrides.
+bool quad_enabled() {
+  if (const char *e = getenv("TLR_QUAD")) return atoi(e) != 0;
+  return false;
 }
 
 // Counters whose waiting tasks all run in later launches than every task that
@@ -2004,8 +2087,11 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
         }
         continue;
       }
-      const std::vector<Task> *lists[2] = {&prep[ri], &fin[ri]};
-      const int kinds[2] = {kKindPrep, kKindFinal}, pairs[2] = {tb.prep_pair, tb.pair};
+      const bool quad = tb.pair == 2 && quad_enabled() && !fin[ri].empty();
+      std::vector<Task> fq;
+      if (quad) fq = quad_regroup(fin[ri], tb.segs);
+      const std::vector<Task> *lists[2] = {&prep[ri], quad ? &fq : &fin[ri]};
+      const int kinds[2] = {kKindPrep, kKindFinal}, pairs[2] = {tb.prep_pair, quad ? 4 : tb.pair};
       for (int q = 0; q < 2; ++q) {
         if (lists[q]->empty()) continue;
         const int64_t t0 = static_cast<int64_t>(stream.size());
@@ -2118,15 +2204,38 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
   }
   const int64_t Cm = pc.pv.Cm, Cn = pc.pv.Cn;
   std::vector<int> task_pair(tb.all.size(), tb.pair), task_launch(tb.all.size(), 0);
+  std::vector<uint8_t> task_quad(tb.all.size(), 0);
   for (size_t li = 0; li < tb.launches.size(); ++li) {
     const Launch &l = tb.launches[li];
-    for (int64_t ti = l.t0; ti < l.t1; ++ti) { task_pair[ti] = l.pair; task_launch[ti] = static_cast<int>(li); }
+    for (int64_t ti = l.t0; ti < l.t1; ++ti) {
+      task_pair[ti] = l.pair == 4 ? 2 : l.pair;   // CTAs working on one task
+      task_quad[ti] = l.pair == 4;
+      task_launch[ti] = static_cast<int>(li);
+    }
+    if (l.pair == 4) {   // whole groups whose two halves agree slot by slot on B
+      const int64_t g = 2 * kTicketBatch;
+      if ((l.t1 - l.t0) % g) return "quad launch: not whole groups of tickets";
+      for (int64_t t = l.t0; t < l.t1; t += g)
+        for (int q = 0; q < kTicketBatch; ++q)
+          if (!same_b_side(tb.all[t + q], tb.all[t + kTicketBatch + q], tb.segs)) {
+            snprintf(buf, sizeof buf, "quad launch: tickets %lld and %lld differ in B", (long long)(t + q),
+                     (long long)(t + kTicketBatch + q));
+            return buf;
+          }
+    }
   }
   std::set<std::pair<int64_t, int64_t>> ctiles;
   double carea = 0;
   for (size_t ti = 0; ti < tb.all.size(); ++ti) {
     const Task &t = tb.all[ti];
-    if (t.rows < 1 || t.rows > kBM * task_pair[ti] || t.cols < 1 || t.cols > tb.bn || t.nseg > kMaxSegs) { snprintf(buf, sizeof buf, "task %zu: bad extent or segment count", ti); return buf; }
+    if (t.rows < (task_quad[ti] ? 0 : 1) || t.rows > kBM * task_pair[ti] || t.cols < 1 || t.cols > tb.bn ||
+        t.nseg > kMaxSegs) {
+      snprintf(buf, sizeof buf, "task %zu: bad extent or segment count", ti);
+      return buf;
+    }
+    if (t.rows == 0) {   // a quad launch's silent task: reads like its partner, stores nothing
+      if (t.signal >= 0 || t.dep[0] >= 0 || t.dep[1] >= 0) { snprintf(buf, sizeof buf, "task %zu: silent task with counters", ti); return buf; }
+    }
     for (int q = 0; q < t.nseg; ++q) {
       const Seg &g = tb.segs[t.seg0 + q];
       if (g.k_len <= 0 || g.a_map < 0 || g.b_map < 0 || g.a_map >= (int)tb.views.size() || g.b_map >= (int)tb.views.size()) {
@@ -2151,7 +2260,7 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
       if (t.npiece || t.row0 < 0 || t.col0 < 0 || t.row0 + t.rows > R || t.col0 + t.cols > Cc) {
         snprintf(buf, sizeof buf, "task %zu: C tile outside C", ti); return buf;
       }
-      if (!ctiles.insert({o.trans ? t.col0 : t.row0, o.trans ? t.row0 : t.col0}).second) {
+      if (t.rows > 0 && !ctiles.insert({o.trans ? t.col0 : t.row0, o.trans ? t.row0 : t.col0}).second) {
         snprintf(buf, sizeof buf, "task %zu: C tile written twice", ti); return buf;
       }
       carea += static_cast<double>(t.rows) * t.cols;
@@ -2502,6 +2611,7 @@ tlr_status_t tlr_analyze(tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A, con
   }
   out->F_R = final_cost(X, 0, X.nr, W);
   out->F_L = final_cost(pc.XL, 0, pc.XL.nr, H);
+  out->F_P = triple_cost(pc);
   out->order = out->F_L < out->F_R ? TLR_ORDER_LEFT : TLR_ORDER_RIGHT;
   out->T_right_rows = sr; out->T_right_cols = W;
   out->T_left_rows = H; out->T_left_cols = sg;
@@ -2522,8 +2632,14 @@ tlr_status_t tlr_analyze(tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A, con
 
 tlr_status_t tlr_gemm_workspace_bytes(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A,
                                       const tlr_operand_t *B, int runs, size_t *bytes) {
+  return tlr_gemm_workspace_bytes_for_order(h, opA, opB, A, B, runs, TLR_ORDER_AUTO, bytes);
+}
+
+tlr_status_t tlr_gemm_workspace_bytes_for_order(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A,
+                                                const tlr_operand_t *B, int runs, tlr_order_t order, size_t *bytes) {
   (void)h;
   if (!bytes) return TLR_STATUS_INVALID_ARG;
+  if (order < TLR_ORDER_AUTO || order > TLR_ORDER_PER_RECT) return TLR_STATUS_INVALID_ARG;
   PlanCore pc;
   tlr_status_t st = core_init(pc, opA, opB, A, B, false, 0);
   if (st) return st;
@@ -2531,21 +2647,23 @@ tlr_status_t tlr_gemm_workspace_bytes(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB
   if (runs <= 0) runs = 1;
   std::vector<Rect> rects;
   int na = 1;
-  int64_t whole = INT64_MAX / 8;
-  if (pc.can_right) whole = std::min(whole, rect_bytes(pc, 0, pc.nI, 0, pc.nJ, false, es));
-  if (pc.can_left) whole = std::min(whole, rect_bytes(pc, 0, pc.nI, 0, pc.nJ, true, es));
+  int64_t whole = 0;   // the largest one-rectangle workspace of any order the plan may take
+  if (pc.can_right) whole = std::max(whole, rect_bytes(pc, 0, pc.nI, 0, pc.nJ, false, es));
+  if (pc.can_left) whole = std::max(whole, rect_bytes(pc, 0, pc.nI, 0, pc.nJ, true, es));
+  if (can_triple(pc)) whole = std::max(whole, rect_bytes_triple(pc, 0, pc.nI, 0, pc.nJ, es));
   int64_t hi = pc.fixed + 2 * whole;
-  if (!plan_split(pc, hi, TLR_ORDER_AUTO, es, rects, na)) return TLR_STATUS_INVALID_ARG;
+  if (order == TLR_ORDER_TRIPLE && !can_triple(pc)) return TLR_STATUS_UNSUPPORTED;
+  if (!plan_split(pc, hi, order, es, rects, na)) return TLR_STATUS_INVALID_ARG;
   const int min_runs = static_cast<int>(rects.size());
   runs = std::max(runs, min_runs);
   int64_t lo = pc.fixed;
   // smallest budget whose plan has at most `runs` rectangles
   while (lo < hi) {
     const int64_t mid = lo + (hi - lo) / 2;
-    if (plan_split(pc, mid, TLR_ORDER_AUTO, es, rects, na) && static_cast<int>(rects.size()) <= runs) hi = mid;
+    if (plan_split(pc, mid, order, es, rects, na) && static_cast<int>(rects.size()) <= runs) hi = mid;
     else lo = mid + 1;
   }
-  plan_split(pc, hi, TLR_ORDER_AUTO, es, rects, na);
+  plan_split(pc, hi, order, es, rects, na);
   *bytes = static_cast<size_t>(pc.fixed + na * align_up(max_rect_bytes(pc, rects, es), 256));
   return TLR_STATUS_OK;
 }
@@ -2575,8 +2693,7 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
                              tlr_order_t order, tlr_plan_t *plan_out) {
   if (!h || !plan_out) return TLR_STATUS_INVALID_ARG;
   *plan_out = nullptr;
-  if (order != TLR_ORDER_AUTO && order != TLR_ORDER_RIGHT && order != TLR_ORDER_LEFT && order != TLR_ORDER_TRIPLE)
-    return TLR_STATUS_INVALID_ARG;
+  if (order < TLR_ORDER_AUTO || order > TLR_ORDER_PER_RECT) return TLR_STATUS_INVALID_ARG;
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TLR_STATUS_ALIGNMENT;
   const uint64_t ws = reinterpret_cast<uint64_t>(workspace);
   PlanCore pc;
@@ -2680,6 +2797,7 @@ tlr_status_t tlr_debug_check_plan(tlr_op_t opA, tlr_op_t opB, const tlr_operand_
                                   size_t workspace_bytes, tlr_order_t order, tlr_plan_info_t *info,
                                   char *msg, size_t msg_len) {
   if (msg && msg_len) msg[0] = 0;
+  if (order < TLR_ORDER_AUTO || order > TLR_ORDER_PER_RECT) return TLR_STATUS_INVALID_ARG;
   const uint64_t ws = 0x100000000000ull;   // a stand-in address: nothing is dereferenced
   PlanCore pc;
   tlr_status_t st = core_init(pc, opA, opB, A, B, true, ws);
@@ -2723,8 +2841,7 @@ tlr_status_t tlr_plan_rects(tlr_plan_t plan, tlr_rect_t *rects, int32_t capacity
 tlr_status_t tlr_debug_plan_rects(tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A, const tlr_operand_t *B,
                                   size_t workspace_bytes, tlr_order_t order, tlr_rect_t *rects, int32_t capacity,
                                   int32_t *count) {
-  if (order != TLR_ORDER_AUTO && order != TLR_ORDER_RIGHT && order != TLR_ORDER_LEFT && order != TLR_ORDER_TRIPLE)
-    return TLR_STATUS_INVALID_ARG;
+  if (order < TLR_ORDER_AUTO || order > TLR_ORDER_PER_RECT) return TLR_STATUS_INVALID_ARG;
   PlanCore pc;
   tlr_status_t st = core_init(pc, opA, opB, A, B, false, 0x100000000000ull);
   if (st) return st;
@@ -2806,6 +2923,10 @@ tlr_status_t tlr_plan_execute(tlr_plan_t p, float alpha, float beta, float *C, i
       const int pairs = max_resident_pairs(p->tf32);
       if (pairs <= 0) return TLR_STATUS_UNSUPPORTED;
       grid = 2 * static_cast<int>(std::min<int64_t>(pairs, l.t1 - l.t0));
+    } else if (l.pair == 4) {   // clusters of two pairs, one group of 2 kTicketBatch tickets each at a time
+      const int quads = max_resident_quads(p->tf32);
+      if (quads <= 0) return TLR_STATUS_UNSUPPORTED;
+      grid = 4 * static_cast<int>(std::min<int64_t>(quads, (l.t1 - l.t0) / (2 * kTicketBatch)));
     }
     if (record_start(h, l.kind, ev) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
     if (launch_task_gemm(p->tf32, l.pair, prm, grid, h->stream) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;

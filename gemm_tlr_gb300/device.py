@@ -120,7 +120,8 @@ class DeviceProblem:
 
     def make_plan(self, handle: int, budget: Optional[int] = None, order: int = _abi.TLR_ORDER_AUTO):
         import torch
-        need_full = _abi.tlr_gemm_workspace_bytes(handle, self.opA, self.opB, self.A.desc, self.B.desc, 1)
+        need_full = _abi.tlr_gemm_workspace_bytes_for_order(handle, self.opA, self.opB, self.A.desc, self.B.desc, 1,
+                                                            order)
         if budget is None:
             budget = self.p.budget if self.p.budget is not None else need_full
         self.ws_bytes = int(budget)

@@ -79,11 +79,16 @@ typedef enum { TLR_OP_N = 0, TLR_OP_T = 1 } tlr_op_t;
 typedef enum { TLR_F32 = 0, TLR_BF16 = 1, TLR_F16 = 2 } tlr_dtype_t;
 typedef enum { TLR_KIND_TLR = 0, TLR_KIND_DENSE = 1 } tlr_kind_t;
 /* Association order of the low-rank products (page 1, "Association order and
- * workspace"; page 2, "The O_A O_B terms"): AUTO takes the cheaper of RIGHT
- * U (S Z^T) and LEFT (U S) Z^T per output rectangle; TRIPLE decides per tile
- * triple (i, k, j) by min(r_ik, r_kj) after S_ikj = V_ik^T W_kj (two TLR
- * operands with a 16-bit element type; otherwise TLR_STATUS_UNSUPPORTED). */
-typedef enum { TLR_ORDER_AUTO = 0, TLR_ORDER_RIGHT = 1, TLR_ORDER_LEFT = 2, TLR_ORDER_TRIPLE = 3 } tlr_order_t;
+ * workspace"; page 2, "The O_A O_B terms"): RIGHT U (S Z^T) or LEFT (U S) Z^T
+ * everywhere; PER_RECT the cheaper of the two per output rectangle; TRIPLE
+ * decided per tile triple (i, k, j) by min(r_ik, r_kj) after S_ikj = V_ik^T W_kj
+ * (two TLR operands with a 16-bit element type; otherwise
+ * TLR_STATUS_UNSUPPORTED). AUTO takes TRIPLE where it is available and its
+ * final stage needs at most 90 % of the FLOPs of the cheaper single order over
+ * all of C, else PER_RECT. */
+typedef enum {
+    TLR_ORDER_AUTO = 0, TLR_ORDER_RIGHT = 1, TLR_ORDER_LEFT = 2, TLR_ORDER_TRIPLE = 3, TLR_ORDER_PER_RECT = 4
+} tlr_order_t;
 
 /* One operand. Fields not used by its kind must be zero / NULL. */
 typedef struct tlr_operand {
@@ -151,6 +156,9 @@ typedef struct tlr_analysis {
     int64_t T_right_rows, T_right_cols, T_left_rows, T_left_cols; /* terminal workspaces (elements) */
     int64_t coupling_products;    /* (i,k,j) with both tiles low-rank and non-zero rank */
     int64_t distinct_shapes;      /* distinct (r_ik, r_kj) among them */
+    double F_P;                   /* final-stage cost of the per-triple order over all of C on the
+                                     terms of F_R and F_L (page 2, "The O_A O_B terms": K = min(r_ik,
+                                     r_kj) per low-rank triple, K = r_ij for the k = j block) */
 } tlr_analysis_t;
 
 /* Status name, never NULL. */
@@ -174,10 +182,15 @@ tlr_status_t tlr_analyze(tlr_op_t opA, tlr_op_t opB, const tlr_operand_t *A,
 tlr_status_t tlr_gemm_workspace_bytes(tlr_handle_t handle, tlr_op_t opA, tlr_op_t opB,
                                       const tlr_operand_t *A, const tlr_operand_t *B,
                                       int runs, size_t *bytes);
+/* The same for a plan created with association order `order` (the call above
+ * sizes for TLR_ORDER_AUTO); TLR_STATUS_UNSUPPORTED where the order cannot apply. */
+tlr_status_t tlr_gemm_workspace_bytes_for_order(tlr_handle_t handle, tlr_op_t opA, tlr_op_t opB,
+                                                const tlr_operand_t *A, const tlr_operand_t *B,
+                                                int runs, tlr_order_t order, size_t *bytes);
 
 /* Plan a product: validate the descriptors, compute the rank prefixes, split C
  * into rectangles of output tiles that fit `workspace_bytes`, choose the
- * association order per rectangle (`order` forces one), and build the
+ * association order (`order`, see tlr_order_t), and build the
  * device-side descriptor tables. The plan binds the operand buffers and the
  * workspace pointer (caller-owned, >= workspace_bytes, 256-byte aligned); it
  * owns only its small descriptor tables. */

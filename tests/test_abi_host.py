@@ -157,13 +157,14 @@ def test_plan_tables_are_valid(g, cfg, scale, order):
     budget = p.budget or g.tlr_gemm_workspace_bytes(0, opA, 0, A, B, 1)
     st, msg, info = g.tlr_debug_check_plan(opA, 0, A, B, budget, order)
     assert st == 0, msg
-    if order == 0:
-        from gemm_tlr_gb300 import flops
-        want = flops.executed_flops(p, "R")["total"]
-        if info["runs_left"] == 0:
-            assert abs(info["flops_executed"] - want) <= 1e-9 * want
+    from gemm_tlr_gb300 import flops
+    rects = g.tlr_debug_plan_rects(opA, 0, A, B, budget, order)
+    want = flops.executed_flops_rects(p, rects)["total"]
+    assert abs(info["flops_executed"] - want) <= 1e-9 * want
     if cfg == 5 and scale == 1:
-        assert info["runs"] >= 2 and info["workspace_bytes"] <= p.budget
+        assert info["workspace_bytes"] <= p.budget
+        # the default takes the per-triple order in one rectangle; a single order needs a split
+        assert info["runs"] >= 2 if order else info["runs_triple"] == info["runs"] == 1
 
 
 def test_workspace_bytes_gives_the_requested_runs(g):
@@ -259,12 +260,19 @@ def test_plan_flops_recounted_rectangle_by_rectangle(g, cfg):
                     ("dense", "flops_dense_terms")):
         assert counted[k] == pytest.approx(info[name], rel=1e-12, abs=1.0)
     if cfg == 5:
-        # both orders over all of C give the right-order count of the survey table,
-        # 4.167e12; the mixed plan is cheaper, never dearer
-        assert {r[4] for r in rects} == {"R", "L"}
+        # the default takes the per-triple order here; the per-rectangle plan of the
+        # 2 GiB budget mixes both orders, and either order over all of C gives the
+        # right-order count of the survey table, 4.167e12
+        assert {r[4] for r in rects} == {"P"}
+        per = g.tlr_debug_plan_rects(opA, opB, A, B, budget, g.TLR_ORDER_PER_RECT)
+        st, msg, pinfo = g.tlr_debug_check_plan(opA, opB, A, B, budget, g.TLR_ORDER_PER_RECT)
+        assert st == 0, msg
+        assert {r[4] for r in per} == {"R", "L"}
+        mixed = fl.executed_flops_rects(p, per)["total"]
+        assert mixed == pytest.approx(pinfo["flops_executed"], rel=1e-12)
         assert fl.executed_flops(p, "R")["total"] == pytest.approx(4.167e12, rel=1e-3)
         assert fl.executed_flops(p, "L")["total"] == pytest.approx(4.167e12, rel=1e-3)
-        assert counted["total"] < fl.executed_flops(p, "R")["total"]
+        assert counted["total"] < mixed < fl.executed_flops(p, "R")["total"]
         forced = g.tlr_debug_plan_rects(opA, opB, A, B, budget, g.TLR_ORDER_RIGHT)
         assert {r[4] for r in forced} == {"R"}
         assert fl.executed_flops_rects(p, forced)["total"] == pytest.approx(fl.executed_flops(p, "R")["total"],
@@ -309,12 +317,12 @@ def test_per_triple_plans_validate_and_count(g, name, make, budget):
     counted = fl.executed_flops_rects(p, rects)
     assert counted["total"] == pytest.approx(info["flops_executed"], rel=1e-12)
     assert counted["stage3"] == pytest.approx(info["flops_stage3"], rel=1e-12)
-    st2, _, auto = g.tlr_debug_check_plan(opA, opB, A, B, budget, g.TLR_ORDER_AUTO)
-    assert st2 == 0 and info["flops_executed"] <= auto["flops_executed"]
+    st2, _, per = g.tlr_debug_check_plan(opA, opB, A, B, budget, g.TLR_ORDER_PER_RECT)
+    assert st2 == 0 and info["flops_executed"] <= per["flops_executed"]
     if name == "cfg5":
         # the large product: final products 3.27e12 -> 1.59e12 FLOP
         assert info["flops_stage3"] == pytest.approx(1.595e12, rel=1e-3)
-        assert auto["flops_stage3"] == pytest.approx(3.265e12, rel=1e-3)
+        assert per["flops_stage3"] == pytest.approx(3.265e12, rel=1e-3)
 
 
 def test_four_orders_differ_on_the_asymmetric_workload(g):
@@ -326,7 +334,7 @@ def test_four_orders_differ_on_the_asymmetric_workload(g):
     A, B, keep, opA, opB = _fake(p)
     seen = {}
     for budget in (1 << 40, 24 << 20, 12 << 20):
-        for order in (g.TLR_ORDER_RIGHT, g.TLR_ORDER_LEFT, g.TLR_ORDER_AUTO, g.TLR_ORDER_TRIPLE):
+        for order in (g.TLR_ORDER_RIGHT, g.TLR_ORDER_LEFT, g.TLR_ORDER_PER_RECT, g.TLR_ORDER_TRIPLE):
             st, msg, info = g.tlr_debug_check_plan(opA, opB, A, B, budget, order)
             if st == 3:
                 continue
@@ -373,3 +381,26 @@ def test_per_triple_segment_limit_on_alternating_ranks(g):
     rule = fl.executed_flops_triple(p)["total"]
     assert info["flops_executed"] >= rule
     assert info["flops_executed"] < fl.executed_flops(p, "R")["total"]
+
+
+@pytest.mark.parametrize("make", [lambda: ti.problem(5, scale_down=4), lambda: ti.asym_grid(2048, 256),
+                                  lambda: ti.asym_grid(4096, 256), lambda: ti.skewed_grid(4096, "bf16")],
+                         ids=["cfg5/4", "asym2048", "asym4096", "skewed"])
+def test_auto_order_follows_the_final_stage_costs(g, make):
+    """tlr_analyze's per-triple final cost F_P equals the independent count, and
+    AUTO takes the per-triple order exactly when F_P <= 0.9 min(F_R, F_L)."""
+    from gemm_tlr_gb300 import flops as fl
+    p = make()
+    A, B, keep, opA, opB = _fake(p)
+    n = len(p.A.rdims)
+    out = g.tlr_analyze(opA, opB, A, B, n, n, n)
+    trip = fl.executed_flops_triple(p)
+    base = fl.executed_flops(p, "R")
+    # on the terms of F_R and F_L: the final products of the low-rank triples and
+    # of the k = j blocks (the dense-tile terms every order shares left out)
+    assert out["F_P"] == pytest.approx(trip["stage3"], rel=1e-12)
+    assert out["F_R"] == pytest.approx(base["stage3"], rel=1e-12)
+    rects = g.tlr_debug_plan_rects(opA, opB, A, B, p.budget or (1 << 40), g.TLR_ORDER_AUTO)
+    want = out["F_P"] <= 0.9 * min(out["F_R"], out["F_L"])
+    assert ({r[4] for r in rects} == {"P"}) == want
+    assert base["total"] > 0

@@ -88,13 +88,14 @@ def test_whole_product_matches_oracle(oracle_lib, handle, cfg, scale, variant):
     print(f"{p.name} {variant}: {res} (runs={info['runs']}, left={info['runs_left']})")
 
 
-@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+@pytest.mark.parametrize("cfg,order", [(2, 0), (3, 0), (4, 0), (5, 0), (5, 4)], ids=["2", "3", "4", "5", "5-per_rect"])
 @pytest.mark.parametrize("variant", ["whole", "lowrank_only"])
-def test_full_size_sampled(oracle_lib, handle, cfg, variant):
-    """The graded sizes, in the launch configuration the benchmark times, on sampled entries."""
+def test_full_size_sampled(oracle_lib, handle, cfg, order, variant):
+    """The graded sizes, in the launch configuration the benchmark times (and, for
+    the large product, with the per-rectangle orders too), on sampled entries."""
     kw = dict(zero_diag=True, beta_override=0.0) if variant == "lowrank_only" else {}
     p = ti.problem(cfg, **kw)
-    out, info = run(p, handle)
+    out, info = run(p, handle, order=order)
     b = p.A.b
     rows = sample_indices(p.m, b, seed=cfg)
     cols = sample_indices(p.n, b if p.B.kind == "tlr" else 1024, seed=cfg + 10)
@@ -102,8 +103,26 @@ def test_full_size_sampled(oracle_lib, handle, cfg, variant):
     got = out[np.ix_(rows, cols)]
     res = check_p(got, ref, p, rows=rows, cols=cols)
     print(f"{p.name} {variant} sampled: {res}")
-    if cfg == 5:
-        assert info["runs"] >= 2          # the 2 GiB budget forces a split
+    if cfg == 5 and order == 4:
+        assert info["runs"] >= 2 and info["runs_triple"] == 0   # the 2 GiB budget forces a split
+    elif cfg == 5:
+        assert info["runs_triple"] == info["runs"]              # the default takes the per-triple order
+
+
+@pytest.mark.parametrize("scale", [16, 8])
+@pytest.mark.parametrize("variant", ["whole", "lowrank_only", "dense_only"])
+def test_per_rectangle_orders_on_the_large_family(oracle_lib, handle, scale, variant):
+    """The per-rectangle orders (TLR_ORDER_PER_RECT), which the default no longer
+    takes for this family, against the oracle."""
+    kw = {}
+    if variant == "lowrank_only":
+        kw = dict(zero_diag=True, beta_override=0.0)
+    elif variant == "dense_only":
+        kw = dict(zero_lowrank=True)
+    p = ti.problem(5, scale_down=scale, **kw)
+    out, info = run(p, handle, order=4)
+    assert info["runs_triple"] == 0
+    print(p.name, variant, check_p(out, oracle_lib.gemm_problem(p), p), info["runs"], info["runs_left"])
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -197,7 +216,7 @@ def test_all_lowrank_rectangular_grid(oracle_lib, handle):
     A = ti.make_tlr(rng, 512, 256, None, "bf16", cols=768, diag_dense=False, ranks=np.array(g["rA"]))
     B = ti.make_tlr(rng, 768, 256, None, "bf16", diag_dense=False, ranks=np.array(g["rB_solutions"][0]))
     p = ti.Problem("worked", A, B, "N", "N", 1.0, 0.0, None, 512, 768, "bf16")
-    out, info = run(p, handle)
+    out, info = run(p, handle, order=4)      # per rectangle: the right order, as the pages' example
     assert info["runs_right"] == 1 and info["runs_left"] == 0
     check_p(out, oracle_lib.gemm_problem(p), p)
 
