@@ -23,10 +23,15 @@ Contents
 * ``planner_ref.py``: the rank-metadata quantities the planner is built on,
   written from their definitions (first page, section "Association order and
   workspace").
+* ``tlr_output.py``: the TLR-output product -- the dense product tiles
+  recompressed tile by tile to the smallest rank within a relative Frobenius
+  tolerance (second page, section "Introduction: TLR GEMM"; the recompression
+  rule is a reading, stated there). It has no GPU counterpart yet.
 
 Every function here is pinned by a ``-m "not gpu"`` test against something other
 than itself (brute force on tiny inputs, closed forms, special cases, printed
-values of the worked example); see ``tests/test_oracle.py``.
+values of the worked example); see ``tests/test_oracle.py`` and
+``tests/test_tlr_output_oracle.py``.
 """
 from __future__ import annotations
 
