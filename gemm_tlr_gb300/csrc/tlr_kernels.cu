@@ -181,6 +181,10 @@ __device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void *tm
       : "memory");
 }
 
+__device__ __forceinline__ void prefetch_l2(const void *ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 // L2 policy for data written once and not read again in the launch (C): its
 // lines are the first candidates for eviction, ahead of operands still in use.
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -623,19 +627,24 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (kSt + s); };
   auto tfull_bar = [&](int a) { return bars + 8u * (2 * kSt + a); };
-  auto tempty_bar = [&](int a) { return bars + 8u * (2 * kSt + 2 + a); };
-  const uint32_t drain_bar = bars + 8u * (2 * kSt + 4);
-  auto sfull_bar = [&](int r) { return bars + 8u * (2 * kSt + 5 + r); };
-  auto sempty_bar = [&](int r) { return bars + 8u * (2 * kSt + 5 + kRing + r); };
-  const uint32_t sig_bar = bars + 8u * (2 * kSt + 5 + 2 * kRing);   // epilogue stores published
-  static_assert(8 * (2 * kSt + 6 + 2 * kRing) + 16 <= 512, "barrier area");
-  uint32_t *tmem_holder =
-      reinterpret_cast<uint32_t *>(base_ptr + kSt * kStB + kRing * kSlotBytes + 8 * (2 * kSt + 6 + 2 * kRing));
+  auto tempty_bar = [&](int a) { return bars + 8u * (2 * kSt + kMaxAcc + a); };
+  const uint32_t drain_bar = bars + 8u * (2 * kSt + 2 * kMaxAcc);
+  auto sfull_bar = [&](int r) { return bars + 8u * (2 * kSt + 2 * kMaxAcc + 1 + r); };
+  auto sempty_bar = [&](int r) { return bars + 8u * (2 * kSt + 2 * kMaxAcc + 1 + kRing + r); };
+  const uint32_t sig_bar = bars + 8u * (2 * kSt + 2 * kMaxAcc + 1 + 2 * kRing);   // epilogue stores published
+  static_assert(8 * (2 * kSt + 2 * kMaxAcc + 2 + 2 * kRing) + 16 <= 512, "barrier area");
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + kSt * kStB + kRing * kSlotBytes +
+                                                       8 * (2 * kSt + 2 * kMaxAcc + 2 + 2 * kRing));
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bn = p.bn;
+  // TMEM holds kTmemCols fp32 columns: two accumulators of 256 columns, or four
+  // of 128 for tiles at most 128 wide, so that the MMAs of up to three tiles
+  // proceed while the epilogue drains the fourth
+  const int nacc = bn <= kMaxBN / 2 ? 4 : 2;
+  const uint32_t acc_cols = static_cast<uint32_t>(kTmemCols / nacc);
   const uint32_t crank = kCG2 ? cluster_rank() : 0u;      // rank in the cluster
   const uint32_t rank = crank & 1u;                        // rank in the pair; 0: leader of the pair
   const uint32_t lead_rank = crank & ~1u;                  // cluster rank of this pair's leader
@@ -646,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), kQuad ? 2 : 1);   // quad: both pairs' MMAs release a stage
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kMaxAcc; ++a) {
       mbar_init(tfull_bar(a), 1);
       mbar_init(tempty_bar(a), 4 * kEpiGroups * kPairCTAs);   // one arrival per epilogue warp of the pair
     }
@@ -888,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
         }
         if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p, 2, kCG2)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kMaxBN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * acc_cols;
         uint32_t accumulate = 0;
         for (int s = 0; ok && s < nseg; ++s) {
           const Seg sg = sl.segs[s];
@@ -940,7 +949,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
           mbar_arrive(tfull_bar(acc));
           if constexpr (kCG2) mbar_arrive_remote(map_to_rank(tfull_bar(acc), lead_rank + 1));
         }
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == nacc) { acc = 0; acc_phase ^= 1u; }
       }
       // All MMAs issued by this thread complete before TMEM is released.
       if (leader) {
@@ -998,12 +1007,27 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       const Out o = sl.out;
       __syncwarp();
       if (lane == 0) mbar_arrive(sempty_bar(r));
+      if (o.kind == kOutC && p.beta != 0.f) {
+        // C is read by this warp's stores: bring its lines into L2 while the
+        // tile's MMAs run, so that the read-modify-write does not wait on DRAM
+        const int64_t d0 = __shfl_sync(0xffffffffu, drow, 0);
+        const bool rows_ok = __all_sync(0xffffffffu, valid && drow == d0 + lane);
+        for (int cc = 64 * grp; cc < ncols; cc += 64 * kEpiGroups) {
+          for (int h = 0; h < 64 && cc + h < ncols; h += 32) {
+            if (!o.trans) {   // column c of the warp's 32 contiguous rows: one 128-byte line
+              if (rows_ok && cc + h + lane < ncols) prefetch_l2(p.C + d0 + (col0 + cc + h + lane) * p.ldc);
+            } else if (valid) {   // this lane's tile row: a contiguous run of C's column drow
+              prefetch_l2(p.C + (col0 + cc + h) + drow * p.ldc);
+            }
+          }
+        }
+      }
       if (!ready(tfull_bar(acc), acc_phase)) flush();
       if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p, 4, kCG2)) break;
       tc_fence_after();
       if (pend != signal || pend_n >= kSignalBatch) flush();   // the earlier stores have had time to drain
       const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                              static_cast<uint32_t>(acc * kMaxBN);
+                              static_cast<uint32_t>(acc) * acc_cols;
       // row-major 16-bit outputs: the output rows of this lane's four 16-byte
       // pieces of every chunk (workspace rows fit in 32 bits)
       int32_t rowd[4] = {-1, -1, -1, -1};
@@ -1038,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
         if (leader) mbar_arrive(tempty_bar(acc));
         else mbar_arrive_remote(map_to_rank(tempty_bar(acc), lead_rank));
       }
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == nacc) { acc = 0; acc_phase ^= 1u; }
       if (signal >= 0) {
         pend = signal;
         pend_n += 1;

@@ -406,7 +406,8 @@ struct Rect {
 struct Launch {
   int kind;
   int64_t t0, t1;
-  int pair = 1;          // CTAs per output tile in this launch (1, or 2 for CTA pairs)
+  int pair = 1;          // CTAs per output tile in this launch (1, 2 for CTA pairs, 4 for two pairs sharing B)
+  int bn = 0;            // output tile width of this launch's tasks (0: the plan's)
 };
 
 // ------------------------------------------------------------------ builder
@@ -446,6 +447,7 @@ struct Builder {
   int pair = 1;                         // CTAs per final-product tile (each epilogue warp of each signals)
   int prep_bm = kBM, prep_pair = 1;     // the same for Stages 1-2 and the dense precomputes
   int l1_bm = kBM, l1_pair = 1;         // Stage 1 and the dense precomputes (may run on pairs)
+  int prep_bn = 256, l1_bn = 256;       // output tile widths of the Stage-2 and first-stage lists
   int cur_pair = 1;                     // of the list being built
   // Dependency counters of the merged launch (see Task in tlr_tables.h).
   std::vector<uint32_t> *counts = nullptr;              // signals each counter receives so far
@@ -705,7 +707,8 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
                 std::vector<Task> &l3) {
   const LOp &X = B.X;
   const LOp &Y = B.Y;
-  const int es = B.es, bn = B.bn;
+  const int es = B.es;
+  int bn = B.l1_bn;                    // output tile width of the list being built
   int64_t BM = B.l1_bm;                // rows of an output tile (256 for a CTA pair)
   B.cur_pair = B.l1_pair;
   const int i0 = L.i0, i1 = L.i1, j0 = L.j0, j1 = L.j1;
@@ -812,6 +815,7 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
   // ---------------- L2: Stage 2, T_i[k, j] = S_ikj Z_kj^T fused over i
   B.tasks = &l2;
   BM = B.prep_bm;
+  bn = B.prep_bn;
   B.cur_pair = B.prep_pair;
   if (!Y.dense)
     for (int k = 0; k < X.nc; ++k) {
@@ -852,6 +856,7 @@ void build_rect(Builder &B, const RectLayout &L, std::vector<Task> &l1, std::vec
   // ---------------- L3: Stage 3, C[i, J] = alpha (U_i T_i + dense segment) + beta C
   B.tasks = &l3;
   BM = B.bm;
+  bn = B.bn;
   B.cur_pair = B.pair;
   const int outC = B.out_c();
   B.deps(B.cL3, 0, B.cPrep, -1);
@@ -1130,7 +1135,8 @@ void build_rect_triple(Builder &B, const TripleLayout &L, std::vector<Task> &l1,
                        std::vector<Task> &l3) {
   const LOp &X = B.X;
   const LOp &Y = B.Y;
-  const int es = B.es, bn = B.bn;
+  const int es = B.es;
+  int bn = B.l1_bn;                    // output tile width of the list being built
   const int i0 = L.i0, i1 = L.i1, j0 = L.j0, j1 = L.j1, nk = L.nk;
   const uint64_t TR = B.ws + static_cast<uint64_t>(L.TRoff), TL = B.ws + static_cast<uint64_t>(L.TLoff);
   const int outR = B.out_ws(TR, L.ldT, true), outL = B.out_ws(TL, L.ldT, true);
@@ -1208,6 +1214,7 @@ void build_rect_triple(Builder &B, const TripleLayout &L, std::vector<Task> &l1,
   const double before2 = B.fl_s2;
   B.tasks = &l2;
   BM = B.prep_bm;
+  bn = B.prep_bn;
   B.cur_pair = B.prep_pair;
   for (int k = 0; k < nk; ++k) {
     if (L.Soff[k] < 0) continue;
@@ -1313,6 +1320,7 @@ void build_rect_triple(Builder &B, const TripleLayout &L, std::vector<Task> &l1,
   const double before3 = B.fl_s3 + B.fl_dense;
   B.tasks = &l3;
   BM = B.bm;
+  bn = B.bn;
   B.cur_pair = B.pair;
   const int outC = B.out_c();
   B.deps(B.cL3, 0, B.cPrep, -1);
@@ -1816,6 +1824,7 @@ struct Tables {
   int pair = 1;
   int prep_pair = 1;
   int l1_pair = 1;                          // Stage 1 and the dense precomputes
+  int prep_bn = 256, l1_bn = 256;           // tile widths of the Stage-2 and first-stage lists
   std::vector<CUtensorMap> maps;
   std::map<std::tuple<uint64_t, int64_t, int64_t, int64_t, int>, int> map_index;
   std::vector<Task> all;
@@ -1835,6 +1844,19 @@ struct Tables {
   std::vector<TripleLayout> tlayouts;       // per rectangle (empty unless per-triple)
   tlr_plan_info_t info{};
 };
+
+// Tile widths of the Stages 1-2 lists (tuning overrides TLR_PREP_BN and
+// TLR_L1_BN, 128 or 256): on single CTAs in launches of their own a width of 128
+// gives the kernel four accumulators instead of two. The lists keep the final
+// products' width otherwise.
+void choose_prep_widths(Tables &tb) {
+  tb.prep_bn = tb.l1_bn = tb.bn;
+  if (tb.bn != kMaxBN || tb.prep_pair != 1) return;
+  if (const char *e = getenv("TLR_PREP_BN")) tb.prep_bn = atoi(e) == 128 ? 128 : kMaxBN;
+  tb.l1_bn = tb.l1_pair == 1 ? tb.prep_bn : tb.bn;
+  if (tb.l1_pair == 1)
+    if (const char *e = getenv("TLR_L1_BN")) tb.l1_bn = atoi(e) == 128 ? 128 : kMaxBN;
+}
 
 // Estimated SM clocks of a task: tensor-core time or store time, whichever is larger.
 double task_cost(const Task &t, const std::vector<Seg> &segs, const std::vector<Out> &outs, int bn) {
@@ -1991,6 +2013,8 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
     B.prep_bm = kBM * tb.prep_pair;
     B.l1_pair = tb.l1_pair;
     B.l1_bm = kBM * tb.l1_pair;
+    B.prep_bn = tb.prep_bn;
+    B.l1_bn = tb.l1_bn;
     // counters: S_k per contraction tile, "T and P ready", "Stage 3 done"
     B.counts = &tb.counter_counts;
     B.cS0 = static_cast<int32_t>(tb.counter_counts.size());
@@ -2074,16 +2098,17 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
     // launch only waits for counters of its own lower tickets; everything an
     // earlier launch signals is complete before the next one starts.
     for (size_t ri = 0; ri < nr; ++ri) {
-      if (tb.l1_pair != tb.prep_pair) {   // Stage 1 and the dense precomputes in a launch of their own
+      if (tb.l1_pair != tb.prep_pair || tb.l1_bn != tb.prep_bn) {   // Stage 1 and the dense precomputes in a launch of their own
         const size_t n1 = prep[ri].size() - l2count[ri];
         std::vector<Task> a(prep[ri].begin(), prep[ri].begin() + n1), b(prep[ri].begin() + n1, prep[ri].end());
         const std::vector<Task> *lists[3] = {&a, &b, &fin[ri]};
         const int kinds[3] = {kKindStage1, kKindPrep, kKindFinal}, pairs[3] = {tb.l1_pair, tb.prep_pair, tb.pair};
+        const int bns[3] = {tb.l1_bn, tb.prep_bn, tb.bn};
         for (int q = 0; q < 3; ++q) {
           if (lists[q]->empty()) continue;
           const int64_t t0 = static_cast<int64_t>(stream.size());
           push(*lists[q], static_cast<int>(ri));
-          tb.launches.push_back(Launch{kinds[q], t0, static_cast<int64_t>(stream.size()), pairs[q]});
+          tb.launches.push_back(Launch{kinds[q], t0, static_cast<int64_t>(stream.size()), pairs[q], bns[q]});
         }
         continue;
       }
@@ -2092,11 +2117,12 @@ tlr_status_t build_tables(const PlanCore &pc, const std::vector<Rect> &rects, in
       if (quad) fq = quad_regroup(fin[ri], tb.segs);
       const std::vector<Task> *lists[2] = {&prep[ri], quad ? &fq : &fin[ri]};
       const int kinds[2] = {kKindPrep, kKindFinal}, pairs[2] = {tb.prep_pair, quad ? 4 : tb.pair};
+      const int bns[2] = {tb.prep_bn, tb.bn};
       for (int q = 0; q < 2; ++q) {
         if (lists[q]->empty()) continue;
         const int64_t t0 = static_cast<int64_t>(stream.size());
         push(*lists[q], static_cast<int>(ri));
-        tb.launches.push_back(Launch{kinds[q], t0, static_cast<int64_t>(stream.size()), pairs[q]});
+        tb.launches.push_back(Launch{kinds[q], t0, static_cast<int64_t>(stream.size()), pairs[q], bns[q]});
       }
     }
     tb.all = stream;
@@ -2205,11 +2231,13 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
   const int64_t Cm = pc.pv.Cm, Cn = pc.pv.Cn;
   std::vector<int> task_pair(tb.all.size(), tb.pair), task_launch(tb.all.size(), 0);
   std::vector<uint8_t> task_quad(tb.all.size(), 0);
+  std::vector<int> task_bn(tb.all.size(), tb.bn);
   for (size_t li = 0; li < tb.launches.size(); ++li) {
     const Launch &l = tb.launches[li];
     for (int64_t ti = l.t0; ti < l.t1; ++ti) {
       task_pair[ti] = l.pair == 4 ? 2 : l.pair;   // CTAs working on one task
       task_quad[ti] = l.pair == 4;
+      task_bn[ti] = l.bn > 0 ? l.bn : tb.bn;
       task_launch[ti] = static_cast<int>(li);
     }
     if (l.pair == 4) {   // whole groups whose two halves agree slot by slot on B
@@ -2228,7 +2256,7 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
   double carea = 0;
   for (size_t ti = 0; ti < tb.all.size(); ++ti) {
     const Task &t = tb.all[ti];
-    if (t.rows < (task_quad[ti] ? 0 : 1) || t.rows > kBM * task_pair[ti] || t.cols < 1 || t.cols > tb.bn ||
+    if (t.rows < (task_quad[ti] ? 0 : 1) || t.rows > kBM * task_pair[ti] || t.cols < 1 || t.cols > task_bn[ti] ||
         t.nseg > kMaxSegs) {
       snprintf(buf, sizeof buf, "task %zu: bad extent or segment count", ti);
       return buf;
@@ -2386,54 +2414,49 @@ std::string validate_tables(const PlanCore &pc, const Tables &tb, uint64_t ws, i
       }
     }
   }
-  // T coverage per rectangle
+  // T coverage per rectangle: every T row Stage 3 reads has its columns [0, W_J)
+  // written exactly once (by tiles of any width)
   for (size_t ri = 0; ri < tb.layouts.size(); ++ri) {
     if (tb.rect_triple[ri]) continue;
     const RectLayout &L = tb.layouts[ri];
     const bool left = tb.rect_left[ri] != 0;
     const LOp &X = left ? pc.XL : pc.XR;
     const uint64_t T = tb.rect_arena[ri] + static_cast<uint64_t>(L.Toffset);
-    // column interval -> written row intervals
-    std::map<std::pair<int64_t, int64_t>, std::vector<std::pair<int64_t, int64_t>>> wr;
+    std::vector<std::vector<std::pair<int64_t, int64_t>>> wr(static_cast<size_t>(L.Trows));
     for (size_t ti = 0; ti < tb.all.size(); ++ti) {
       if (tb.task_rect[ti] != static_cast<int>(ri)) continue;
       const Task &t = tb.all[ti];
       const Out &o = tb.outs[t.out];
       if (o.kind == kOutC || reinterpret_cast<uint64_t>(o.ptr) != T) continue;
-      auto &rows = wr[{t.col0, t.col0 + t.cols}];
-      if (t.npiece == 0) rows.push_back({t.row0, t.row0 + t.rows});
-      for (int q = 0; q < t.npiece; ++q) {
-        const Piece &pe = tb.pieces[t.piece0 + q];
-        rows.push_back({pe.dst0, pe.dst0 + pe.len});
-      }
+      auto add = [&](int64_t r0, int64_t n) {
+        for (int64_t r = r0; r < r0 + n; ++r)
+          if (r >= 0 && r < L.Trows) wr[r].push_back({t.col0, t.col0 + t.cols});
+      };
+      if (t.npiece == 0) add(t.row0, t.rows);
+      for (int q = 0; q < t.npiece; ++q) add(tb.pieces[t.piece0 + q].dst0, tb.pieces[t.piece0 + q].len);
     }
-    std::vector<std::pair<int64_t, int64_t>> need;
+    std::vector<uint8_t> needed(static_cast<size_t>(L.Trows), 0);
     for (int i = L.i0; i < L.i1; ++i)
       for (size_t pi = 0; pi < X.rowp[i].size(); ++pi)
-        if (X.rowp[i][pi].v.cols > 0) need.push_back({L.Toff[i][pi], L.Toff[i][pi] + X.rowp[i][pi].v.cols});
-    std::sort(need.begin(), need.end());
-    if (need.empty()) continue;
-    int64_t c = 0;
-    for (auto &kv : wr) {
-      if (kv.first.first != c) { snprintf(buf, sizeof buf, "rect %zu: T columns not tiled at %lld", ri, (long long)c); return buf; }
-      c = kv.first.second;
-      auto rows = kv.second;
-      std::sort(rows.begin(), rows.end());
-      if (rows != need) {
-        // merge adjacent written intervals before comparing
-        std::vector<std::pair<int64_t, int64_t>> m;
-        for (auto &x : rows) {
-          if (!m.empty() && m.back().second > x.first) { snprintf(buf, sizeof buf, "rect %zu: T rows written twice", ri); return buf; }
-          if (!m.empty() && m.back().second == x.first) m.back().second = x.second; else m.push_back(x);
+        for (int64_t r = L.Toff[i][pi]; r < L.Toff[i][pi] + X.rowp[i][pi].v.cols; ++r) needed[r] = 1;
+    for (int64_t r = 0; r < L.Trows; ++r) {
+      auto &v = wr[r];
+      std::sort(v.begin(), v.end());
+      int64_t c = 0;
+      for (auto &iv : v) {
+        if (iv.first != c) {
+          snprintf(buf, sizeof buf, "rect %zu: T row %lld written %s at column %lld", ri, (long long)r,
+                   iv.first < c ? "twice" : "with a gap", (long long)c);
+          return buf;
         }
-        std::vector<std::pair<int64_t, int64_t>> n2;
-        for (auto &x : need) {
-          if (!n2.empty() && n2.back().second == x.first) n2.back().second = x.second; else n2.push_back(x);
-        }
-        if (m != n2) { snprintf(buf, sizeof buf, "rect %zu: T rows read by Stage 3 not written exactly once", ri); return buf; }
+        c = iv.second;
+      }
+      if (needed[r] && c != L.WJ) {
+        snprintf(buf, sizeof buf, "rect %zu: T row %lld read by Stage 3 written up to column %lld of %lld", ri,
+                 (long long)r, (long long)c, (long long)L.WJ);
+        return buf;
       }
     }
-    if (c != L.WJ) { snprintf(buf, sizeof buf, "rect %zu: T columns end at %lld of %lld", ri, (long long)c, (long long)L.WJ); return buf; }
   }
   return std::string();
 }
@@ -2727,6 +2750,7 @@ tlr_status_t tlr_plan_create(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB, const t
   tb.pair = p->pair = choose_pair(pc, p->bn);
   tb.prep_pair = choose_prep_pair(pc, p->bn, tb.pair);
   tb.l1_pair = choose_l1_pair(pc, tb.prep_pair, tb.pair);
+  choose_prep_widths(tb);
   st = build_tables(pc, rects, narenas, ws, false, tb);
   if (st) { delete p; return st; }
   p->launches = tb.launches;
@@ -2813,6 +2837,7 @@ tlr_status_t tlr_debug_check_plan(tlr_op_t opA, tlr_op_t opB, const tlr_operand_
   tb.pair = choose_pair(pc, tb.bn);
   tb.prep_pair = choose_prep_pair(pc, tb.bn, tb.pair);
   tb.l1_pair = choose_l1_pair(pc, tb.prep_pair, tb.pair);
+  choose_prep_widths(tb);
   st = build_tables(pc, rects, narenas, ws, true, tb);
   if (st) return st;
   const int64_t need = pc.fixed + narenas * align_up(max_rect_bytes(pc, rects, es), 256);
@@ -2916,6 +2941,7 @@ tlr_status_t tlr_plan_execute(tlr_plan_t p, float alpha, float beta, float *C, i
   for (size_t li = 0; li < p->launches.size(); ++li) {
     const Launch &l = p->launches[li];
     prm.ticket = p->d_counters + li;
+    prm.bn = l.bn > 0 ? l.bn : p->bn;
     prm.tasks = p->d_tasks + l.t0;
     prm.ntasks = static_cast<int32_t>(l.t1 - l.t0);
     int grid = static_cast<int>(std::min<int64_t>(sms, l.t1 - l.t0));
@@ -3002,6 +3028,7 @@ tlr_status_t tlr_gemm_static_scratch(tlr_handle_t h, tlr_op_t opA, tlr_op_t opB,
   tb.pair = p.pair = choose_pair(pc, p.bn);
   tb.prep_pair = choose_prep_pair(pc, p.bn, tb.pair);
   tb.l1_pair = choose_l1_pair(pc, tb.prep_pair, tb.pair);
+  choose_prep_widths(tb);
   st = build_tables(pc, rects, narenas, ws, false, tb);
   if (st) return st;
   p.launches = tb.launches;

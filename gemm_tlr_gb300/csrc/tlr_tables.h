@@ -30,7 +30,8 @@ constexpr int kStageBytes = kSmemA + kSmemB;
 constexpr int kEpiGroups = TLR_EPI_GROUPS;   // epilogue warp groups; each stores every kEpiGroups-th 64-column block
 constexpr int kEpiThreads = 128 * kEpiGroups;
 constexpr int kThreads = 96 + kEpiThreads;   // warp 0 TMA, warp 1 MMA, warp 2 descriptors, then the epilogue
-constexpr int kTmemCols = 512;      // two accumulators of up to 256 fp32 columns
+constexpr int kTmemCols = 512;      // two accumulators of up to 256 fp32 columns, or four of 128
+constexpr int kMaxAcc = 4;          // accumulators in TMEM at most (tiles at most 128 wide)
 constexpr int kMaxSegs = 8;         // K segments per task
 constexpr int kRing = 8;            // task descriptors staged ahead in shared memory
 constexpr int kTicketBatch = 4;     // consecutive tickets a CTA (or CTA pair) claims at once
@@ -40,7 +41,7 @@ constexpr int kSignalBatch = 16;    // completion signals an epilogue warp may h
 constexpr int kSmemBytes = kStages * kStageBytes + kRing * kSlotBytes + 1024 /*align*/ + 512 /*barriers*/ +
                            4 * kEpiGroups * kEpiStageBytes;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-static_assert(8 * (2 * kStages + 6 + 2 * kRing) + 16 <= 512, "barrier area");
+static_assert(8 * (2 * kStages + 2 * kMaxAcc + 2 + 2 * kRing) + 16 <= 512, "barrier area");
 
 enum : uint32_t {
   kSegAMN = 1u,   // A operand MN-major (rows of its view are M); else K-major
