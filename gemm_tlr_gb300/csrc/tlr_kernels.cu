@@ -181,10 +181,6 @@ __device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void *tm
       : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l2(const void *ptr) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
-}
-
 // L2 policy for data written once and not read again in the launch (C): its
 // lines are the first candidates for eviction, ahead of operands still in use.
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -1007,21 +1003,6 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
       const Out o = sl.out;
       __syncwarp();
       if (lane == 0) mbar_arrive(sempty_bar(r));
-      if (o.kind == kOutC && p.beta != 0.f) {
-        // C is read by this warp's stores: bring its lines into L2 while the
-        // tile's MMAs run, so that the read-modify-write does not wait on DRAM
-        const int64_t d0 = __shfl_sync(0xffffffffu, drow, 0);
-        const bool rows_ok = __all_sync(0xffffffffu, valid && drow == d0 + lane);
-        for (int cc = 64 * grp; cc < ncols; cc += 64 * kEpiGroups) {
-          for (int h = 0; h < 64 && cc + h < ncols; h += 32) {
-            if (!o.trans) {   // column c of the warp's 32 contiguous rows: one 128-byte line
-              if (rows_ok && cc + h + lane < ncols) prefetch_l2(p.C + d0 + (col0 + cc + h + lane) * p.ldc);
-            } else if (valid) {   // this lane's tile row: a contiguous run of C's column drow
-              prefetch_l2(p.C + (col0 + cc + h) + drow * p.ldc);
-            }
-          }
-        }
-      }
       if (!ready(tfull_bar(acc), acc_phase)) flush();
       if (!wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p, 4, kCG2)) break;
       tc_fence_after();
