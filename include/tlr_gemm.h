@@ -226,11 +226,11 @@ tlr_status_t tlr_gemm(tlr_handle_t handle, tlr_op_t opA, tlr_op_t opB, float alp
  * memory while they run (an allocator that owns all free memory, or a loop
  * that must not stall on allocation).
  *   Setup: the first call on each device (that device current) looks up the
- *   array's device address with cudaGetSymbolAddress and keeps it; make that
- *   first call before any stream capture. After the device's context has been
- *   destroyed and re-created (cudaDeviceReset), the next call looks the
- *   address up again. The current device must be the handle's device (the one
- *   current at tlr_create), else TLR_STATUS_INVALID_ARG.
+ *   array's device address with cudaGetSymbolAddress and keeps it. After the
+ *   device's context has been destroyed and re-created (cudaDeviceReset), the
+ *   next call looks the address up again. The current device must be the
+ *   handle's device (the one current at tlr_create), else
+ *   TLR_STATUS_INVALID_ARG.
  *   Sharing: every call on a device, from any handle or thread, uses the same
  *   array. Calls must be ordered (one stream, or events between streams);
  *   overlapping calls race on the workspace and the counters and give wrong
