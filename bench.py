@@ -40,21 +40,20 @@ WORKLOAD = "large_var_rank_bf16_N32768_b1024"
 # capture. The figure belongs to the kernel sources it was taken with:
 # `sources_sha256` is their hash, and the bench reports null traffic once the
 # sources differ.
-TRAFFIC = {"sources_sha256": "7d38f860b2d7edfc28c55b7bb7bfc3aa9d36a058ba21a865e54d411ace4d66d8",
-           # final-product launch (CTA pairs), mean of four: 0.976 GB read + 1.022 GB written
-           "bytes_per_launch": 0.9764e9 + 1.0221e9,
-           # its operands once and C once: (T 3.354 + C 4.295 + U 0.105 + P^T 0.105 + Z 0.105
-           # + dense tiles 0.134 GB) over the four rectangles of the product
-           "algorithmic_bytes_per_launch": 8.098e9 / 4}
-# Algorithmic bytes of one product: inputs 0.553 GB, C 4.295 GB written, T 3.354 GB
-# written and read back, S^T 0.167 GB and P^T 0.105 GB written and read back.
-ALGORITHMIC_BYTES = 12.100e9
+TRAFFIC = {"sources_sha256": "9753659e5a0097acf14cf0be666cebd44dd363af5e77cadb0e0d92d23af38b7b",
+           # final-product launch (CTA pairs) of the default per-triple plan, one launch per
+           # product, from a capture at N = 16384 (0.810 GB read, 1.020 GB written) scaled
+           # to N = 32768: reads by the algorithmic reads (2.006 / 0.634 GB), writes by C (x4)
+           "bytes_per_launch": 2.563e9 + 4.082e9,
+           # its operands once and C once: terminal blocks T^R, T^L 1.662 GB, U 0.105,
+           # Z 0.105 and the diagonal tiles 0.134 GB read, C 4.295 GB written
+           "algorithmic_bytes_per_launch": 6.301e9}
 
 
-def recorded_traffic(main_workload: bool, scale_down: int):
+def recorded_traffic(main_workload: bool, scale_down: int, per_triple: bool):
     """The recorded DRAM bytes per final-product launch, or None unless they were
-    captured on this workload with the kernel sources as they are now."""
-    if not main_workload or scale_down != 1 or sources_sha256() != TRAFFIC["sources_sha256"]:
+    captured on this workload and plan with the kernel sources as they are now."""
+    if not (main_workload and per_triple) or scale_down != 1 or sources_sha256() != TRAFFIC["sources_sha256"]:
         return None
     return TRAFFIC["bytes_per_launch"]
 
@@ -593,9 +592,10 @@ def main():
         avg_ms = k_ms / k_n
         achieved = per_launch_flops / (avg_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak_used, "unit": "TFLOP/s",
-                "frac": achieved / peak_used, "traffic": recorded_traffic(main_workload, args.scale_down),
+                "frac": achieved / peak_used, "traffic": recorded_traffic(main_workload, args.scale_down, order == "per-triple"),
                 "traffic_unit": "bytes per launch (DRAM read + write)",
-                "algorithmic_bytes": TRAFFIC["algorithmic_bytes_per_launch"] if main_workload else None,
+                "algorithmic_bytes": (TRAFFIC["algorithmic_bytes_per_launch"]
+                                      if main_workload and args.scale_down == 1 and order == "per-triple" else None),
                 "kernel": names[dom] + " (executed FLOPs per launch / mean launch time)",
                 "launches_per_step": launches_per_step,
                 "peak_source": f"{peak_src} bf16 {which} (timed region {ms_total / 1e3:.2f} s: burst below 3 s, "

@@ -28,10 +28,15 @@ def test_clock_summary_reports_throttle_reasons_and_no_samples():
 def test_traffic_is_reported_only_for_the_sources_it_was_captured_with(monkeypatch):
     now = bench.sources_sha256()
     monkeypatch.setitem(bench.TRAFFIC, "sources_sha256", now)
-    assert bench.recorded_traffic(True, 1) == bench.TRAFFIC["bytes_per_launch"]
-    assert bench.recorded_traffic(False, 1) is None and bench.recorded_traffic(True, 2) is None
+    assert bench.recorded_traffic(True, 1, True) == bench.TRAFFIC["bytes_per_launch"]
+    assert bench.recorded_traffic(False, 1, True) is None and bench.recorded_traffic(True, 2, True) is None
+    assert bench.recorded_traffic(True, 1, False) is None      # captured on the per-triple plan only
     monkeypatch.setitem(bench.TRAFFIC, "sources_sha256", "0" * 64)
-    assert bench.recorded_traffic(True, 1) is None
+    assert bench.recorded_traffic(True, 1, True) is None
+
+
+def test_recorded_traffic_matches_the_current_kernel_sources():
+    assert bench.TRAFFIC["sources_sha256"] == bench.sources_sha256()
 
 
 def test_var_rank_grid_keeps_the_large_products_tiles():
