@@ -107,6 +107,13 @@ _SIGS = {
     "tlr_debug_check_plan": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _OP, _OP, ctypes.c_size_t, ctypes.c_int,
                                             ctypes.POINTER(tlr_plan_info_t), ctypes.c_char_p, ctypes.c_size_t]),
     "tlr_debug_unsatisfied_wait": (ctypes.c_int, [_P]),
+    "tlr_compress_workspace_bytes": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int64,
+                                                    ctypes.POINTER(ctypes.c_size_t)]),
+    "tlr_compress": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                    ctypes.c_int32, ctypes.c_float, ctypes.c_int32, _P, ctypes.c_int32,
+                                    _P, _P, _P, _P, _P, _P, ctypes.c_size_t]),
+    "tlr_pack": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P,
+                                _P, _P, _P, _P, _P]),
 }
 
 _lib = None
@@ -286,3 +293,24 @@ def tlr_debug_check_plan(opA: int, opB: int, A: tlr_operand_t, B: tlr_operand_t,
     st = lib().tlr_debug_check_plan(opA, opB, ctypes.byref(A), ctypes.byref(B), ws_bytes, order,
                                     ctypes.byref(info), msg, 512)
     return st, msg.value.decode(), _info_dict(info)
+
+
+def tlr_compress_workspace_bytes(b: int, s: int, tiles: int) -> int:
+    n = ctypes.c_size_t()
+    check(lib().tlr_compress_workspace_bytes(b, s, tiles, ctypes.byref(n)), "tlr_compress_workspace_bytes")
+    return n.value
+
+
+def tlr_compress(h: int, C: int, ldc: int, m: int, n: int, b: int, dense_diagonal: bool, eps: float, r_max: int,
+                 omega: int, s: int, U: int, V: int, D: int, ranks: int, errors: int, ws: int, ws_bytes: int) -> None:
+    check(lib().tlr_compress(_P(h), _P(C), ldc, m, n, b, 1 if dense_diagonal else 0, eps, r_max, _P(omega), s,
+                             _P(U), _P(V), _P(D), _P(ranks), _P(errors), _P(ws), ws_bytes), "tlr_compress")
+
+
+def tlr_pack(h: int, n: int, b: int, r_max: int, ranks_host, U_pad: int, V_pad: int, D_pad: int, U: int, V: int,
+             D: int, bu_U: int, bu_V: int, bv_U: int, bv_V: int, gamma: int) -> None:
+    """ranks_host: a C-contiguous int32 numpy array of the nt x nt ranks."""
+    import numpy as np
+    r = np.ascontiguousarray(ranks_host, dtype=np.int32)
+    check(lib().tlr_pack(_P(h), n, b, r_max, _P(r.ctypes.data), _P(U_pad), _P(V_pad), _P(D_pad), _P(U), _P(V),
+                         _P(D), _P(bu_U), _P(bu_V), _P(bv_U), _P(bv_V), _P(gamma)), "tlr_pack")

@@ -1,7 +1,8 @@
 """Build the sm_103a shared library ``libtlrgemm.so`` in-tree with nvcc.
 
-The two translation units (kernels, host planner) compile in parallel; the
-library links the CUDA runtime statically, so it loads next to any PyTorch.
+The three translation units (task kernel, host planner, recompression) compile
+in parallel; the library links the CUDA runtime statically, so it loads next to
+any PyTorch.
 """
 from __future__ import annotations
 
@@ -16,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libtlrgemm.so")
-SOURCES = ["tlr_kernels.cu", "tlr_plan.cu"]
+SOURCES = ["tlr_kernels.cu", "tlr_plan.cu", "tlr_compress.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

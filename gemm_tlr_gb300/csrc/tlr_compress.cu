@@ -1,0 +1,643 @@
+// Recompression of a dense matrix into TLR form: the step the TLR-output
+// products add after the dense-output product ("TLR Matrix Multiplication",
+// section "Introduction: TLR GEMM", names the TLR-output cases; "Tile-Low-Rank
+// GEMM: Designing Storage Around the Contraction", section "Many small GEMMs",
+// gives the format: each tile of a regular grid compressed on its own, its
+// rank following its own compressibility). Neither page describes the
+// recompression; the rule taken here is the truncated singular value
+// decomposition of every off-diagonal tile with the smallest rank r whose
+// discarded part is at most eps times the tile's Frobenius norm, capped at
+// r_max.
+//
+// Per tile T (d_i x d_j, fp32), all in fp32 with the energies in fp64:
+//   1. ||T||_F^2;
+//   2. Y = T Omega, a sketch with s columns (randomized range finder of Halko,
+//      Martinsson and Tropp, 2011; Omega is an input, drawn by the caller);
+//   3. Q = an orthonormal basis of Y, classical Gram-Schmidt with one
+//      reorthogonalisation (Giraud, Langou and Rozloznik, 2005);
+//   4. B = Q^T T (s x d_j) and the core G = B B^T (s x s, fp64 accumulation
+//      across blocks of 16 products);
+//   5. G = W diag(lambda) W^T by the cyclic Jacobi method (two-sided
+//      rotations, round-robin pair order; Golub and Van Loan, "Matrix
+//      Computations", section 8.5), eigenvalues sorted in decreasing order:
+//      lambda_k are the squared singular values of B;
+//   6. r = the smallest rank with ||T||^2 - sum_{k<r} lambda_k <= eps^2 ||T||^2
+//      (the energy left out of U V^T below, including what the sketch missed),
+//      at most min(r_max, d_i, d_j, s);
+//   7. U = Q W_r (d_i x r, orthonormal columns) and V = B^T W_r (d_j x r), so
+//      that U V^T = Q W_r W_r^T Q^T T.
+// When the sketch holds the tile's range (s above its numerical rank) this is
+// the truncated SVD up to rounding; otherwise the rank may exceed the optimal
+// one and the error stays within eps (or is reported when r_max caps it).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "tlr_gemm.h"
+
+namespace tlr {
+// handle access (tlr_plan.cu)
+cudaStream_t handle_stream(tlr_handle_t h);
+bool handle_on_current_device(tlr_handle_t h);
+bool is_device_pointer(const void *p);
+}
+
+namespace tlr_cmp {
+
+constexpr int kMaxSketch = 128;   // columns of the sketch (the core fits in shared memory)
+constexpr int kThreads = 256;
+
+struct Geo {
+  int64_t m, n, b;
+  int32_t nI, nJ;
+  int32_t dense_diag;
+  int32_t s, r_max;
+  float eps;
+};
+
+__device__ __forceinline__ int64_t tile_dim(int64_t total, int64_t b, int64_t t) {
+  const int64_t d = total - t * b;
+  return d < b ? d : b;
+}
+
+// Per-tile scratch of one batch: Y/Q (b x s, ld b), B (s x b, ld s), G (s x s),
+// W sorted (s x s), eigenvalues (s), the tile energy (fp64).
+struct Scratch {
+  float *Q, *B, *G, *W, *lam;
+  double *norm2;
+  int64_t q_stride, b_stride, g_stride;   // elements per tile
+};
+
+__device__ __forceinline__ bool is_dense_tile(const Geo &g, int64_t i, int64_t j) {
+  return g.dense_diag && i == j;
+}
+
+// ---------------------------------------------------------------- tile energy
+__global__ void __launch_bounds__(kThreads) norm_kernel(const float *C, int64_t ldc, Geo g, int64_t t0, Scratch w) {
+  const int64_t t = t0 + blockIdx.x;
+  const int64_t i = t / g.nJ, j = t % g.nJ;
+  const int64_t di = tile_dim(g.m, g.b, i), dj = tile_dim(g.n, g.b, j);
+  double acc = 0.0;
+  if (!is_dense_tile(g, i, j)) {
+    const float *T = C + i * g.b + j * g.b * ldc;
+    for (int64_t c = 0; c < dj; ++c)
+      for (int64_t r = threadIdx.x; r < di; r += blockDim.x) {
+        const double x = T[r + c * ldc];
+        acc += x * x;
+      }
+  }
+  __shared__ double red[kThreads / 32];
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+    for (int k = 0; k < kThreads / 32; ++k) s += red[k];
+    w.norm2[blockIdx.x] = s;
+  }
+}
+
+// ---------------------------------------------------------------- batched SIMT GEMM
+// out(r, c) = sum_k A(r, k) B(k, c) for one 64 x 64 block of one tile; each of
+// the 256 threads holds 4 x 4 results. kAk / kBk: the operand's contiguous
+// index is k (else r for A, c for B), which decides the loading order so that
+// neighbouring threads read neighbouring addresses. kWide: partial sums of 16
+// products in fp32 are added into fp64 accumulators.
+template <bool kAk, bool kBk, bool kWide, class LA, class LB, class ST>
+__device__ __forceinline__ void gemm_block(int64_t M, int64_t N, int64_t K, int64_t m0, int64_t n0, LA la, LB lb,
+                                           ST st) {
+  __shared__ float As[16][64 + 4];
+  __shared__ float Bs[16][64 + 4];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  float acc[4][4];
+  double wacc[kWide ? 4 : 1][kWide ? 4 : 1];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
+  if constexpr (kWide) {
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) wacc[a][c] = 0.0;
+  }
+  for (int64_t k0 = 0; k0 < K; k0 += 16) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int idx = tid + kThreads * q;   // 0 .. 1023
+      const int r = kAk ? idx >> 4 : idx & 63, k = kAk ? idx & 15 : idx >> 6;
+      const int64_t gr = m0 + r, gk = k0 + k;
+      As[k][r] = gr < M && gk < K ? la(gr, gk) : 0.f;
+      const int c = kBk ? idx >> 4 : idx & 63, kb = kBk ? idx & 15 : idx >> 6;
+      const int64_t gc = n0 + c, gkb = k0 + kb;
+      Bs[kb][c] = gc < N && gkb < K ? lb(gkb, gc) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      float a[4], bb[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) a[x] = As[k][ty * 4 + x];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) bb[x] = Bs[k][tx * 4 + x];
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(a[x], bb[y], acc[x][y]);
+    }
+    if constexpr (kWide) {
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) { wacc[x][y] += acc[x][y]; acc[x][y] = 0.f; }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y) {
+      const int64_t r = m0 + ty * 4 + x, c = n0 + tx * 4 + y;
+      if (r < M && c < N) {
+        if constexpr (kWide) st(r, c, static_cast<float>(wacc[x][y]));
+        else st(r, c, acc[x][y]);
+      }
+    }
+}
+
+// Y = T Omega (d_i x s)
+__global__ void __launch_bounds__(kThreads) sketch_kernel(const float *C, int64_t ldc, const float *omega, Geo g,
+                                                          int64_t t0, Scratch w) {
+  const int64_t t = t0 + blockIdx.z;
+  const int64_t i = t / g.nJ, j = t % g.nJ;
+  if (is_dense_tile(g, i, j)) return;
+  const int64_t di = tile_dim(g.m, g.b, i), dj = tile_dim(g.n, g.b, j);
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * 64, n0 = static_cast<int64_t>(blockIdx.y) * 64;
+  if (m0 >= di || n0 >= g.s) return;
+  const float *T = C + i * g.b + j * g.b * ldc;
+  float *Y = w.Q + blockIdx.z * w.q_stride;
+  const int64_t b = g.b;
+  gemm_block<false, true, false>(
+      di, g.s, dj, m0, n0, [&](int64_t r, int64_t k) { return T[r + k * ldc]; },
+      [&](int64_t k, int64_t c) { return omega[k + c * b]; }, [&](int64_t r, int64_t c, float v) { Y[r + c * b] = v; });
+}
+
+// B = Q^T T (s x d_j, ld s)
+__global__ void __launch_bounds__(kThreads) project_kernel(const float *C, int64_t ldc, Geo g, int64_t t0, Scratch w) {
+  const int64_t t = t0 + blockIdx.z;
+  const int64_t i = t / g.nJ, j = t % g.nJ;
+  if (is_dense_tile(g, i, j)) return;
+  const int64_t di = tile_dim(g.m, g.b, i), dj = tile_dim(g.n, g.b, j);
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * 64, n0 = static_cast<int64_t>(blockIdx.y) * 64;
+  if (m0 >= g.s || n0 >= dj) return;
+  const float *T = C + i * g.b + j * g.b * ldc;
+  const float *Q = w.Q + blockIdx.z * w.q_stride;
+  float *B = w.B + blockIdx.z * w.b_stride;
+  const int64_t b = g.b, s = g.s;
+  gemm_block<true, true, true>(
+      g.s, dj, di, m0, n0, [&](int64_t r, int64_t k) { return Q[k + r * b]; },
+      [&](int64_t k, int64_t c) { return T[k + c * ldc]; }, [&](int64_t r, int64_t c, float v) { B[r + c * s] = v; });
+}
+
+// G = B B^T (s x s)
+__global__ void __launch_bounds__(kThreads) core_kernel(Geo g, int64_t t0, Scratch w) {
+  const int64_t t = t0 + blockIdx.z;
+  const int64_t i = t / g.nJ, j = t % g.nJ;
+  if (is_dense_tile(g, i, j)) return;
+  const int64_t dj = tile_dim(g.n, g.b, j);
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * 64, n0 = static_cast<int64_t>(blockIdx.y) * 64;
+  const float *B = w.B + blockIdx.z * w.b_stride;
+  float *G = w.G + blockIdx.z * w.g_stride;
+  const int64_t s = g.s;
+  gemm_block<false, false, true>(
+      s, s, dj, m0, n0, [&](int64_t r, int64_t k) { return B[r + k * s]; },
+      [&](int64_t k, int64_t c) { return B[c + k * s]; }, [&](int64_t r, int64_t c, float v) { G[r + c * s] = v; });
+}
+
+// U = Q W (d_i x r_max) and V = B^T W (d_j x r_max), W with its columns from
+// the rank on set to zero; written at the tile's place in the padded outputs.
+__global__ void __launch_bounds__(kThreads) factor_kernel(Geo g, int64_t t0, Scratch w, float *Uo, float *Vo,
+                                                          int which) {
+  const int64_t t = t0 + blockIdx.z;
+  const int64_t i = t / g.nJ, j = t % g.nJ;
+  if (is_dense_tile(g, i, j)) return;
+  const int64_t di = tile_dim(g.m, g.b, i), dj = tile_dim(g.n, g.b, j);
+  const int64_t rows = which == 0 ? di : dj;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * 64, n0 = static_cast<int64_t>(blockIdx.y) * 64;
+  if (m0 >= rows || n0 >= g.r_max) return;
+  const float *W = w.W + blockIdx.z * w.g_stride;
+  const int64_t b = g.b, s = g.s;
+  float *out = (which == 0 ? Uo : Vo) + t * b * g.r_max;
+  auto st = [&](int64_t r, int64_t c, float v) { out[r + c * b] = v; };
+  auto lw = [&](int64_t k, int64_t c) { return W[k + c * s]; };
+  if (which == 0) {
+    const float *Q = w.Q + blockIdx.z * w.q_stride;
+    gemm_block<false, true, false>(di, g.r_max, s, m0, n0, [&](int64_t r, int64_t k) { return Q[r + k * b]; }, lw, st);
+  } else {
+    const float *B = w.B + blockIdx.z * w.b_stride;
+    gemm_block<true, true, false>(dj, g.r_max, s, m0, n0, [&](int64_t r, int64_t k) { return B[k + r * s]; }, lw, st);
+  }
+}
+
+// ---------------------------------------------------------------- orthonormal basis
+// Classical Gram-Schmidt with one reorthogonalisation, column by column, in
+// place on Y (d_i x s). A column whose remainder after both passes is below
+// 1e-5 of its own norm adds no direction the others do not hold to within
+// fp32 rounding (there the second pass cannot restore orthogonality): it
+// becomes zero, and its eigenvalue in the core is zero.
+__global__ void __launch_bounds__(kThreads) orth_kernel(Geo g, int64_t t0, Scratch w) {
+  const int64_t t = t0 + blockIdx.x;
+  const int64_t i = t / g.nJ, j = t % g.nJ;
+  if (is_dense_tile(g, i, j)) return;
+  const int64_t di = tile_dim(g.m, g.b, i);
+  float *Q = w.Q + blockIdx.x * w.q_stride;
+  const int64_t b = g.b;
+  extern __shared__ float sm[];
+  float *y = sm;                       // the current column (d_i <= b)
+  float *coef = sm + b;                // kMaxSketch projections
+  __shared__ float red[kThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  auto sum_sq = [&]() {                // sum of y^2 over the block (every thread gets it)
+    float a = 0.f;
+    for (int64_t r = threadIdx.x; r < di; r += blockDim.x) a = fmaf(y[r], y[r], a);
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    if (lane == 0) red[warp] = a;
+    __syncthreads();
+    float tot = 0.f;
+    for (int k = 0; k < kThreads / 32; ++k) tot += red[k];
+    __syncthreads();                   // red is reused by the next call
+    return tot;
+  };
+  for (int c = 0; c < g.s; ++c) {
+    for (int64_t r = threadIdx.x; r < di; r += blockDim.x) y[r] = Q[r + c * b];
+    __syncthreads();
+    const float orig2 = sum_sq();
+    for (int pass = 0; pass < 2; ++pass) {
+      for (int k = warp; k < c; k += kThreads / 32) {
+        float a = 0.f;
+        for (int64_t r = lane; r < di; r += 32) a = fmaf(Q[r + k * b], y[r], a);
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane == 0) coef[k] = a;
+      }
+      __syncthreads();
+      for (int64_t r = threadIdx.x; r < di; r += blockDim.x) {
+        float v = y[r];
+        for (int k = 0; k < c; ++k) v = fmaf(-coef[k], Q[r + k * b], v);
+        y[r] = v;
+      }
+      __syncthreads();
+    }
+    const float nrm2 = sum_sq();
+    const float inv = nrm2 > 1e-10f * orig2 && nrm2 > 1e-36f ? rsqrtf(nrm2) : 0.f;
+    for (int64_t r = threadIdx.x; r < di; r += blockDim.x) Q[r + c * b] = y[r] * inv;
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- eigen-decomposition of the core
+// Cyclic Jacobi on G (s x s, s even) in shared memory, rows padded to s + 1
+// floats. Each sweep runs s - 1 rounds of s/2 disjoint pairs (round-robin
+// tournament: position 0 fixed, the others rotate); a round computes every
+// pair's rotation, applies all of them to the rows (J^T G), then to the
+// columns (G J) and to the accumulated eigenvectors (W J).
+__global__ void __launch_bounds__(kThreads) eig_kernel(Geo g, int64_t t0, Scratch w, int32_t *ranks, float *errors) {
+  const int64_t t = t0 + blockIdx.x;
+  const int64_t i = t / g.nJ, j = t % g.nJ;
+  if (is_dense_tile(g, i, j)) {
+    if (threadIdx.x == 0) { ranks[t] = 0; errors[t] = 0.f; }
+    return;
+  }
+  const int s = g.s, ps = s + 1;
+  extern __shared__ float sm[];
+  float *G = sm;                      // s x ps
+  float *W = G + s * ps;              // s x ps
+  float *cs = W + s * ps;             // s/2 cosines
+  float *sn = cs + s / 2;             // s/2 sines
+  int *pp = reinterpret_cast<int *>(sn + s / 2), *pq = pp + s / 2;
+  float *lam = reinterpret_cast<float *>(pq + s / 2);   // s
+  int *order = reinterpret_cast<int *>(lam + s);        // s
+  const float *Gg = w.G + blockIdx.x * w.g_stride;
+  for (int e = threadIdx.x; e < s * s; e += blockDim.x) {
+    const int r = e % s, c = e / s;
+    G[r * ps + c] = Gg[r + c * s];
+    W[r * ps + c] = r == c ? 1.f : 0.f;
+  }
+  __syncthreads();
+  __shared__ int rotated;
+  for (int sweep = 0; sweep < 30; ++sweep) {
+    // threshold Jacobi: a pair is rotated only while its off-diagonal entry is
+    // above 1e-6 sqrt(|G_pp G_qq|) and above the rounding level of its larger
+    // diagonal entry; the sweeps end when one rotates nothing
+    if (threadIdx.x == 0) rotated = 0;
+    __syncthreads();
+    for (int round = 0; round < s - 1; ++round) {
+      if (threadIdx.x < s / 2) {
+        const int k = threadIdx.x;
+        auto pos = [&](int x) { return x == 0 ? 0 : 1 + (x - 1 + round) % (s - 1); };
+        int p = pos(k), q = pos(s - 1 - k);
+        if (p > q) { const int tmp = p; p = q; q = tmp; }
+        const float a = G[p * ps + p], d = G[q * ps + q], o = G[p * ps + q];
+        float c = 1.f, sv = 0.f;
+        const float ao = fabsf(o);
+        if (ao > 1e-6f * sqrtf(fabsf(a)) * sqrtf(fabsf(d)) && ao > 1e-7f * fmaxf(fabsf(a), fabsf(d)) && ao > 1e-35f) {
+          rotated = 1;
+          // symmetric 2 x 2 Schur decomposition: t = tan(theta) with the smaller angle
+          const float tau = (d - a) / (2.f * o);
+          const float tt = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
+          c = rsqrtf(1.f + tt * tt);
+          sv = tt * c;
+        }
+        cs[k] = c; sn[k] = sv; pp[k] = p; pq[k] = q;
+      }
+      __syncthreads();
+      const int half = s / 2;
+      for (int e = threadIdx.x; e < half * s; e += blockDim.x) {   // rows p, q of G
+        const int k = e / s, col = e % s;
+        const int p = pp[k], q = pq[k];
+        const float c = cs[k], sv = sn[k];
+        const float gp = G[p * ps + col], gq = G[q * ps + col];
+        G[p * ps + col] = c * gp - sv * gq;
+        G[q * ps + col] = sv * gp + c * gq;
+      }
+      __syncthreads();
+      for (int e = threadIdx.x; e < half * s; e += blockDim.x) {   // columns p, q of G and W
+        const int k = e % half, row = e / half;
+        const int p = pp[k], q = pq[k];
+        const float c = cs[k], sv = sn[k];
+        const float gp = G[row * ps + p], gq = G[row * ps + q];
+        G[row * ps + p] = c * gp - sv * gq;
+        G[row * ps + q] = sv * gp + c * gq;
+        const float wp = W[row * ps + p], wq = W[row * ps + q];
+        W[row * ps + p] = c * wp - sv * wq;
+        W[row * ps + q] = sv * wp + c * wq;
+      }
+      __syncthreads();
+    }
+    const int any = rotated;
+    __syncthreads();   // every thread has read the flag before it is reset
+    if (!any) break;
+  }
+  // eigenvalues (clamped at zero: the core is a Gram matrix) and their order
+  for (int k = threadIdx.x; k < s; k += blockDim.x) lam[k] = fmaxf(G[k * ps + k], 0.f);
+  __syncthreads();
+  for (int k = threadIdx.x; k < s; k += blockDim.x) {
+    int pos = 0;
+    for (int q = 0; q < s; ++q) pos += lam[q] > lam[k] || (lam[q] == lam[k] && q < k);
+    order[pos] = k;
+  }
+  __syncthreads();
+  __shared__ int rank_s;
+  if (threadIdx.x == 0) {
+    const int64_t di = tile_dim(g.m, g.b, i), dj = tile_dim(g.n, g.b, j);
+    int64_t cap = g.r_max;
+    if (di < cap) cap = di;
+    if (dj < cap) cap = dj;
+    if (s < cap) cap = s;
+    const double total = w.norm2[blockIdx.x];
+    const double bound = static_cast<double>(g.eps) * static_cast<double>(g.eps) * total;
+    double kept = 0.0;
+    int r = 0;
+    double tail = total;
+    if (total > 0.0) {
+      while (r < cap && tail > bound) {
+        kept += lam[order[r]];
+        ++r;
+        tail = total - kept;
+      }
+    }
+    if (tail < 0.0) tail = 0.0;
+    ranks[t] = r;
+    errors[t] = total > 0.0 ? static_cast<float>(sqrt(tail / total)) : 0.f;
+    rank_s = r;
+  }
+  __syncthreads();
+  const int r = rank_s;
+  float *Wo = w.W + blockIdx.x * w.g_stride;
+  float *lo = w.lam + blockIdx.x * static_cast<int64_t>(kMaxSketch);
+  for (int e = threadIdx.x; e < s * s; e += blockDim.x) {
+    const int row = e % s, k = e / s;
+    Wo[row + k * s] = k < r ? W[row * ps + order[k]] : 0.f;
+  }
+  for (int k = threadIdx.x; k < s; k += blockDim.x) lo[k] = lam[order[k]];
+}
+
+// ---------------------------------------------------------------- dense tiles
+__global__ void dense_copy_kernel(const float *C, int64_t ldc, Geo g, float *D) {
+  const int64_t t = blockIdx.y;   // diagonal tile t
+  const int64_t d = tile_dim(g.m, g.b, t);
+  const float *T = C + t * g.b + t * g.b * ldc;
+  float *o = D + t * g.b * g.b;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < d * d;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = e % d, c = e / d;
+    o[r + c * g.b] = T[r + c * ldc];
+  }
+}
+
+// ---------------------------------------------------------------- packing
+struct CopyJob {
+  const float *src;
+  float *dst;
+  int64_t rows, cols, src_ld, dst_ld;
+};
+
+__global__ void copy_jobs_kernel(const CopyJob *jobs, int njobs) {
+  for (int jb = blockIdx.y; jb < njobs; jb += gridDim.y) {
+    const CopyJob J = jobs[jb];
+    const int64_t n = J.rows * J.cols;
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const int64_t r = e % J.rows, c = e / J.rows;
+      J.dst[r + c * J.dst_ld] = J.src[r + c * J.src_ld];
+    }
+  }
+}
+
+size_t eig_smem(int s) {
+  const int ps = s + 1;
+  return static_cast<size_t>(2 * s * ps + s + 2 * s + s + s) * 4;
+}
+
+}  // namespace tlr_cmp
+
+using namespace tlr_cmp;
+
+extern "C" {
+
+tlr_status_t tlr_compress_workspace_bytes(int64_t b, int32_t s, int64_t tiles, size_t *bytes) {
+  if (!bytes || b <= 0 || s <= 0 || tiles < 0) return TLR_STATUS_INVALID_ARG;
+  const int64_t per = (2 * b * s + 2 * static_cast<int64_t>(s) * s + kMaxSketch) * 4 + 8;
+  *bytes = static_cast<size_t>(per * std::max<int64_t>(tiles, 1) + 1024);
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_compress(tlr_handle_t h, const float *C, int64_t ldc, int64_t m, int64_t n, int64_t b,
+                          int32_t dense_diagonal, float eps, int32_t r_max, const float *omega, int32_t s,
+                          float *U, float *V, float *D, int32_t *ranks, float *errors, void *workspace,
+                          size_t workspace_bytes) {
+  if (!h) return TLR_STATUS_INVALID_ARG;
+  if (m < 0 || n < 0 || b <= 0 || b > (1 << 20) || ldc < std::max<int64_t>(m, 1)) return TLR_STATUS_INVALID_ARG;
+  if (s < 2 || s > kMaxSketch || (s & 1) || r_max < 0 || r_max > s) return TLR_STATUS_INVALID_ARG;
+  if (!(eps >= 0.f) || !(eps < 1e30f)) return TLR_STATUS_INVALID_ARG;
+  if (dense_diagonal && m != n) return TLR_STATUS_INVALID_ARG;
+  if (m == 0 || n == 0) return TLR_STATUS_OK;
+  if (!tlr::handle_on_current_device(h)) return TLR_STATUS_INVALID_ARG;
+  const int64_t nI = (m + b - 1) / b, nJ = (n + b - 1) / b;
+  if (nI * nJ > (int64_t(1) << 31)) return TLR_STATUS_INVALID_ARG;
+  const bool need_f = r_max > 0 && !(dense_diagonal && nI == 1);
+  if (!C || !omega || !ranks || !errors || !workspace || (need_f && (!U || !V)) || (dense_diagonal && !D))
+    return TLR_STATUS_INVALID_ARG;
+  const void *need[5] = {C, omega, ranks, errors, workspace};
+  for (const void *p : need)
+    if (!tlr::is_device_pointer(p)) return TLR_STATUS_INVALID_ARG;
+  if ((need_f && (!tlr::is_device_pointer(U) || !tlr::is_device_pointer(V))) ||
+      (dense_diagonal && !tlr::is_device_pointer(D)))
+    return TLR_STATUS_INVALID_ARG;
+  size_t per1 = 0;
+  tlr_compress_workspace_bytes(b, s, 1, &per1);
+  const int64_t per = static_cast<int64_t>(per1) - 1024;
+  const int64_t ntiles = nI * nJ;
+  const int64_t batch = std::min<int64_t>(ntiles, (static_cast<int64_t>(workspace_bytes) - 1024) / per);
+  if (batch < 1) return TLR_STATUS_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = tlr::handle_stream(h);
+
+  Geo g;
+  g.m = m; g.n = n; g.b = b;
+  g.nI = static_cast<int32_t>(nI); g.nJ = static_cast<int32_t>(nJ);
+  g.dense_diag = dense_diagonal ? 1 : 0;
+  g.s = s; g.r_max = r_max; g.eps = eps;
+
+  // scratch of one batch, 256-byte aligned pieces
+  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255));
+  Scratch w;
+  w.q_stride = b * s;
+  w.b_stride = static_cast<int64_t>(s) * b;
+  w.g_stride = static_cast<int64_t>(s) * s;
+  w.Q = reinterpret_cast<float *>(base);
+  w.B = w.Q + batch * w.q_stride;
+  w.G = w.B + batch * w.b_stride;
+  w.W = w.G + batch * w.g_stride;
+  w.lam = w.W + batch * w.g_stride;
+  w.norm2 = reinterpret_cast<double *>(
+      (reinterpret_cast<uintptr_t>(w.lam + batch * kMaxSketch) + 7) & ~uintptr_t(7));
+  if (reinterpret_cast<uint8_t *>(w.norm2 + batch) > reinterpret_cast<uint8_t *>(workspace) + workspace_bytes)
+    return TLR_STATUS_WORKSPACE_TOO_SMALL;
+
+  const size_t esm = eig_smem(s);
+  if (cudaFuncSetAttribute(eig_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(esm)) !=
+      cudaSuccess)
+    return TLR_STATUS_CUDA_ERROR;
+  const size_t osm = static_cast<size_t>(b + kMaxSketch) * 4;
+  if (osm > 227 * 1024) return TLR_STATUS_UNSUPPORTED;
+  if (osm > 48 * 1024 &&
+      cudaFuncSetAttribute(orth_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(osm)) !=
+          cudaSuccess)
+    return TLR_STATUS_CUDA_ERROR;
+
+  const unsigned bm = static_cast<unsigned>((b + 63) / 64), sm64 = static_cast<unsigned>((s + 63) / 64);
+  const unsigned rm64 = static_cast<unsigned>((std::max(r_max, 1) + 63) / 64);
+  for (int64_t t0 = 0; t0 < ntiles; t0 += batch) {
+    const unsigned nb = static_cast<unsigned>(std::min<int64_t>(batch, ntiles - t0));
+    norm_kernel<<<nb, kThreads, 0, st>>>(C, ldc, g, t0, w);
+    sketch_kernel<<<dim3(bm, sm64, nb), kThreads, 0, st>>>(C, ldc, omega, g, t0, w);
+    orth_kernel<<<nb, kThreads, osm, st>>>(g, t0, w);
+    project_kernel<<<dim3(sm64, bm, nb), kThreads, 0, st>>>(C, ldc, g, t0, w);
+    core_kernel<<<dim3(sm64, sm64, nb), kThreads, 0, st>>>(g, t0, w);
+    eig_kernel<<<nb, kThreads, esm, st>>>(g, t0, w, ranks, errors);
+    if (r_max > 0) {
+      factor_kernel<<<dim3(bm, rm64, nb), kThreads, 0, st>>>(g, t0, w, U, V, 0);
+      factor_kernel<<<dim3(bm, rm64, nb), kThreads, 0, st>>>(g, t0, w, U, V, 1);
+    }
+    if (cudaGetLastError() != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+  }
+  if (dense_diagonal) {
+    dense_copy_kernel<<<dim3(64, static_cast<unsigned>(nI)), kThreads, 0, st>>>(C, ldc, g, D);
+    if (cudaGetLastError() != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+  }
+  return TLR_STATUS_OK;
+}
+
+tlr_status_t tlr_pack(tlr_handle_t h, int64_t n, int64_t b, int32_t r_max, const int32_t *ranks, const float *U_pad,
+                      const float *V_pad, const float *D_pad, float *U, float *V, float *D, float *bu_U, float *bu_V,
+                      float *bv_U, float *bv_V, float *gamma) {
+  if (!h || !ranks || n <= 0 || b <= 0 || r_max < 0) return TLR_STATUS_INVALID_ARG;
+  if (!tlr::handle_on_current_device(h)) return TLR_STATUS_INVALID_ARG;
+  const int64_t mf = n / b, rem = n % b, nt = (n + b - 1) / b;
+  bool lowrank = false, boundary_col = false, boundary_row = false;
+  for (int64_t t = 0; t < nt * nt; ++t) {
+    const int64_t i = t / nt, k = t % nt;
+    if (ranks[t] < 0 || ranks[t] > r_max || (i == k && ranks[t] != 0)) return TLR_STATUS_INVALID_ARG;
+    if (ranks[t] > 0) {
+      lowrank = true;
+      if (rem > 0 && k == mf) boundary_col = true;
+      if (rem > 0 && i == mf) boundary_row = true;
+    }
+  }
+  // every buffer a copy reads or writes must be there before any address is formed
+  if (lowrank && (!U_pad || !V_pad)) return TLR_STATUS_INVALID_ARG;
+  if (mf > 0 && (!D_pad || !D)) return TLR_STATUS_INVALID_ARG;
+  if (rem > 0 && (!D_pad || !gamma)) return TLR_STATUS_INVALID_ARG;
+  if (boundary_col && (!bu_U || !bu_V)) return TLR_STATUS_INVALID_ARG;
+  if (boundary_row && (!bv_U || !bv_V)) return TLR_STATUS_INVALID_ARG;
+  bool interior = false;
+  for (int64_t i = 0; i < mf; ++i)
+    for (int64_t k = 0; k < mf; ++k) interior = interior || ranks[i * nt + k] > 0;
+  if (interior && (!U || !V)) return TLR_STATUS_INVALID_ARG;
+  std::vector<CopyJob> jobs;
+  auto add = [&](const float *src, float *dst, int64_t rows, int64_t cols, int64_t sld, int64_t dld) {
+    if (rows > 0 && cols > 0) jobs.push_back(CopyJob{src, dst, rows, cols, sld, dld});
+  };
+  auto rk = [&](int64_t i, int64_t k) { return static_cast<int64_t>(ranks[i * nt + k]); };
+  auto padU = [&](int64_t i, int64_t k) { return U_pad + (i * nt + k) * b * r_max; };
+  auto padV = [&](int64_t i, int64_t k) { return V_pad + (i * nt + k) * b * r_max; };
+  // interior: U by tile row, V by tile column
+  int64_t off = 0;
+  for (int64_t i = 0; i < mf; ++i)
+    for (int64_t k = 0; k < mf; ++k)
+      if (i != k && rk(i, k) > 0) { add(padU(i, k), U + off, b, rk(i, k), b, b); off += b * rk(i, k); }
+  off = 0;
+  for (int64_t k = 0; k < mf; ++k)
+    for (int64_t i = 0; i < mf; ++i)
+      if (i != k && rk(i, k) > 0) { add(padV(i, k), V + off, b, rk(i, k), b, b); off += b * rk(i, k); }
+  for (int64_t t = 0; t < mf; ++t) add(D_pad + t * b * b, D + t * b * b, b, b, b, b);
+  if (rem > 0) {
+    int64_t ou = 0, ov = 0;
+    for (int64_t i = 0; i < mf; ++i) {   // boundary column: tiles (i, mf)
+      const int64_t r = rk(i, mf);
+      if (r == 0) continue;
+      add(padU(i, mf), bu_U + ou, b, r, b, b);
+      add(padV(i, mf), bu_V + ov, rem, r, b, rem);
+      ou += b * r; ov += rem * r;
+    }
+    ou = 0; ov = 0;
+    for (int64_t j = 0; j < mf; ++j) {   // boundary row: tiles (mf, j)
+      const int64_t r = rk(mf, j);
+      if (r == 0) continue;
+      add(padU(mf, j), bv_U + ou, rem, r, b, rem);
+      add(padV(mf, j), bv_V + ov, b, r, b, b);
+      ou += rem * r; ov += b * r;
+    }
+    add(D_pad + mf * b * b, gamma, rem, rem, b, rem);
+  }
+  for (const CopyJob &J : jobs)
+    if (!J.dst || !J.src || !tlr::is_device_pointer(J.dst) || !tlr::is_device_pointer(J.src))
+      return TLR_STATUS_INVALID_ARG;
+  if (jobs.empty()) return TLR_STATUS_OK;
+  cudaStream_t st = tlr::handle_stream(h);
+  CopyJob *dj = nullptr;
+  const size_t bytes = jobs.size() * sizeof(CopyJob);
+  if (cudaMallocAsync(reinterpret_cast<void **>(&dj), bytes, st) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+  // from pageable memory: the call returns once the jobs are staged
+  if (cudaMemcpyAsync(dj, jobs.data(), bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
+  copy_jobs_kernel<<<dim3(16, static_cast<unsigned>(std::min<size_t>(jobs.size(), 65535))), kThreads, 0, st>>>(
+      dj, static_cast<int>(jobs.size()));
+  const bool ok = cudaGetLastError() == cudaSuccess;
+  cudaFreeAsync(dj, st);
+  return ok ? TLR_STATUS_OK : TLR_STATUS_CUDA_ERROR;
+}
+
+}  // extern "C"

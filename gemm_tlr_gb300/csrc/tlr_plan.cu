@@ -3151,3 +3151,14 @@ tlr_status_t tlr_debug_unsatisfied_wait(tlr_handle_t h) {
 }
 
 }  // extern "C"
+
+// Handle access for the library's other translation unit (tlr_compress.cu).
+namespace tlr {
+cudaStream_t handle_stream(tlr_handle_t h) { return h->stream; }
+bool handle_on_current_device(tlr_handle_t h) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return false; }
+  return dev == h->device;
+}
+bool is_device_pointer(const void *p) { return p != nullptr && device_memory(p); }
+}  // namespace tlr

@@ -160,3 +160,96 @@ def fake_descriptor(X, base: int) -> tuple:
         es = elem_bytes(X.dtype)
         addr += ((a.size * es + 4095) // 4096) * 4096
     return d, keep
+
+
+class DeviceCompression:
+    """Recompression of a dense device matrix's tiles into TLR form
+    (``tlr_compress``), its outputs in device memory and, for square matrices
+    with a dense diagonal, their packing into TLR buffers (``tlr_pack``).
+
+    ``C`` is a flat float32 device tensor (m x n, column-major, leading
+    dimension ``ldc``), ``omega`` a (b, s) float32 numpy array (the sketch).
+    """
+
+    def __init__(self, m: int, n: int, b: int, dense_diagonal: bool, eps: float, r_max: int, omega: np.ndarray,
+                 device="cuda", batch_tiles: Optional[int] = None):
+        import torch
+        self.m, self.n, self.b = m, n, b
+        self.nI, self.nJ = -(-m // b), -(-n // b)
+        self.dense_diagonal = bool(dense_diagonal)
+        self.eps, self.r_max = float(eps), int(r_max)
+        self.s = int(omega.shape[1])
+        assert omega.shape[0] == b
+        self.omega = torch.from_numpy(np.asfortranarray(omega, dtype=np.float32).reshape(-1, order="F")).to(device)
+        nt = self.nI * self.nJ
+        self.U = torch.zeros(max(1, nt * b * r_max), dtype=torch.float32, device=device)
+        self.V = torch.zeros_like(self.U)
+        self.D = torch.zeros(max(1, self.nI * b * b if self.dense_diagonal else 1), dtype=torch.float32, device=device)
+        self.ranks = torch.zeros(nt, dtype=torch.int32, device=device)
+        self.errors = torch.zeros(nt, dtype=torch.float32, device=device)
+        tiles = nt if batch_tiles is None else max(1, min(nt, batch_tiles))
+        self.ws_bytes = _abi.tlr_compress_workspace_bytes(b, self.s, tiles)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+
+    def run(self, handle: int, C, ldc: int):
+        _abi.tlr_compress(handle, C.data_ptr(), ldc, self.m, self.n, self.b, self.dense_diagonal, self.eps,
+                          self.r_max, self.omega.data_ptr(), self.s, self.U.data_ptr(), self.V.data_ptr(),
+                          self.D.data_ptr(), self.ranks.data_ptr(), self.errors.data_ptr(), self.ws.data_ptr(),
+                          self.ws_bytes)
+
+    def dims(self):
+        rd = [min(self.b, self.m - i * self.b) for i in range(self.nI)]
+        cd = [min(self.b, self.n - j * self.b) for j in range(self.nJ)]
+        return rd, cd
+
+    def tiles(self) -> dict:
+        """Host copy: ranks (nI, nJ), errors, and per tile ("lr", U, V) or ("dense", D) in float64."""
+        b, r_max = self.b, self.r_max
+        ranks = self.ranks.cpu().numpy().reshape(self.nI, self.nJ)
+        errors = self.errors.cpu().numpy().astype(np.float64).reshape(self.nI, self.nJ)
+        U = self.U.double().cpu().numpy()
+        V = self.V.double().cpu().numpy()
+        D = self.D.double().cpu().numpy()
+        rd, cd = self.dims()
+        tiles = {}
+        for i in range(self.nI):
+            for j in range(self.nJ):
+                t = i * self.nJ + j
+                if self.dense_diagonal and i == j:
+                    tiles[(i, j)] = ("dense", D[i * b * b:(i + 1) * b * b].reshape(b, b, order="F")[:rd[i], :rd[i]])
+                    continue
+                r = int(ranks[i, j])
+                u = U[t * b * r_max:(t + 1) * b * r_max].reshape(b, r_max, order="F")[:rd[i], :r]
+                v = V[t * b * r_max:(t + 1) * b * r_max].reshape(b, r_max, order="F")[:cd[j], :r]
+                tiles[(i, j)] = ("lr", u, v)
+        return {"ranks": ranks, "errors": errors, "tiles": tiles, "rdims": rd, "cdims": cd,
+                "dense_diagonal": self.dense_diagonal}
+
+    def pack(self, handle: int, device="cuda"):
+        """Packed fp32 TLR buffers of the result and a tlr_operand_t pointing at them:
+        (descriptor, keep-alive list)."""
+        import torch
+        assert self.dense_diagonal and self.m == self.n
+        n, b = self.n, self.b
+        nt, mf, rem = self.nI, n // b, n % b
+        ranks = np.ascontiguousarray(self.ranks.cpu().numpy().reshape(nt, nt), dtype=np.int32)
+        R = ranks.astype(np.int64)
+        inner = R[:mf, :mf].copy()
+        np.fill_diagonal(inner, 0)
+        size = {"U": b * inner.sum(), "V": b * inner.sum(), "D": mf * b * b}
+        if rem:
+            size.update({"bu_U": b * R[:mf, mf].sum(), "bu_V": rem * R[:mf, mf].sum(),
+                         "bv_U": rem * R[mf, :mf].sum(), "bv_V": b * R[mf, :mf].sum(), "gamma": rem * rem})
+        bufs = {k: torch.empty(max(1, int(v)), dtype=torch.float32, device=device) for k, v in size.items()}
+        ptr = {k: (t.data_ptr() if size[k] > 0 else 0) for k, t in bufs.items()}
+        _abi.tlr_pack(handle, n, b, self.r_max, ranks, self.U.data_ptr(), self.V.data_ptr(), self.D.data_ptr(),
+                      ptr.get("U", 0), ptr.get("V", 0), ptr.get("D", 0), ptr.get("bu_U", 0), ptr.get("bu_V", 0),
+                      ptr.get("bv_U", 0), ptr.get("bv_V", 0), ptr.get("gamma", 0))
+        d = _abi.tlr_operand_t()
+        d.kind, d.dtype, d.rows, d.cols, d.b, d.diag_dense = _abi.TLR_KIND_TLR, _DTYPES["f32"], n, n, b, 1
+        r32 = np.ascontiguousarray(ranks, dtype=np.int32)
+        d.ranks = r32.ctypes.data
+        for k, v in ptr.items():
+            if v:
+                setattr(d, k, v)
+        return d, [r32, bufs]

@@ -265,6 +265,60 @@ tlr_status_t tlr_set_timing(tlr_handle_t handle, int enabled);
 tlr_status_t tlr_get_timing(tlr_handle_t handle, int kind, double *ms, int64_t *launches);
 tlr_status_t tlr_reset_timing(tlr_handle_t handle);
 
+/* ---- TLR output ("TLR Matrix Multiplication", section "Introduction: TLR
+ * GEMM": the TLR-output cases of the product). A TLR-output product is the
+ * dense-output product (tlr_gemm into a dense scratch C, which holds
+ * beta * C0 on entry) followed by tlr_compress of that C, and tlr_pack to the
+ * packed TLR format of this header. Neither page describes the recompression;
+ * the rule here is the truncated SVD of each tile:
+ *   every tile (i, j) of C's grid (b x b, the last row/column of tiles
+ *   ragged) except the diagonal ones when dense_diagonal != 0 (square C) gets
+ *   the smallest rank r with sqrt(sum_{k > r} sigma_k^2) <= eps * ||C_ij||_F,
+ *   capped at min(r_max, d_i, d_j); U_ij V_ij^T approximates C_ij.
+ * Method (per tile, fp32 arithmetic, tile energies in fp64): sketch
+ * Y = C_ij Omega with the caller's s columns of Omega (b x s, column-major,
+ * leading dimension b; typically Gaussian; random numbers are an input),
+ * orthonormal basis Q of Y (Gram-Schmidt with reorthogonalisation),
+ * B = Q^T C_ij, Jacobi eigen-decomposition of B B^T, then the rule above on
+ * ||C_ij||^2 minus the kept eigenvalues, U = Q W_r (orthonormal columns),
+ * V = B^T W_r. With s above a tile's numerical rank the result is that tile's
+ * truncated SVD up to rounding; otherwise the rank can exceed the optimal one
+ * and the rule still bounds the error, which is returned per tile. Energies
+ * are resolved to about 1e-5 of a tile's, so eps below about 3e-3 decides ranks
+ * on rounding.
+ *
+ * tlr_compress arguments (DEVICE pointers unless stated):
+ *   C (m x n, column-major, ldc >= m) is read only; b tile size; s even,
+ *   2 <= s <= 128; 0 <= r_max <= s; eps >= 0.
+ *   Outputs, tile t = i * nJ + j of the nI x nJ grid (nI = ceil(m/b)):
+ *   ranks[t] (int32) and errors[t] (relative Frobenius error of U V^T; 0 for
+ *   dense tiles); U: a b x r_max column-major block per tile at t*b*r_max
+ *   (leading dimension b, rows d_i used, columns from ranks[t] on zero); V
+ *   likewise with rows d_j; D (dense_diagonal only): diagonal tile t at t*b*b,
+ *   leading dimension b. U and V may be NULL when r_max == 0.
+ *   workspace: at least tlr_compress_workspace_bytes(b, s, 1); with more, up
+ *   to tlr_compress_workspace_bytes(b, s, nI*nJ), more tiles run at once.
+ *   Asynchronous on the handle's stream; the current device must be the
+ *   handle's. Errors: TLR_STATUS_INVALID_ARG (bad size, argument or host
+ *   pointer), TLR_STATUS_WORKSPACE_TOO_SMALL, TLR_STATUS_UNSUPPORTED (b above
+ *   what one block's shared memory holds), TLR_STATUS_CUDA_ERROR. */
+tlr_status_t tlr_compress_workspace_bytes(int64_t b, int32_t s, int64_t tiles, size_t *bytes);
+tlr_status_t tlr_compress(tlr_handle_t handle, const float *C, int64_t ldc, int64_t m, int64_t n, int64_t b,
+                          int32_t dense_diagonal, float eps, int32_t r_max, const float *omega, int32_t s,
+                          float *U, float *V, float *D, int32_t *ranks, float *errors, void *workspace,
+                          size_t workspace_bytes);
+
+/* Packs the output of tlr_compress for a square n x n matrix with dense
+ * diagonal into the fp32 TLR buffers that a tlr_operand_t points at: interior
+ * U by tile row, V by tile column, D; with n % b != 0 also the boundary panels
+ * bu_U, bu_V, bv_U, bv_V and the corner gamma. `ranks` is a HOST copy of tlr_compress's ranks
+ * (nt * nt, nt = ceil(n/b); 0 on the diagonal). Each destination holds exactly
+ * the prefix-summed sizes of this header's format; buffers for parts with no
+ * columns may be NULL. Asynchronous on the handle's stream. */
+tlr_status_t tlr_pack(tlr_handle_t handle, int64_t n, int64_t b, int32_t r_max, const int32_t *ranks,
+                      const float *U_pad, const float *V_pad, const float *D_pad, float *U, float *V, float *D,
+                      float *bu_U, float *bu_V, float *bv_U, float *bv_V, float *gamma);
+
 /* Host-only check of the tables a plan would launch, with no device use.
  * Pointer fields of A and B may be arbitrary distinct 16-byte-aligned values
  * (nothing is dereferenced). Builds the plan for `workspace_bytes` and

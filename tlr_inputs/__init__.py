@@ -473,3 +473,11 @@ def _zero_parts(X, zero_diag: bool, zero_lowrank: bool) -> None:
         for a in (X.U, X.V, X.bu_U, X.bu_V, X.bv_U, X.bv_V):
             if a is not None:
                 a[:] = 0
+
+
+def sketch(b: int, s: int, seed: int = 0) -> np.ndarray:
+    """The random test matrix Omega (b x s, entries N(0, 1), float32) that the
+    GPU recompression of TLR-output products takes as an input; the oracle's
+    recompression is exact and draws nothing."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0x5EC, b, s]))
+    return rng.standard_normal((b, s)).astype(np.float32)
