@@ -428,6 +428,77 @@ def per_config_timings(h, stream, local: int, peaks: dict, cfgs=(1, 2, 3, 4)) ->
     return out
 
 
+# fp32 lanes per SM, SMs and the maximum SM clock of a GB300: the ALU peak the
+# recompression's SIMT kernels are measured against (2 FLOP per fused multiply-add)
+FP32_LANES_PER_SM, SMS, SM_MAX_GHZ = 128, 152, 2.07
+
+
+def tlr_output_timings(h, stream, local: int, peaks: dict, n: int, eps: float, r_max: int, s: int,
+                       steps: int, warmup: int) -> dict:
+    """TLR output of the large product's family at order n (b = 1024, bf16): the
+    dense-output product into a scratch C, then tlr_compress of C's tiles
+    (sketch of s columns, rank at most r_max, tolerance eps). Each stage timed
+    with CUDA events on the library's stream over `steps` products."""
+    import numpy as np
+    import torch
+    import gemm_tlr_gb300 as g
+    import tlr_inputs
+    from gemm_tlr_gb300.device import DeviceCompression, DeviceProblem
+    p = tlr_inputs.var_rank_grid(n)
+    dp = DeviceProblem(p)
+    b = p.A.b
+    dc = DeviceCompression(p.m, p.n, b, True, eps, r_max, tlr_inputs.sketch(b, s))
+    try:
+        dp.make_plan(h)
+        for _ in range(warmup):
+            dp.run()
+            dc.run(h, dp.C, dp.ldc)
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        with ClockSampler(local) as clk:
+            clk.mark("start")
+            for e in ev:
+                e[0].record(stream)
+                dp.run()
+                e[1].record(stream)
+                dc.run(h, dp.C, dp.ldc)
+                e[2].record(stream)
+            torch.cuda.synchronize()
+            clk.mark("end")
+        assert g.tlr_get_device_status(h) == 0
+        prod_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+        comp_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+        ranks = dc.ranks.cpu().numpy().reshape(dc.nI, dc.nJ)
+        errors = dc.errors.cpu().numpy().reshape(dc.nI, dc.nJ)
+        nt = dc.nI
+        low = ~np.eye(nt, dtype=bool)
+        tiles = int(low.sum())
+        # SIMT work per low-rank tile (b x b): sketch and projection 2 b^2 s each,
+        # core 2 s^2 b, factors 2 (2 b) s r_max, Gram-Schmidt 2 (2 b s^2 / 2)
+        flop = tiles * (4.0 * b * b * s + 2.0 * s * s * b + 4.0 * b * s * r_max + 2.0 * b * s * s)
+        c_bytes = 4.0 * p.m * p.n
+        out_bytes = 4.0 * float(ranks[low].sum()) * 2 * b + 4.0 * nt * b * b
+        alu_peak = FP32_LANES_PER_SM * SMS * 2 * SM_MAX_GHZ / 1e3   # TFLOP/s
+        return {
+            "workload": f"{p.name} with TLR output", "n": n, "b": b, "eps": eps, "r_max": r_max, "sketch": s,
+            "steps": steps, "product_ms": prod_ms, "compress_ms": comp_ms,
+            "ranks": {"mean": float(ranks[low].mean()), "min": int(ranks[low].min()), "max": int(ranks[low].max()),
+                      "at_cap": float((ranks[low] == r_max).mean())},
+            "errors": {"mean": float(errors[low].mean()), "max": float(errors[low].max())},
+            "compress_simt_tflops": flop / (comp_ms * 1e-3) / 1e12,
+            "compress_alu": {"bound": "alu", "achieved": flop / (comp_ms * 1e-3) / 1e12, "peak": alu_peak,
+                             "unit": "TFLOP/s", "frac": flop / (comp_ms * 1e-3) / 1e12 / alu_peak,
+                             "peak_source": "152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz"},
+            "compress_hbm": {"algorithmic_bytes": c_bytes + out_bytes,
+                             "gbs": (c_bytes + out_bytes) / (comp_ms * 1e-3) / 1e9,
+                             "frac": (c_bytes + out_bytes) / (comp_ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
+                             "note": "C read once and the factors written once; the kernels read C three times"},
+            "clocks": clk.summary(),
+        }
+    finally:
+        dp.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -441,10 +512,12 @@ def main():
     ap.add_argument("--scale-down", type=int, default=1,
                     help="profile a smaller member of the workload family (N/s, b/s, budget/s^2); "
                          "bench lines are taken at 1")
-    ap.add_argument("--workload", default="large_var_rank", choices=["large_var_rank", "skewed8x8", "var_rank"],
+    ap.add_argument("--workload", default="large_var_rank",
+                    choices=["large_var_rank", "skewed8x8", "var_rank", "tlr_output"],
                     help="skewed8x8: the pages' variable-rank 8 x 8 grid (b = N/8, ranks on [b/32, b/16]), "
                          "a second measurement beside the metric's workload; var_rank: the large product's "
-                         "tiles and rank rule at order --n (smaller cases for profiling)")
+                         "tiles and rank rule at order --n (smaller cases for profiling); tlr_output: that "
+                         "product with TLR output (recompression timed beside the product)")
     ap.add_argument("--n", type=int, default=65536, help="order of the skewed8x8 or var_rank workload")
     ap.add_argument("--dtype", default="f16", choices=["f16", "bf16", "f32"], help="element type of skewed8x8")
     ap.add_argument("--budget-gib", type=float, default=None,
@@ -466,6 +539,20 @@ def main():
 
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
+    if args.workload == "tlr_output":
+        __graft_entry__.build()
+        h = g.tlr_create(torch.cuda.current_stream().cuda_stream)
+        peaks, _ = _peaks()
+        n = args.n if args.n != 65536 else 16384
+        res = tlr_output_timings(h, torch.cuda.current_stream(), local, peaks, n, 1e-2, 96, 128,
+                                 min(args.steps, 20), args.warmup)
+        g.tlr_destroy(h)
+        if rank == 0:
+            print(json.dumps({"metric": "TLR-output GEMM: recompression time beside the dense-output product",
+                              "value": res["compress_ms"], "unit": "ms", "higher_is_better": False,
+                              "n_gpus": 1, "dtype": "f32", "data": "synthetic", "config": {"workload": res["workload"]},
+                              "tlr_output": res}), flush=True)
+        return 0
     dist = None
     if world > 1:
         import torch.distributed as dist

@@ -16,7 +16,7 @@
 //   3. Q = an orthonormal basis of Y, classical Gram-Schmidt with one
 //      reorthogonalisation (Giraud, Langou and Rozloznik, 2005);
 //   4. B = Q^T T (s x d_j) and the core G = B B^T (s x s, fp64 accumulation
-//      across blocks of 16 products);
+//      across blocks of 512 products);
 //   5. G = W diag(lambda) W^T by the cyclic Jacobi method (two-sided
 //      rotations, round-robin pair order; Golub and Van Loan, "Matrix
 //      Computations", section 8.5), eigenvalues sorted in decreasing order:
@@ -49,7 +49,9 @@ bool is_device_pointer(const void *p);
 namespace tlr_cmp {
 
 constexpr int kMaxSketch = 128;   // columns of the sketch (the core fits in shared memory)
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;      // the GEMM blocks
+constexpr int kBigThreads = 1024;  // one block per tile: energy, Jacobi
+constexpr int kOrthThreads = 512;  // one block per tile: Gram-Schmidt
 
 struct Geo {
   int64_t m, n, b;
@@ -77,26 +79,31 @@ __device__ __forceinline__ bool is_dense_tile(const Geo &g, int64_t i, int64_t j
 }
 
 // ---------------------------------------------------------------- tile energy
-__global__ void __launch_bounds__(kThreads) norm_kernel(const float *C, int64_t ldc, Geo g, int64_t t0, Scratch w) {
+__global__ void __launch_bounds__(kBigThreads) norm_kernel(const float *C, int64_t ldc, Geo g, int64_t t0, Scratch w) {
   const int64_t t = t0 + blockIdx.x;
   const int64_t i = t / g.nJ, j = t % g.nJ;
   const int64_t di = tile_dim(g.m, g.b, i), dj = tile_dim(g.n, g.b, j);
   double acc = 0.0;
   if (!is_dense_tile(g, i, j)) {
     const float *T = C + i * g.b + j * g.b * ldc;
-    for (int64_t c = 0; c < dj; ++c)
-      for (int64_t r = threadIdx.x; r < di; r += blockDim.x) {
-        const double x = T[r + c * ldc];
-        acc += x * x;
-      }
+    for (int64_t c0 = 0; c0 < dj; c0 += 16) {   // fp32 sums of up to 16 x (b / blockDim) squares, then fp64
+      float part = 0.f;
+      const int64_t c1 = c0 + 16 < dj ? c0 + 16 : dj;
+      for (int64_t c = c0; c < c1; ++c)
+        for (int64_t r = threadIdx.x; r < di; r += blockDim.x) {
+          const float x = T[r + c * ldc];
+          part = fmaf(x, x, part);
+        }
+      acc += part;
+    }
   }
-  __shared__ double red[kThreads / 32];
+  __shared__ double red[32];
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
   __syncthreads();
   if (threadIdx.x == 0) {
     double s = 0.0;
-    for (int k = 0; k < kThreads / 32; ++k) s += red[k];
+    for (int k = 0; k < static_cast<int>(blockDim.x >> 5); ++k) s += red[k];
     w.norm2[blockIdx.x] = s;
   }
 }
@@ -105,7 +112,7 @@ __global__ void __launch_bounds__(kThreads) norm_kernel(const float *C, int64_t 
 // out(r, c) = sum_k A(r, k) B(k, c) for one 64 x 64 block of one tile; each of
 // the 256 threads holds 4 x 4 results. kAk / kBk: the operand's contiguous
 // index is k (else r for A, c for B), which decides the loading order so that
-// neighbouring threads read neighbouring addresses. kWide: partial sums of 16
+// neighbouring threads read neighbouring addresses. kWide: partial sums of 512
 // products in fp32 are added into fp64 accumulators.
 template <bool kAk, bool kBk, bool kWide, class LA, class LB, class ST>
 __device__ __forceinline__ void gemm_block(int64_t M, int64_t N, int64_t K, int64_t m0, int64_t n0, LA la, LB lb,
@@ -150,10 +157,12 @@ __device__ __forceinline__ void gemm_block(int64_t M, int64_t N, int64_t K, int6
         for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(a[x], bb[y], acc[x][y]);
     }
     if constexpr (kWide) {
+      if ((k0 & 511) == 496 || k0 + 16 >= K) {
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
+        for (int x = 0; x < 4; ++x)
 #pragma unroll
-        for (int y = 0; y < 4; ++y) { wacc[x][y] += acc[x][y]; acc[x][y] = 0.f; }
+          for (int y = 0; y < 4; ++y) { wacc[x][y] += acc[x][y]; acc[x][y] = 0.f; }
+      }
     }
     __syncthreads();
   }
@@ -249,7 +258,7 @@ __global__ void __launch_bounds__(kThreads) factor_kernel(Geo g, int64_t t0, Scr
 // 1e-5 of its own norm adds no direction the others do not hold to within
 // fp32 rounding (there the second pass cannot restore orthogonality): it
 // becomes zero, and its eigenvalue in the core is zero.
-__global__ void __launch_bounds__(kThreads) orth_kernel(Geo g, int64_t t0, Scratch w) {
+__global__ void __launch_bounds__(kOrthThreads) orth_kernel(Geo g, int64_t t0, Scratch w) {
   const int64_t t = t0 + blockIdx.x;
   const int64_t i = t / g.nJ, j = t % g.nJ;
   if (is_dense_tile(g, i, j)) return;
@@ -259,8 +268,8 @@ __global__ void __launch_bounds__(kThreads) orth_kernel(Geo g, int64_t t0, Scrat
   extern __shared__ float sm[];
   float *y = sm;                       // the current column (d_i <= b)
   float *coef = sm + b;                // kMaxSketch projections
-  __shared__ float red[kThreads / 32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __shared__ float red[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = static_cast<int>(blockDim.x >> 5);
   auto sum_sq = [&]() {                // sum of y^2 over the block (every thread gets it)
     float a = 0.f;
     for (int64_t r = threadIdx.x; r < di; r += blockDim.x) a = fmaf(y[r], y[r], a);
@@ -268,7 +277,7 @@ __global__ void __launch_bounds__(kThreads) orth_kernel(Geo g, int64_t t0, Scrat
     if (lane == 0) red[warp] = a;
     __syncthreads();
     float tot = 0.f;
-    for (int k = 0; k < kThreads / 32; ++k) tot += red[k];
+    for (int k = 0; k < nwarps; ++k) tot += red[k];
     __syncthreads();                   // red is reused by the next call
     return tot;
   };
@@ -277,7 +286,7 @@ __global__ void __launch_bounds__(kThreads) orth_kernel(Geo g, int64_t t0, Scrat
     __syncthreads();
     const float orig2 = sum_sq();
     for (int pass = 0; pass < 2; ++pass) {
-      for (int k = warp; k < c; k += kThreads / 32) {
+      for (int k = warp; k < c; k += nwarps) {
         float a = 0.f;
         for (int64_t r = lane; r < di; r += 32) a = fmaf(Q[r + k * b], y[r], a);
         for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
@@ -304,7 +313,7 @@ __global__ void __launch_bounds__(kThreads) orth_kernel(Geo g, int64_t t0, Scrat
 // tournament: position 0 fixed, the others rotate); a round computes every
 // pair's rotation, applies all of them to the rows (J^T G), then to the
 // columns (G J) and to the accumulated eigenvectors (W J).
-__global__ void __launch_bounds__(kThreads) eig_kernel(Geo g, int64_t t0, Scratch w, int32_t *ranks, float *errors) {
+__global__ void __launch_bounds__(kBigThreads) eig_kernel(Geo g, int64_t t0, Scratch w, int32_t *ranks, float *errors) {
   const int64_t t = t0 + blockIdx.x;
   const int64_t i = t / g.nJ, j = t % g.nJ;
   if (is_dense_tile(g, i, j)) {
@@ -315,10 +324,7 @@ __global__ void __launch_bounds__(kThreads) eig_kernel(Geo g, int64_t t0, Scratc
   extern __shared__ float sm[];
   float *G = sm;                      // s x ps
   float *W = G + s * ps;              // s x ps
-  float *cs = W + s * ps;             // s/2 cosines
-  float *sn = cs + s / 2;             // s/2 sines
-  int *pp = reinterpret_cast<int *>(sn + s / 2), *pq = pp + s / 2;
-  float *lam = reinterpret_cast<float *>(pq + s / 2);   // s
+  float *lam = W + s * ps;            // s
   int *order = reinterpret_cast<int *>(lam + s);        // s
   const float *Gg = w.G + blockIdx.x * w.g_stride;
   for (int e = threadIdx.x; e < s * s; e += blockDim.x) {
@@ -327,53 +333,73 @@ __global__ void __launch_bounds__(kThreads) eig_kernel(Geo g, int64_t t0, Scratc
     W[r * ps + c] = r == c ? 1.f : 0.f;
   }
   __syncthreads();
+  // the trace (invariant under the rotations) sets the absolute scale
+  __shared__ float trace_s;
+  if (threadIdx.x == 0) {
+    float tr = 0.f;
+    for (int k = 0; k < s; ++k) tr += fabsf(G[k * ps + k]);
+    trace_s = tr;
+  }
+  __syncthreads();
+  const float floor_o = 2e-7f * trace_s;
   __shared__ int rotated;
   for (int sweep = 0; sweep < 30; ++sweep) {
     // threshold Jacobi: a pair is rotated only while its off-diagonal entry is
-    // above 1e-6 sqrt(|G_pp G_qq|) and above the rounding level of its larger
-    // diagonal entry; the sweeps end when one rotates nothing
+    // above 1e-6 sqrt(|G_pp G_qq|), above the rounding level of its larger
+    // diagonal entry and above 2e-7 of the trace (fp32 rounding of the core;
+    // below that no energy the rank rule resolves can move); the sweeps end
+    // when one rotates nothing
     if (threadIdx.x == 0) rotated = 0;
     __syncthreads();
+    // Thread mapping: tpp threads per pair, thread (k, j) with k = tid / tpp
+    // works on pair k and on the columns (rows) j, j + tpp, ... of it, so one
+    // warp touches consecutive columns of a row (row update) or consecutive
+    // rows of a column (column update). Each thread computes its pair's
+    // rotation itself from the entries as they stand at the start of the round.
+    const int half = s / 2;
+    const int tpp = static_cast<int>(blockDim.x) / half;
+    const int kq = static_cast<int>(threadIdx.x) / tpp, jq = static_cast<int>(threadIdx.x) % tpp;
+    const bool active = kq < half;
     for (int round = 0; round < s - 1; ++round) {
-      if (threadIdx.x < s / 2) {
-        const int k = threadIdx.x;
+      int p = 0, q = 0;
+      float c = 1.f, sv = 0.f;
+      if (active) {
         auto pos = [&](int x) { return x == 0 ? 0 : 1 + (x - 1 + round) % (s - 1); };
-        int p = pos(k), q = pos(s - 1 - k);
+        p = pos(kq);
+        q = pos(s - 1 - kq);
         if (p > q) { const int tmp = p; p = q; q = tmp; }
         const float a = G[p * ps + p], d = G[q * ps + q], o = G[p * ps + q];
-        float c = 1.f, sv = 0.f;
         const float ao = fabsf(o);
-        if (ao > 1e-6f * sqrtf(fabsf(a)) * sqrtf(fabsf(d)) && ao > 1e-7f * fmaxf(fabsf(a), fabsf(d)) && ao > 1e-35f) {
-          rotated = 1;
+        if (ao > 1e-6f * sqrtf(fabsf(a)) * sqrtf(fabsf(d)) && ao > 1e-7f * fmaxf(fabsf(a), fabsf(d)) &&
+            ao > floor_o && ao > 1e-35f) {
+          if (jq == 0) rotated = 1;
           // symmetric 2 x 2 Schur decomposition: t = tan(theta) with the smaller angle
           const float tau = (d - a) / (2.f * o);
           const float tt = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
           c = rsqrtf(1.f + tt * tt);
           sv = tt * c;
         }
-        cs[k] = c; sn[k] = sv; pp[k] = p; pq[k] = q;
       }
       __syncthreads();
-      const int half = s / 2;
-      for (int e = threadIdx.x; e < half * s; e += blockDim.x) {   // rows p, q of G
-        const int k = e / s, col = e % s;
-        const int p = pp[k], q = pq[k];
-        const float c = cs[k], sv = sn[k];
-        const float gp = G[p * ps + col], gq = G[q * ps + col];
-        G[p * ps + col] = c * gp - sv * gq;
-        G[q * ps + col] = sv * gp + c * gq;
+      if (active && sv != 0.f) {           // rows p, q of G
+        float *gp = G + p * ps, *gq = G + q * ps;
+        for (int col = jq; col < s; col += tpp) {
+          const float x = gp[col], y = gq[col];
+          gp[col] = c * x - sv * y;
+          gq[col] = sv * x + c * y;
+        }
       }
       __syncthreads();
-      for (int e = threadIdx.x; e < half * s; e += blockDim.x) {   // columns p, q of G and W
-        const int k = e % half, row = e / half;
-        const int p = pp[k], q = pq[k];
-        const float c = cs[k], sv = sn[k];
-        const float gp = G[row * ps + p], gq = G[row * ps + q];
-        G[row * ps + p] = c * gp - sv * gq;
-        G[row * ps + q] = sv * gp + c * gq;
-        const float wp = W[row * ps + p], wq = W[row * ps + q];
-        W[row * ps + p] = c * wp - sv * wq;
-        W[row * ps + q] = sv * wp + c * wq;
+      if (active && sv != 0.f) {           // columns p, q of G and W
+        for (int row = jq; row < s; row += tpp) {
+          float *g = G + row * ps, *wr = W + row * ps;
+          const float x = g[p], y = g[q];
+          g[p] = c * x - sv * y;
+          g[q] = sv * x + c * y;
+          const float u = wr[p], v = wr[q];
+          wr[p] = c * u - sv * v;
+          wr[q] = sv * u + c * v;
+        }
       }
       __syncthreads();
     }
@@ -459,7 +485,7 @@ __global__ void copy_jobs_kernel(const CopyJob *jobs, int njobs) {
 
 size_t eig_smem(int s) {
   const int ps = s + 1;
-  return static_cast<size_t>(2 * s * ps + s + 2 * s + s + s) * 4;
+  return static_cast<size_t>(2 * s * ps + 2 * s) * 4;
 }
 
 }  // namespace tlr_cmp
@@ -542,12 +568,12 @@ tlr_status_t tlr_compress(tlr_handle_t h, const float *C, int64_t ldc, int64_t m
   const unsigned rm64 = static_cast<unsigned>((std::max(r_max, 1) + 63) / 64);
   for (int64_t t0 = 0; t0 < ntiles; t0 += batch) {
     const unsigned nb = static_cast<unsigned>(std::min<int64_t>(batch, ntiles - t0));
-    norm_kernel<<<nb, kThreads, 0, st>>>(C, ldc, g, t0, w);
+    norm_kernel<<<nb, kBigThreads, 0, st>>>(C, ldc, g, t0, w);
     sketch_kernel<<<dim3(bm, sm64, nb), kThreads, 0, st>>>(C, ldc, omega, g, t0, w);
-    orth_kernel<<<nb, kThreads, osm, st>>>(g, t0, w);
+    orth_kernel<<<nb, kOrthThreads, osm, st>>>(g, t0, w);
     project_kernel<<<dim3(sm64, bm, nb), kThreads, 0, st>>>(C, ldc, g, t0, w);
     core_kernel<<<dim3(sm64, sm64, nb), kThreads, 0, st>>>(g, t0, w);
-    eig_kernel<<<nb, kThreads, esm, st>>>(g, t0, w, ranks, errors);
+    eig_kernel<<<nb, kBigThreads, esm, st>>>(g, t0, w, ranks, errors);
     if (r_max > 0) {
       factor_kernel<<<dim3(bm, rm64, nb), kThreads, 0, st>>>(g, t0, w, U, V, 0);
       factor_kernel<<<dim3(bm, rm64, nb), kThreads, 0, st>>>(g, t0, w, U, V, 1);

@@ -398,3 +398,30 @@ def test_invalid_arguments_are_refused(torch_cuda, handle):
     assert call(m=0, n=0) == 0
     torch.cuda.synchronize()
     assert g.tlr_get_device_status(handle) == 0
+
+
+def test_large_product_sampled_tiles(torch_cuda, handle):
+    """The large variable-rank product (N = 32768, b = 1024, bf16 on the tensor
+    cores) with TLR output (eps = 1e-2, r_max = 96, s = 128), in the launch
+    configuration of the dense product's benchmark; four tiles computed by the
+    oracle one by one: a dense diagonal tile, two tiles next to the diagonal
+    (their ranks above r_max: capped) and the far corner."""
+    p = ti.problem(5)
+    dc, gpu, _ = _product_then_compress(torch_cuda, handle, p, 1e-2, 96, 128)
+    b = p.A.b
+    for (i, j) in [(7, 7), (5, 6), (31, 30), (0, 31)]:
+        rows, cols = np.arange(i * b, (i + 1) * b), np.arange(j * b, (j + 1) * b)
+        T = oracle.gemm_problem(p, rows, cols)
+        nrm = np.linalg.norm(T)
+        kind, *f = gpu["tiles"][(i, j)]
+        if i == j:
+            assert kind == "dense" and np.linalg.norm(f[0] - T) / nrm <= 1e-2
+            continue
+        Uo, Vo, ro, eo = to.compress_tile(T, 1e-2, 96)
+        rg, eg = int(gpu["ranks"][i, j]), float(gpu["errors"][i, j])
+        e_true = np.linalg.norm(f[0] @ f[1].T - T) / nrm
+        assert e_true <= np.sqrt(eg ** 2 + E2) + 1e-2, (i, j, e_true, eg)
+        if ro == 96:                                     # capped on both sides
+            assert rg == 96 and eo - 1e-2 <= eg <= 1.5 * eo + 1e-2, (i, j, eg, eo)
+        else:
+            assert eg ** 2 <= 1e-4 + E2 and ro - 2 <= rg <= 1.2 * ro + 4, (i, j, rg, ro, eg)
