@@ -377,7 +377,9 @@ __device__ __forceinline__ float round_tf32(float x) {
 // is the warp's 2 KiB staging area in shared memory.
 // kRowIdx: rowd holds this lane's output rows for row-major 16-bit outputs
 // (resolved once per task); otherwise they are shuffled out per chunk.
-template <bool kRowIdx>
+// kLoadC: with beta != 0, each half's C is loaded before any of it is stored
+// (more registers; the fp32-input kernels, whose products carry beta != 0).
+template <bool kRowIdx, bool kLoadC>
 __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, int64_t drow, bool valid,
                                             const Params &p, const Out &o, int lane, uint8_t *stg,
                                             const int32_t (&rowd)[4], bool &bulk_live) {
@@ -408,9 +410,20 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
           __syncwarp();
           bulk_live = false;
         }
+        // with beta != 0 this half's C is loaded before any of it is stored, all
+        // four loads in flight at once (a load after a store to C could not be
+        // issued early), once the values are parked and their registers free
+        float4 cv[4];
         if (!o.trans) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) sf[j * 32 + lane] = p.alpha * v[16 * h + j];   // [column][row]
+          if (kLoadC && p.beta != 0.f) {
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              const int j = 4 * s + (lane >> 3), r4 = 4 * (lane & 7);
+              if (j < nch) cv[s] = *reinterpret_cast<const float4 *>(C + d0 + r4 + (c0 + 16 * h + j) * ld);
+            }
+          }
           if (bulk && nch == 16) {
             fence_async_shared();
             __syncwarp();
@@ -427,7 +440,7 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
               float4 x = *reinterpret_cast<const float4 *>(sf + j * 32 + r4);
               float4 *dst = reinterpret_cast<float4 *>(C + d0 + r4 + (c0 + 16 * h + j) * ld);
               if (p.beta != 0.f) {
-                const float4 c = *dst;
+                const float4 c = kLoadC ? cv[s] : *dst;
                 x.x = fmaf(p.beta, c.x, x.x); x.y = fmaf(p.beta, c.y, x.y);
                 x.z = fmaf(p.beta, c.z, x.z); x.w = fmaf(p.beta, c.w, x.w);
               }
@@ -440,6 +453,16 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
             *reinterpret_cast<float4 *>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
                 make_float4(p.alpha * v[16 * h + 4 * c], p.alpha * v[16 * h + 4 * c + 1],
                             p.alpha * v[16 * h + 4 * c + 2], p.alpha * v[16 * h + 4 * c + 3]);
+          int64_t dd[4];
+          if constexpr (kLoadC) {
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              const int r = 8 * s + (lane >> 2), c = lane & 3;
+              dd[s] = __shfl_sync(0xffffffffu, valid ? drow : int64_t(-1), r);
+              if (p.beta != 0.f && dd[s] >= 0 && 4 * c < nch)
+                cv[s] = *reinterpret_cast<const float4 *>(C + (c0 + 16 * h + 4 * c) + dd[s] * ld);
+            }
+          }
           if (bulk && nch == 16) {   // the XOR layout above is the map's 64-byte swizzle
             fence_async_shared();
             __syncwarp();
@@ -453,13 +476,15 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], int nc, int64_t c0, 
           for (int s = 0; s < 4; ++s) {
             const int r = 8 * s + (lane >> 2), c = lane & 3;
             float4 x = *reinterpret_cast<const float4 *>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
-            const int64_t d = __shfl_sync(0xffffffffu, valid ? drow : int64_t(-1), r);
+            int64_t d;
+            if constexpr (kLoadC) d = dd[s];
+            else d = __shfl_sync(0xffffffffu, valid ? drow : int64_t(-1), r);
             if (d >= 0 && 4 * c < nch) {
               float4 *dst = reinterpret_cast<float4 *>(C + (c0 + 16 * h + 4 * c) + d * ld);
               if (p.beta != 0.f) {
-                const float4 cv = *dst;
-                x.x = fmaf(p.beta, cv.x, x.x); x.y = fmaf(p.beta, cv.y, x.y);
-                x.z = fmaf(p.beta, cv.z, x.z); x.w = fmaf(p.beta, cv.w, x.w);
+                const float4 cw = kLoadC ? cv[s] : *dst;
+                x.x = fmaf(p.beta, cw.x, x.x); x.y = fmaf(p.beta, cw.y, x.y);
+                x.z = fmaf(p.beta, cw.z, x.z); x.w = fmaf(p.beta, cw.w, x.w);
               }
               *dst = x;
             }
@@ -1032,7 +1057,8 @@ __global__ void __launch_bounds__(kThreads, 1) tlr_task_gemm(const __grid_consta
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = v64[32 * h + i];
-          store_chunk<kPair == 1>(v, ncols - c < 32 ? ncols - c : 32, col0 + c, drow, valid, p, o, lane, stg, rowd, bulk_live);
+          store_chunk<kPair == 1, kTF32>(v, ncols - c < 32 ? ncols - c : 32, col0 + c, drow, valid, p, o, lane, stg,
+                                         rowd, bulk_live);
         }
       }
       // every lane's TMEM reads are complete; one arrival per warp hands the
