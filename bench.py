@@ -506,7 +506,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=0,
-                    help="end-to-end steps (0: as many as fill one second, at least 3)")
+                    help="end-to-end steps (0: about two seconds at the link's usual rate, 40 to 400)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="skip the timings of the other four workloads")
     ap.add_argument("--scale-down", type=int, default=1,
@@ -640,10 +640,12 @@ def main():
     l2.record(stream)
     barrier()
     h2d_ms, d2h_ms = l0.elapsed_time(l1), l1.elapsed_time(l2)
-    # steps for about two seconds: the host link of this machine has slow phases
-    # (copies at a fifth of their usual rate for a second or more), which a long
-    # region averages and the per-step spread below shows
-    e2e_steps = args.e2e_steps or max(3, math.ceil(2000.0 / max(1e-3, h2d_ms + d2h_ms + ms_step)))
+    # steps for about two seconds at the link's usual rate, and at least 40: the
+    # host link of this machine has slow phases (copies at a fifth of their usual
+    # rate for a second or more), which a long region averages and the per-step
+    # spread below shows; a probe copy caught in one must not shorten the region
+    usual_ms = (h2d + d2h) / 150e9 * 1e3 + ms_step
+    e2e_steps = args.e2e_steps or min(400, max(40, math.ceil(2000.0 / max(1e-3, usual_ms))))
     e2e_steps = int(max_over_ranks(float(e2e_steps)))   # every rank runs the same number
     marks = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
     marks[0].record(stream)
