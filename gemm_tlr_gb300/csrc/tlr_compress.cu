@@ -109,57 +109,69 @@ __global__ void __launch_bounds__(kBigThreads) norm_kernel(const float *C, int64
 }
 
 // ---------------------------------------------------------------- batched SIMT GEMM
-// out(r, c) = sum_k A(r, k) B(k, c) for one 64 x 64 block of one tile; each of
-// the 256 threads holds 4 x 4 results. kAk / kBk: the operand's contiguous
-// index is k (else r for A, c for B), which decides the loading order so that
-// neighbouring threads read neighbouring addresses. kWide: partial sums of 512
-// products in fp32 are added into fp64 accumulators.
-template <bool kAk, bool kBk, bool kWide, class LA, class LB, class ST>
+// out(r, c) = sum_k A(r, k) B(k, c) for one TM x kTN block of one tile, K in
+// steps of TK; each of the 256 threads holds TM/16 x 4 results. kAk / kBk: the
+// operand's contiguous index is k (else r for A, c for B), which decides the
+// loading order so that neighbouring threads read neighbouring addresses (TK =
+// 32 gives 128-byte runs along a k-contiguous operand). kWide: partial sums of
+// 512 products in fp32 are added into fp64 accumulators.
+constexpr int kTN = 64;
+template <int TM, int TK, bool kAk, bool kBk, bool kWide, class LA, class LB, class ST>
 __device__ __forceinline__ void gemm_block(int64_t M, int64_t N, int64_t K, int64_t m0, int64_t n0, LA la, LB lb,
                                            ST st) {
-  __shared__ float As[16][64 + 4];
-  __shared__ float Bs[16][64 + 4];
+  constexpr int RM = TM / 16;          // rows per thread (4 or 8)
+  static_assert(TM == 64 || TM == 128, "tile rows");
+  static_assert(TK == 16 || TK == 32, "tile depth");
+  __shared__ __align__(16) float As[TK][TM + 4];
+  __shared__ __align__(16) float Bs[TK][kTN + 4];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  float acc[4][4];
-  double wacc[kWide ? 4 : 1][kWide ? 4 : 1];
+  float acc[RM][4];
+  double wacc[kWide ? RM : 1][kWide ? 4 : 1];
 #pragma unroll
-  for (int a = 0; a < 4; ++a)
+  for (int a = 0; a < RM; ++a)
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
   if constexpr (kWide) {
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < RM; ++a)
 #pragma unroll
       for (int c = 0; c < 4; ++c) wacc[a][c] = 0.0;
   }
-  for (int64_t k0 = 0; k0 < K; k0 += 16) {
+  for (int64_t k0 = 0; k0 < K; k0 += TK) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int idx = tid + kThreads * q;   // 0 .. 1023
-      const int r = kAk ? idx >> 4 : idx & 63, k = kAk ? idx & 15 : idx >> 6;
+    for (int q = 0; q < TM * TK / kThreads; ++q) {
+      const int idx = tid + kThreads * q;
+      const int r = kAk ? idx / TK : idx % TM, k = kAk ? idx % TK : idx / TM;
       const int64_t gr = m0 + r, gk = k0 + k;
       As[k][r] = gr < M && gk < K ? la(gr, gk) : 0.f;
-      const int c = kBk ? idx >> 4 : idx & 63, kb = kBk ? idx & 15 : idx >> 6;
+    }
+#pragma unroll
+    for (int q = 0; q < TK * kTN / kThreads; ++q) {
+      const int idx = tid + kThreads * q;
+      const int c = kBk ? idx / TK : idx % kTN, kb = kBk ? idx % TK : idx / kTN;
       const int64_t gc = n0 + c, gkb = k0 + kb;
       Bs[kb][c] = gc < N && gkb < K ? lb(gkb, gc) : 0.f;
     }
     __syncthreads();
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      float a[4], bb[4];
+    for (int k = 0; k < TK; ++k) {
+      float a[RM];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) a[x] = As[k][ty * 4 + x];
+      for (int h = 0; h < RM / 4; ++h) {
+        const float4 a4 = *reinterpret_cast<const float4 *>(&As[k][ty * RM + 4 * h]);
+        a[4 * h] = a4.x; a[4 * h + 1] = a4.y; a[4 * h + 2] = a4.z; a[4 * h + 3] = a4.w;
+      }
+      const float4 b4 = *reinterpret_cast<const float4 *>(&Bs[k][tx * 4]);
+      const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-      for (int x = 0; x < 4; ++x) bb[x] = Bs[k][tx * 4 + x];
-#pragma unroll
-      for (int x = 0; x < 4; ++x)
+      for (int x = 0; x < RM; ++x)
 #pragma unroll
         for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(a[x], bb[y], acc[x][y]);
     }
     if constexpr (kWide) {
-      if ((k0 & 511) == 496 || k0 + 16 >= K) {
+      if ((k0 & 511) == 512 - TK || k0 + TK >= K) {
 #pragma unroll
-        for (int x = 0; x < 4; ++x)
+        for (int x = 0; x < RM; ++x)
 #pragma unroll
           for (int y = 0; y < 4; ++y) { wacc[x][y] += acc[x][y]; acc[x][y] = 0.f; }
       }
@@ -167,16 +179,19 @@ __device__ __forceinline__ void gemm_block(int64_t M, int64_t N, int64_t K, int6
     __syncthreads();
   }
 #pragma unroll
-  for (int x = 0; x < 4; ++x)
+  for (int x = 0; x < RM; ++x)
 #pragma unroll
     for (int y = 0; y < 4; ++y) {
-      const int64_t r = m0 + ty * 4 + x, c = n0 + tx * 4 + y;
+      const int64_t r = m0 + ty * RM + x, c = n0 + tx * 4 + y;
       if (r < M && c < N) {
         if constexpr (kWide) st(r, c, static_cast<float>(wacc[x][y]));
         else st(r, c, acc[x][y]);
       }
     }
 }
+
+// rows of the GEMM blocks of each kernel
+constexpr int kSketchTM = 128, kProjTM = 64, kCoreTM = 64, kFactorTM = 128;
 
 // Y = T Omega (d_i x s)
 __global__ void __launch_bounds__(kThreads) sketch_kernel(const float *C, int64_t ldc, const float *omega, Geo g,
@@ -185,12 +200,12 @@ __global__ void __launch_bounds__(kThreads) sketch_kernel(const float *C, int64_
   const int64_t i = t / g.nJ, j = t % g.nJ;
   if (is_dense_tile(g, i, j)) return;
   const int64_t di = tile_dim(g.m, g.b, i), dj = tile_dim(g.n, g.b, j);
-  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * 64, n0 = static_cast<int64_t>(blockIdx.y) * 64;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kSketchTM, n0 = static_cast<int64_t>(blockIdx.y) * kTN;
   if (m0 >= di || n0 >= g.s) return;
   const float *T = C + i * g.b + j * g.b * ldc;
   float *Y = w.Q + blockIdx.z * w.q_stride;
   const int64_t b = g.b;
-  gemm_block<false, true, false>(
+  gemm_block<kSketchTM, 16, false, true, false>(
       di, g.s, dj, m0, n0, [&](int64_t r, int64_t k) { return T[r + k * ldc]; },
       [&](int64_t k, int64_t c) { return omega[k + c * b]; }, [&](int64_t r, int64_t c, float v) { Y[r + c * b] = v; });
 }
@@ -201,13 +216,13 @@ __global__ void __launch_bounds__(kThreads) project_kernel(const float *C, int64
   const int64_t i = t / g.nJ, j = t % g.nJ;
   if (is_dense_tile(g, i, j)) return;
   const int64_t di = tile_dim(g.m, g.b, i), dj = tile_dim(g.n, g.b, j);
-  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * 64, n0 = static_cast<int64_t>(blockIdx.y) * 64;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kProjTM, n0 = static_cast<int64_t>(blockIdx.y) * kTN;
   if (m0 >= g.s || n0 >= dj) return;
   const float *T = C + i * g.b + j * g.b * ldc;
   const float *Q = w.Q + blockIdx.z * w.q_stride;
   float *B = w.B + blockIdx.z * w.b_stride;
   const int64_t b = g.b, s = g.s;
-  gemm_block<true, true, true>(
+  gemm_block<kProjTM, 32, true, true, true>(
       g.s, dj, di, m0, n0, [&](int64_t r, int64_t k) { return Q[k + r * b]; },
       [&](int64_t k, int64_t c) { return T[k + c * ldc]; }, [&](int64_t r, int64_t c, float v) { B[r + c * s] = v; });
 }
@@ -218,11 +233,11 @@ __global__ void __launch_bounds__(kThreads) core_kernel(Geo g, int64_t t0, Scrat
   const int64_t i = t / g.nJ, j = t % g.nJ;
   if (is_dense_tile(g, i, j)) return;
   const int64_t dj = tile_dim(g.n, g.b, j);
-  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * 64, n0 = static_cast<int64_t>(blockIdx.y) * 64;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kCoreTM, n0 = static_cast<int64_t>(blockIdx.y) * kTN;
   const float *B = w.B + blockIdx.z * w.b_stride;
   float *G = w.G + blockIdx.z * w.g_stride;
   const int64_t s = g.s;
-  gemm_block<false, false, true>(
+  gemm_block<kCoreTM, 16, false, false, true>(
       s, s, dj, m0, n0, [&](int64_t r, int64_t k) { return B[r + k * s]; },
       [&](int64_t k, int64_t c) { return B[c + k * s]; }, [&](int64_t r, int64_t c, float v) { G[r + c * s] = v; });
 }
@@ -236,7 +251,7 @@ __global__ void __launch_bounds__(kThreads) factor_kernel(Geo g, int64_t t0, Scr
   if (is_dense_tile(g, i, j)) return;
   const int64_t di = tile_dim(g.m, g.b, i), dj = tile_dim(g.n, g.b, j);
   const int64_t rows = which == 0 ? di : dj;
-  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * 64, n0 = static_cast<int64_t>(blockIdx.y) * 64;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kFactorTM, n0 = static_cast<int64_t>(blockIdx.y) * kTN;
   if (m0 >= rows || n0 >= g.r_max) return;
   const float *W = w.W + blockIdx.z * w.g_stride;
   const int64_t b = g.b, s = g.s;
@@ -245,10 +260,10 @@ __global__ void __launch_bounds__(kThreads) factor_kernel(Geo g, int64_t t0, Scr
   auto lw = [&](int64_t k, int64_t c) { return W[k + c * s]; };
   if (which == 0) {
     const float *Q = w.Q + blockIdx.z * w.q_stride;
-    gemm_block<false, true, false>(di, g.r_max, s, m0, n0, [&](int64_t r, int64_t k) { return Q[r + k * b]; }, lw, st);
+    gemm_block<kFactorTM, 16, false, true, false>(di, g.r_max, s, m0, n0, [&](int64_t r, int64_t k) { return Q[r + k * b]; }, lw, st);
   } else {
     const float *B = w.B + blockIdx.z * w.b_stride;
-    gemm_block<true, true, false>(dj, g.r_max, s, m0, n0, [&](int64_t r, int64_t k) { return B[k + r * s]; }, lw, st);
+    gemm_block<kFactorTM, 16, true, true, false>(dj, g.r_max, s, m0, n0, [&](int64_t r, int64_t k) { return B[k + r * s]; }, lw, st);
   }
 }
 
@@ -564,19 +579,20 @@ tlr_status_t tlr_compress(tlr_handle_t h, const float *C, int64_t ldc, int64_t m
           cudaSuccess)
     return TLR_STATUS_CUDA_ERROR;
 
-  const unsigned bm = static_cast<unsigned>((b + 63) / 64), sm64 = static_cast<unsigned>((s + 63) / 64);
-  const unsigned rm64 = static_cast<unsigned>((std::max(r_max, 1) + 63) / 64);
+  // GEMM grids: blocks of (kernel's rows) x kTN columns
+  auto blocks = [](int64_t n, int64_t per) { return static_cast<unsigned>((n + per - 1) / per); };
+  const unsigned bN = blocks(b, kTN), sN = blocks(s, kTN), rN = blocks(std::max(r_max, 1), kTN);
   for (int64_t t0 = 0; t0 < ntiles; t0 += batch) {
     const unsigned nb = static_cast<unsigned>(std::min<int64_t>(batch, ntiles - t0));
     norm_kernel<<<nb, kBigThreads, 0, st>>>(C, ldc, g, t0, w);
-    sketch_kernel<<<dim3(bm, sm64, nb), kThreads, 0, st>>>(C, ldc, omega, g, t0, w);
+    sketch_kernel<<<dim3(blocks(b, kSketchTM), sN, nb), kThreads, 0, st>>>(C, ldc, omega, g, t0, w);
     orth_kernel<<<nb, kOrthThreads, osm, st>>>(g, t0, w);
-    project_kernel<<<dim3(sm64, bm, nb), kThreads, 0, st>>>(C, ldc, g, t0, w);
-    core_kernel<<<dim3(sm64, sm64, nb), kThreads, 0, st>>>(g, t0, w);
+    project_kernel<<<dim3(blocks(s, kProjTM), bN, nb), kThreads, 0, st>>>(C, ldc, g, t0, w);
+    core_kernel<<<dim3(blocks(s, kCoreTM), sN, nb), kThreads, 0, st>>>(g, t0, w);
     eig_kernel<<<nb, kBigThreads, esm, st>>>(g, t0, w, ranks, errors);
     if (r_max > 0) {
-      factor_kernel<<<dim3(bm, rm64, nb), kThreads, 0, st>>>(g, t0, w, U, V, 0);
-      factor_kernel<<<dim3(bm, rm64, nb), kThreads, 0, st>>>(g, t0, w, U, V, 1);
+      factor_kernel<<<dim3(blocks(b, kFactorTM), rN, nb), kThreads, 0, st>>>(g, t0, w, U, V, 0);
+      factor_kernel<<<dim3(blocks(b, kFactorTM), rN, nb), kThreads, 0, st>>>(g, t0, w, U, V, 1);
     }
     if (cudaGetLastError() != cudaSuccess) return TLR_STATUS_CUDA_ERROR;
   }

@@ -425,3 +425,18 @@ def test_large_product_sampled_tiles(torch_cuda, handle):
             assert rg == 96 and eo - 1e-2 <= eg <= 1.5 * eo + 1e-2, (i, j, eg, eo)
         else:
             assert eg ** 2 <= 1e-4 + E2 and ro - 2 <= rg <= 1.2 * ro + 4, (i, j, rg, ro, eg)
+
+
+def test_boundary_transposed_product(torch_cuda, handle):
+    """The boundary/transpose product scaled by 8 (N = 1252, b = 64: 19 full
+    tiles and a 36-wide boundary, op(A) = A^T, beta = 1, fp32 on TF32 tensor
+    cores) with TLR output (eps = 0.1, r_max = s = b: ranks 32-51, none capped):
+    ragged boundary tiles and a dense diagonal including the corner."""
+    p = ti.problem(3, scale_down=8)
+    dc, gpu, _ = _product_then_compress(torch_cuda, handle, p, 0.1, 64, 64)
+    ora = to.tlr_output_product(p, 0.1, 64)
+    C = oracle.gemm_problem(p)
+    nt = len(gpu["rdims"])
+    agree = _compare_product(gpu, ora, C, 0.1, 2e-3, 64)
+    assert agree >= 0.8 * nt * (nt - 1)
+    assert gpu["rdims"][-1] == p.m - (nt - 1) * p.A.b          # the ragged boundary row of tiles
