@@ -301,17 +301,34 @@ __global__ void __launch_bounds__(kOrthThreads) orth_kernel(Geo g, int64_t t0, S
     __syncthreads();
     const float orig2 = sum_sq();
     for (int pass = 0; pass < 2; ++pass) {
+      // four independent partial sums per lane keep several loads of Q in flight
       for (int k = warp; k < c; k += nwarps) {
-        float a = 0.f;
-        for (int64_t r = lane; r < di; r += 32) a = fmaf(Q[r + k * b], y[r], a);
+        const float *qk = Q + k * b;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        int64_t r = lane;
+        for (; r + 96 < di; r += 128) {
+          a0 = fmaf(qk[r], y[r], a0);
+          a1 = fmaf(qk[r + 32], y[r + 32], a1);
+          a2 = fmaf(qk[r + 64], y[r + 64], a2);
+          a3 = fmaf(qk[r + 96], y[r + 96], a3);
+        }
+        for (; r < di; r += 32) a0 = fmaf(qk[r], y[r], a0);
+        float a = (a0 + a1) + (a2 + a3);
         for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
         if (lane == 0) coef[k] = a;
       }
       __syncthreads();
       for (int64_t r = threadIdx.x; r < di; r += blockDim.x) {
-        float v = y[r];
-        for (int k = 0; k < c; ++k) v = fmaf(-coef[k], Q[r + k * b], v);
-        y[r] = v;
+        float v0 = y[r], v1 = 0.f, v2 = 0.f, v3 = 0.f;
+        int k = 0;
+        for (; k + 3 < c; k += 4) {
+          v0 = fmaf(-coef[k], Q[r + k * b], v0);
+          v1 = fmaf(-coef[k + 1], Q[r + (k + 1) * b], v1);
+          v2 = fmaf(-coef[k + 2], Q[r + (k + 2) * b], v2);
+          v3 = fmaf(-coef[k + 3], Q[r + (k + 3) * b], v3);
+        }
+        for (; k < c; ++k) v0 = fmaf(-coef[k], Q[r + k * b], v0);
+        y[r] = (v0 + v1) + (v2 + v3);
       }
       __syncthreads();
     }
