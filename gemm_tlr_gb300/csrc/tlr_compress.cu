@@ -51,6 +51,8 @@ namespace tlr_cmp {
 constexpr int kMaxSketch = 128;   // columns of the sketch (the core fits in shared memory)
 constexpr int kThreads = 256;      // the GEMM blocks
 constexpr int kBigThreads = 1024;  // one block per tile: energy, Jacobi
+constexpr int kWarps = kBigThreads / 32;
+constexpr int kPairsPerWarp = (kMaxSketch / 2 + kWarps - 1) / kWarps;   // Jacobi pairs per warp
 constexpr int kOrthThreads = 512;  // one block per tile: Gram-Schmidt
 
 struct Geo {
@@ -383,54 +385,99 @@ __global__ void __launch_bounds__(kBigThreads) eig_kernel(Geo g, int64_t t0, Scr
     // when one rotates nothing
     if (threadIdx.x == 0) rotated = 0;
     __syncthreads();
-    // Thread mapping: tpp threads per pair, thread (k, j) with k = tid / tpp
-    // works on pair k and on the columns (rows) j, j + tpp, ... of it, so one
-    // warp touches consecutive columns of a row (row update) or consecutive
-    // rows of a column (column update). Each thread computes its pair's
-    // rotation itself from the entries as they stand at the start of the round.
+    // Thread mapping: one warp per pair, warp w working on pairs w, w + 32,
+    // ... in turn, its lanes on consecutive columns of a row (row update) or
+    // consecutive rows of a column (column update); with the row pitch s + 1
+    // both touch 32 distinct banks. Lane m of warp w computes the rotation of
+    // pair w + 32 m from the entries as they stand at the start of the round
+    // and the warp's lanes take it by shuffle.
     const int half = s / 2;
-    const int tpp = static_cast<int>(blockDim.x) / half;
-    const int kq = static_cast<int>(threadIdx.x) / tpp, jq = static_cast<int>(threadIdx.x) % tpp;
-    const bool active = kq < half;
+    const int lane = static_cast<int>(threadIdx.x) & 31, warp = static_cast<int>(threadIdx.x) >> 5;
     for (int round = 0; round < s - 1; ++round) {
-      int p = 0, q = 0;
-      float c = 1.f, sv = 0.f;
-      if (active) {
-        auto pos = [&](int x) { return x == 0 ? 0 : 1 + (x - 1 + round) % (s - 1); };
-        p = pos(kq);
-        q = pos(s - 1 - kq);
+      int pr = 0, qr = 0;
+      float cr = 1.f, sr = 0.f;
+      const int kq = warp + lane * kWarps;
+      if (lane < kPairsPerWarp && kq < half) {
+        // round-robin order: position 0 stays, the others shift by one a round
+        auto pos = [&](int x) {
+          if (x == 0) return 0;
+          const int y = x - 1 + round;
+          return 1 + (y >= s - 1 ? y - (s - 1) : y);
+        };
+        int p = pos(kq), q = pos(s - 1 - kq);
         if (p > q) { const int tmp = p; p = q; q = tmp; }
+        pr = p; qr = q;
         const float a = G[p * ps + p], d = G[q * ps + q], o = G[p * ps + q];
         const float ao = fabsf(o);
         if (ao > 1e-6f * sqrtf(fabsf(a)) * sqrtf(fabsf(d)) && ao > 1e-7f * fmaxf(fabsf(a), fabsf(d)) &&
             ao > floor_o && ao > 1e-35f) {
-          if (jq == 0) rotated = 1;
+          rotated = 1;
           // symmetric 2 x 2 Schur decomposition: t = tan(theta) with the smaller angle
           const float tau = (d - a) / (2.f * o);
           const float tt = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
-          c = rsqrtf(1.f + tt * tt);
-          sv = tt * c;
+          cr = rsqrtf(1.f + tt * tt);
+          sr = tt * cr;
+        }
+      }
+      int pv[kPairsPerWarp], qv[kPairsPerWarp];
+      float cv[kPairsPerWarp], sn[kPairsPerWarp];
+#pragma unroll
+      for (int m = 0; m < kPairsPerWarp; ++m) {
+        pv[m] = __shfl_sync(0xffffffffu, pr, m);
+        qv[m] = __shfl_sync(0xffffffffu, qr, m);
+        cv[m] = __shfl_sync(0xffffffffu, cr, m);
+        sn[m] = __shfl_sync(0xffffffffu, sr, m);
+      }
+      // Rows p and q (which hold the entries the rotation was computed from)
+      // are written by this pair's warp alone.
+      __syncwarp();
+      constexpr int kPer = kMaxSketch / 32;   // columns (rows) per lane
+#pragma unroll
+      for (int m = 0; m < kPairsPerWarp; ++m) {   // rows p, q of G
+        if (sn[m] == 0.f) continue;
+        const float c = cv[m], sv = sn[m];
+        float *gp = G + pv[m] * ps, *gq = G + qv[m] * ps;
+        float x[kPer], y[kPer];
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {       // every load before any store
+          const int col = lane + 32 * e;
+          x[e] = col < s ? gp[col] : 0.f;
+          y[e] = col < s ? gq[col] : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+          const int col = lane + 32 * e;
+          if (col < s) {
+            gp[col] = c * x[e] - sv * y[e];
+            gq[col] = sv * x[e] + c * y[e];
+          }
         }
       }
       __syncthreads();
-      if (active && sv != 0.f) {           // rows p, q of G
-        float *gp = G + p * ps, *gq = G + q * ps;
-        for (int col = jq; col < s; col += tpp) {
-          const float x = gp[col], y = gq[col];
-          gp[col] = c * x - sv * y;
-          gq[col] = sv * x + c * y;
+#pragma unroll
+      for (int m = 0; m < kPairsPerWarp; ++m) {   // columns p, q of G and W
+        if (sn[m] == 0.f) continue;
+        const float c = cv[m], sv = sn[m];
+        const int p = pv[m], q = qv[m];
+        float x[kPer], y[kPer], u[kPer], v[kPer];
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+          const int row = lane + 32 * e;
+          const bool in = row < s;
+          x[e] = in ? G[row * ps + p] : 0.f;
+          y[e] = in ? G[row * ps + q] : 0.f;
+          u[e] = in ? W[row * ps + p] : 0.f;
+          v[e] = in ? W[row * ps + q] : 0.f;
         }
-      }
-      __syncthreads();
-      if (active && sv != 0.f) {           // columns p, q of G and W
-        for (int row = jq; row < s; row += tpp) {
-          float *g = G + row * ps, *wr = W + row * ps;
-          const float x = g[p], y = g[q];
-          g[p] = c * x - sv * y;
-          g[q] = sv * x + c * y;
-          const float u = wr[p], v = wr[q];
-          wr[p] = c * u - sv * v;
-          wr[q] = sv * u + c * v;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+          const int row = lane + 32 * e;
+          if (row < s) {
+            G[row * ps + p] = c * x[e] - sv * y[e];
+            G[row * ps + q] = sv * x[e] + c * y[e];
+            W[row * ps + p] = c * u[e] - sv * v[e];
+            W[row * ps + q] = sv * u[e] + c * v[e];
+          }
         }
       }
       __syncthreads();
