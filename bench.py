@@ -286,6 +286,7 @@ ORDERS = {"auto": 0, "right": 1, "left": 2, "triple": 3, "per_rect": 4}   # tlr_
 
 # Nominal dense tensor-core peaks of one GB300 (TFLOP/s): bf16/fp16 2250, tf32 1100.
 NOMINAL_TFLOPS = {"bf16": 2250.0, "f16": 2250.0, "f32": 1100.0}
+LINK_PROBES = 5   # timed copies of a step's inputs and result for the link-rate estimate
 
 
 def dtype_peaks(dtype: str, peaks: dict):
@@ -628,18 +629,24 @@ def main():
         dp.run()
         C_host.copy_(dp.C, non_blocking=True)
 
-    # link rates of the same buffers, copies alone (for the expected end-to-end time)
+    # link rates of the same buffers, copies alone (for the expected end-to-end
+    # time): the median of LINK_PROBES probes, so that one probe caught in a slow
+    # phase of the host link does not set the estimate
     e2e_step()
     barrier()
-    l0, l1, l2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-    l0.record(stream)
-    dp.A.upload()
-    dp.B.upload()
-    l1.record(stream)
-    C_host.copy_(dp.C, non_blocking=True)
-    l2.record(stream)
-    barrier()
-    h2d_ms, d2h_ms = l0.elapsed_time(l1), l1.elapsed_time(l2)
+    probes = []
+    for _ in range(LINK_PROBES):
+        l0, l1, l2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        l0.record(stream)
+        dp.A.upload()
+        dp.B.upload()
+        l1.record(stream)
+        C_host.copy_(dp.C, non_blocking=True)
+        l2.record(stream)
+        barrier()
+        probes.append((l0.elapsed_time(l1), l1.elapsed_time(l2)))
+    h2d_ms = sorted(q[0] for q in probes)[len(probes) // 2]
+    d2h_ms = sorted(q[1] for q in probes)[len(probes) // 2]
     # steps for about two seconds at the link's usual rate, and at least 40: the
     # host link of this machine has slow phases (copies at a fifth of their usual
     # rate for a second or more), which a long region averages and the per-step
@@ -721,7 +728,8 @@ def main():
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "steps": e2e_steps,
                 "step_ms": {"min": per_step[0], "median": per_step[len(per_step) // 2], "max": per_step[-1]},
-                "link_gbs": {"h2d": h2d / (h2d_ms * 1e-3) / 1e9, "d2h": d2h / (d2h_ms * 1e-3) / 1e9},
+                "link_gbs": {"h2d": h2d / (h2d_ms * 1e-3) / 1e9, "d2h": d2h / (d2h_ms * 1e-3) / 1e9,
+                             "probes": LINK_PROBES, "of": "median per direction"},
                 "expected_ms": h2d_ms + ms_step + d2h_ms,
                 "host_buffers": (f"pinned, allocated on CPUs {numa.cpus[0]}-{numa.cpus[-1]} local to the GPU"
                                  if numa.cpus else "pinned, default placement (GPU-local CPUs unknown)")},
