@@ -347,6 +347,9 @@ __global__ void __launch_bounds__(kOrthThreads) orth_kernel(Geo g, int64_t t0, S
 // tournament: position 0 fixed, the others rotate); a round computes every
 // pair's rotation, applies all of them to the rows (J^T G), then to the
 // columns (G J) and to the accumulated eigenvectors (W J).
+// kS: the sketch width when it is known when compiling (the row pitch kS + 1
+// and the loop bounds become constants), 0 for any other width.
+template <int kS>
 __global__ void __launch_bounds__(kBigThreads) eig_kernel(Geo g, int64_t t0, Scratch w, int32_t *ranks, float *errors) {
   const int64_t t = t0 + blockIdx.x;
   const int64_t i = t / g.nJ, j = t % g.nJ;
@@ -354,7 +357,7 @@ __global__ void __launch_bounds__(kBigThreads) eig_kernel(Geo g, int64_t t0, Scr
     if (threadIdx.x == 0) { ranks[t] = 0; errors[t] = 0.f; }
     return;
   }
-  const int s = g.s, ps = s + 1;
+  const int s = kS ? kS : g.s, ps = s + 1;
   extern __shared__ float sm[];
   float *G = sm;                      // s x ps
   float *W = G + s * ps;              // s x ps
@@ -413,8 +416,10 @@ __global__ void __launch_bounds__(kBigThreads) eig_kernel(Geo g, int64_t t0, Scr
             ao > floor_o && ao > 1e-35f) {
           rotated = 1;
           // symmetric 2 x 2 Schur decomposition: t = tan(theta) with the smaller angle
-          const float tau = (d - a) / (2.f * o);
-          const float tt = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
+          // |o| is above 2e-7 of the trace, so |tau| <= 2.5e6 and both fast
+          // divisions stay far from their range limit
+          const float tau = __fdividef(d - a, 2.f * o);
+          const float tt = __fdividef(tau >= 0.f ? 1.f : -1.f, fabsf(tau) + sqrtf(1.f + tau * tau));
           cr = rsqrtf(1.f + tt * tt);
           sr = tt * cr;
         }
@@ -633,8 +638,10 @@ tlr_status_t tlr_compress(tlr_handle_t h, const float *C, int64_t ldc, int64_t m
     return TLR_STATUS_WORKSPACE_TOO_SMALL;
 
   const size_t esm = eig_smem(s);
-  if (cudaFuncSetAttribute(eig_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(esm)) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(eig_kernel<kMaxSketch>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(esm)) != cudaSuccess ||
+      cudaFuncSetAttribute(eig_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(esm)) !=
+          cudaSuccess)
     return TLR_STATUS_CUDA_ERROR;
   const size_t osm = static_cast<size_t>(b + kMaxSketch) * 4;
   if (osm > 227 * 1024) return TLR_STATUS_UNSUPPORTED;
@@ -653,7 +660,8 @@ tlr_status_t tlr_compress(tlr_handle_t h, const float *C, int64_t ldc, int64_t m
     orth_kernel<<<nb, kOrthThreads, osm, st>>>(g, t0, w);
     project_kernel<<<dim3(blocks(s, kProjTM), bN, nb), kThreads, 0, st>>>(C, ldc, g, t0, w);
     core_kernel<<<dim3(blocks(s, kCoreTM), sN, nb), kThreads, 0, st>>>(g, t0, w);
-    eig_kernel<<<nb, kBigThreads, esm, st>>>(g, t0, w, ranks, errors);
+    if (s == kMaxSketch) eig_kernel<kMaxSketch><<<nb, kBigThreads, esm, st>>>(g, t0, w, ranks, errors);
+    else eig_kernel<0><<<nb, kBigThreads, esm, st>>>(g, t0, w, ranks, errors);
     if (r_max > 0) {
       factor_kernel<<<dim3(blocks(b, kFactorTM), rN, nb), kThreads, 0, st>>>(g, t0, w, U, V, 0);
       factor_kernel<<<dim3(blocks(b, kFactorTM), rN, nb), kThreads, 0, st>>>(g, t0, w, U, V, 1);
