@@ -380,6 +380,8 @@ __global__ void __launch_bounds__(kBigThreads) eig_kernel(Geo g, int64_t t0, Scr
   __syncthreads();
   const float floor_o = 2e-7f * trace_s;
   __shared__ int rotated;
+  __shared__ int rot_pq[kMaxSketch / 2];   // a round's pairs (p | q << 16) and rotations
+  __shared__ float rot_c[kMaxSketch / 2], rot_s[kMaxSketch / 2];
   for (int sweep = 0; sweep < 30; ++sweep) {
     // threshold Jacobi: a pair is rotated only while its off-diagonal entry is
     // above 1e-6 sqrt(|G_pp G_qq|), above the rounding level of its larger
@@ -391,16 +393,17 @@ __global__ void __launch_bounds__(kBigThreads) eig_kernel(Geo g, int64_t t0, Scr
     // Thread mapping: one warp per pair, warp w working on pairs w, w + 32,
     // ... in turn, its lanes on consecutive columns of a row (row update) or
     // consecutive rows of a column (column update); with the row pitch s + 1
-    // both touch 32 distinct banks. Lane m of warp w computes the rotation of
-    // pair w + 32 m from the entries as they stand at the start of the round
-    // and the warp's lanes take it by shuffle.
+    // both touch 32 distinct banks. Thread k < s / 2 computes the rotation of
+    // pair k from the entries as they stand at the start of the round and
+    // leaves it in a shared table for the warp working on that pair.
     const int half = s / 2;
     const int lane = static_cast<int>(threadIdx.x) & 31, warp = static_cast<int>(threadIdx.x) >> 5;
     for (int round = 0; round < s - 1; ++round) {
-      int pr = 0, qr = 0;
-      float cr = 1.f, sr = 0.f;
-      const int kq = warp + lane * kWarps;
-      if (lane < kPairsPerWarp && kq < half) {
+      // the round's rotations, one pair per thread of the first warps, into a
+      // table the block reads after the barrier (the other warps issue none of
+      // this arithmetic)
+      if (static_cast<int>(threadIdx.x) < half) {
+        const int kq = static_cast<int>(threadIdx.x);
         // round-robin order: position 0 stays, the others shift by one a round
         auto pos = [&](int x) {
           if (x == 0) return 0;
@@ -409,7 +412,7 @@ __global__ void __launch_bounds__(kBigThreads) eig_kernel(Geo g, int64_t t0, Scr
         };
         int p = pos(kq), q = pos(s - 1 - kq);
         if (p > q) { const int tmp = p; p = q; q = tmp; }
-        pr = p; qr = q;
+        float cr = 1.f, sr = 0.f;
         const float a = G[p * ps + p], d = G[q * ps + q], o = G[p * ps + q];
         const float ao = fabsf(o);
         if (ao > 1e-6f * sqrtf(fabsf(a)) * sqrtf(fabsf(d)) && ao > 1e-7f * fmaxf(fabsf(a), fabsf(d)) &&
@@ -423,19 +426,26 @@ __global__ void __launch_bounds__(kBigThreads) eig_kernel(Geo g, int64_t t0, Scr
           cr = rsqrtf(1.f + tt * tt);
           sr = tt * cr;
         }
+        rot_pq[kq] = p | (q << 16);
+        rot_c[kq] = cr;
+        rot_s[kq] = sr;
       }
+      // the table is complete, and every read of the entries it came from is done
+      __syncthreads();
       int pv[kPairsPerWarp], qv[kPairsPerWarp];
       float cv[kPairsPerWarp], sn[kPairsPerWarp];
 #pragma unroll
       for (int m = 0; m < kPairsPerWarp; ++m) {
-        pv[m] = __shfl_sync(0xffffffffu, pr, m);
-        qv[m] = __shfl_sync(0xffffffffu, qr, m);
-        cv[m] = __shfl_sync(0xffffffffu, cr, m);
-        sn[m] = __shfl_sync(0xffffffffu, sr, m);
+        const int kq = warp + m * kWarps;
+        pv[m] = 0; qv[m] = 0; cv[m] = 1.f; sn[m] = 0.f;
+        if (kq < half) {
+          const int pq = rot_pq[kq];
+          pv[m] = pq & 0xffff;
+          qv[m] = pq >> 16;
+          cv[m] = rot_c[kq];
+          sn[m] = rot_s[kq];
+        }
       }
-      // Rows p and q (which hold the entries the rotation was computed from)
-      // are written by this pair's warp alone.
-      __syncwarp();
       constexpr int kPer = kMaxSketch / 32;   // columns (rows) per lane
 #pragma unroll
       for (int m = 0; m < kPairsPerWarp; ++m) {   // rows p, q of G
