@@ -134,20 +134,23 @@ def _spectrum_tile(rng, n, sigma):
     return q1 @ np.diag(s) @ q2.T
 
 
+@pytest.mark.parametrize("b", [64, 128, 10])
 @pytest.mark.parametrize("eps", [0.3, 0.1, 0.03, 0.01])
-def test_prescribed_spectra(torch_cuda, handle, eps):
+def test_prescribed_spectra(torch_cuda, handle, eps, b):
     """Tiles with singular values base^-k (a different base per tile): the
-    sketch spans each tile (s = b), so ranks and factors are the oracle's."""
+    sketch spans each tile (s = b), so ranks and factors are the oracle's.
+    b = 128 runs the Jacobi kernel compiled for 128-column sketches, b = 64
+    and b = 10 (five pairs of rows) the general one."""
     rng = np.random.default_rng(11)
-    b, nt = 64, 3
+    nt = 3
     M = np.zeros((b * nt, b * nt))
     for i in range(nt):
         for j in range(nt):
             base = 1.3 + 0.25 * (i * nt + j)
             M[i * b:(i + 1) * b, j * b:(j + 1) * b] = _spectrum_tile(rng, b, [base ** -k for k in range(b)])
-    _, gpu = _compress(torch_cuda, handle, M, b, False, eps, 64, 64)
-    ora = _oracle(M, b, False, eps, 64)
-    assert _compare(gpu, ora, M, eps, 2e-4, 64) >= nt * nt - 1
+    _, gpu = _compress(torch_cuda, handle, M, b, False, eps, b, b)
+    ora = _oracle(M, b, False, eps, b)
+    assert _compare(gpu, ora, M, eps, 2e-4, b) >= nt * nt - 1
 
 
 def test_exact_low_rank_tiles_with_a_small_sketch(torch_cuda, handle):
