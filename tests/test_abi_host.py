@@ -213,7 +213,10 @@ def _problem(cfg, scale):
 
 
 SCHEDULES = [{}, {"TLR_HYBRID": "0"}, {"TLR_SPLIT_LAUNCHES": "1"}, {"TLR_L1_PAIR": "1"},
-             {"TLR_L1_PAIR": "0"}, {"TLR_PAIR": "1"}, {"TLR_ARENAS": "1", "TLR_HYBRID": "0"}]
+             {"TLR_L1_PAIR": "0"}, {"TLR_PAIR": "1"}, {"TLR_ARENAS": "1", "TLR_HYBRID": "0"},
+             {"TLR_TRIPLE": "0"}, {"TLR_TRIPLE": "1"}, {"TLR_PIPELINE_ROWS": "0", "TLR_HYBRID": "0"},
+             {"TLR_PIPELINE_ROWS": "2", "TLR_HYBRID": "0"}, {"TLR_PREP_BN": "128"},
+             {"TLR_PREP_BN": "128", "TLR_L1_BN": "128"}, {"TLR_QUAD": "1"}]
 
 
 @pytest.mark.parametrize("env", SCHEDULES, ids=lambda e: ",".join(f"{k}={v}" for k, v in e.items()) or "default")
