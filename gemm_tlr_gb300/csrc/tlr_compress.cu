@@ -111,33 +111,37 @@ __global__ void __launch_bounds__(kBigThreads) norm_kernel(const float *C, int64
 }
 
 // ---------------------------------------------------------------- batched SIMT GEMM
-// out(r, c) = sum_k A(r, k) B(k, c) for one TM x kTN block of one tile, K in
-// steps of TK; each of the 256 threads holds TM/16 x 4 results. kAk / kBk: the
-// operand's contiguous index is k (else r for A, c for B), which decides the
-// loading order so that neighbouring threads read neighbouring addresses (TK =
-// 32 gives 128-byte runs along a k-contiguous operand). kWide: partial sums of
+// out(r, c) = sum_k A(r, k) B(k, c) for one TM x TN block of one tile, K in
+// steps of TK; each of the 256 threads holds TM/16 x TN/16 results, its
+// columns in groups of four 64 apart (tx * 4 + 64 g + y), so that the float4
+// reads of a row of B touch consecutive addresses. kAk / kBk: the operand's
+// contiguous index is k (else r for A, c for B), which decides the loading
+// order so that neighbouring threads read neighbouring addresses (TK = 32
+// gives 128-byte runs along a k-contiguous operand). kWide: partial sums of
 // 512 products in fp32 are added into fp64 accumulators.
 constexpr int kTN = 64;
-template <int TM, int TK, bool kAk, bool kBk, bool kWide, class LA, class LB, class ST>
+template <int TM, int TK, bool kAk, bool kBk, bool kWide, int TN = kTN, class LA, class LB, class ST>
 __device__ __forceinline__ void gemm_block(int64_t M, int64_t N, int64_t K, int64_t m0, int64_t n0, LA la, LB lb,
                                            ST st) {
   constexpr int RM = TM / 16;          // rows per thread (4 or 8)
+  constexpr int CN = TN / 16;          // columns per thread (4 or 8)
   static_assert(TM == 64 || TM == 128, "tile rows");
+  static_assert(TN == 64 || TN == 128, "tile columns");
   static_assert(TK == 16 || TK == 32, "tile depth");
   __shared__ __align__(16) float As[TK][TM + 4];
-  __shared__ __align__(16) float Bs[TK][kTN + 4];
+  __shared__ __align__(16) float Bs[TK][TN + 4];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  float acc[RM][4];
-  double wacc[kWide ? RM : 1][kWide ? 4 : 1];
+  float acc[RM][CN];
+  double wacc[kWide ? RM : 1][kWide ? CN : 1];
 #pragma unroll
   for (int a = 0; a < RM; ++a)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
+    for (int c = 0; c < CN; ++c) acc[a][c] = 0.f;
   if constexpr (kWide) {
 #pragma unroll
     for (int a = 0; a < RM; ++a)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) wacc[a][c] = 0.0;
+      for (int c = 0; c < CN; ++c) wacc[a][c] = 0.0;
   }
   for (int64_t k0 = 0; k0 < K; k0 += TK) {
 #pragma unroll
@@ -148,34 +152,37 @@ __device__ __forceinline__ void gemm_block(int64_t M, int64_t N, int64_t K, int6
       As[k][r] = gr < M && gk < K ? la(gr, gk) : 0.f;
     }
 #pragma unroll
-    for (int q = 0; q < TK * kTN / kThreads; ++q) {
+    for (int q = 0; q < TK * TN / kThreads; ++q) {
       const int idx = tid + kThreads * q;
-      const int c = kBk ? idx / TK : idx % kTN, kb = kBk ? idx % TK : idx / kTN;
+      const int c = kBk ? idx / TK : idx % TN, kb = kBk ? idx % TK : idx / TN;
       const int64_t gc = n0 + c, gkb = k0 + kb;
       Bs[kb][c] = gc < N && gkb < K ? lb(gkb, gc) : 0.f;
     }
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < TK; ++k) {
-      float a[RM];
+      float a[RM], bb[CN];
 #pragma unroll
       for (int h = 0; h < RM / 4; ++h) {
         const float4 a4 = *reinterpret_cast<const float4 *>(&As[k][ty * RM + 4 * h]);
         a[4 * h] = a4.x; a[4 * h + 1] = a4.y; a[4 * h + 2] = a4.z; a[4 * h + 3] = a4.w;
       }
-      const float4 b4 = *reinterpret_cast<const float4 *>(&Bs[k][tx * 4]);
-      const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+      for (int h = 0; h < CN / 4; ++h) {
+        const float4 b4 = *reinterpret_cast<const float4 *>(&Bs[k][64 * h + tx * 4]);
+        bb[4 * h] = b4.x; bb[4 * h + 1] = b4.y; bb[4 * h + 2] = b4.z; bb[4 * h + 3] = b4.w;
+      }
 #pragma unroll
       for (int x = 0; x < RM; ++x)
 #pragma unroll
-        for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(a[x], bb[y], acc[x][y]);
+        for (int y = 0; y < CN; ++y) acc[x][y] = fmaf(a[x], bb[y], acc[x][y]);
     }
     if constexpr (kWide) {
       if ((k0 & 511) == 512 - TK || k0 + TK >= K) {
 #pragma unroll
         for (int x = 0; x < RM; ++x)
 #pragma unroll
-          for (int y = 0; y < 4; ++y) { wacc[x][y] += acc[x][y]; acc[x][y] = 0.f; }
+          for (int y = 0; y < CN; ++y) { wacc[x][y] += acc[x][y]; acc[x][y] = 0.f; }
       }
     }
     __syncthreads();
@@ -183,8 +190,8 @@ __device__ __forceinline__ void gemm_block(int64_t M, int64_t N, int64_t K, int6
 #pragma unroll
   for (int x = 0; x < RM; ++x)
 #pragma unroll
-    for (int y = 0; y < 4; ++y) {
-      const int64_t r = m0 + ty * RM + x, c = n0 + tx * 4 + y;
+    for (int y = 0; y < CN; ++y) {
+      const int64_t r = m0 + ty * RM + x, c = n0 + 64 * (y / 4) + tx * 4 + (y % 4);
       if (r < M && c < N) {
         if constexpr (kWide) st(r, c, static_cast<float>(wacc[x][y]));
         else st(r, c, acc[x][y]);
@@ -195,19 +202,21 @@ __device__ __forceinline__ void gemm_block(int64_t M, int64_t N, int64_t K, int6
 // rows of the GEMM blocks of each kernel
 constexpr int kSketchTM = 128, kProjTM = 64, kCoreTM = 64, kFactorTM = 128;
 
-// Y = T Omega (d_i x s)
+// Y = T Omega (d_i x s); TN: the block's columns (128 for sketches wider than
+// 64 columns, so that each block reads its rows of T once)
+template <int TN>
 __global__ void __launch_bounds__(kThreads) sketch_kernel(const float *C, int64_t ldc, const float *omega, Geo g,
                                                           int64_t t0, Scratch w) {
   const int64_t t = t0 + blockIdx.z;
   const int64_t i = t / g.nJ, j = t % g.nJ;
   if (is_dense_tile(g, i, j)) return;
   const int64_t di = tile_dim(g.m, g.b, i), dj = tile_dim(g.n, g.b, j);
-  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kSketchTM, n0 = static_cast<int64_t>(blockIdx.y) * kTN;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kSketchTM, n0 = static_cast<int64_t>(blockIdx.y) * TN;
   if (m0 >= di || n0 >= g.s) return;
   const float *T = C + i * g.b + j * g.b * ldc;
   float *Y = w.Q + blockIdx.z * w.q_stride;
   const int64_t b = g.b;
-  gemm_block<kSketchTM, 16, false, true, false>(
+  gemm_block<kSketchTM, 16, false, true, false, TN>(
       di, g.s, dj, m0, n0, [&](int64_t r, int64_t k) { return T[r + k * ldc]; },
       [&](int64_t k, int64_t c) { return omega[k + c * b]; }, [&](int64_t r, int64_t c, float v) { Y[r + c * b] = v; });
 }
@@ -666,7 +675,8 @@ tlr_status_t tlr_compress(tlr_handle_t h, const float *C, int64_t ldc, int64_t m
   for (int64_t t0 = 0; t0 < ntiles; t0 += batch) {
     const unsigned nb = static_cast<unsigned>(std::min<int64_t>(batch, ntiles - t0));
     norm_kernel<<<nb, kBigThreads, 0, st>>>(C, ldc, g, t0, w);
-    sketch_kernel<<<dim3(blocks(b, kSketchTM), sN, nb), kThreads, 0, st>>>(C, ldc, omega, g, t0, w);
+    if (s > 64) sketch_kernel<128><<<dim3(blocks(b, kSketchTM), blocks(s, 128), nb), kThreads, 0, st>>>(C, ldc, omega, g, t0, w);
+    else sketch_kernel<64><<<dim3(blocks(b, kSketchTM), sN, nb), kThreads, 0, st>>>(C, ldc, omega, g, t0, w);
     orth_kernel<<<nb, kOrthThreads, osm, st>>>(g, t0, w);
     project_kernel<<<dim3(blocks(s, kProjTM), bN, nb), kThreads, 0, st>>>(C, ldc, g, t0, w);
     core_kernel<<<dim3(blocks(s, kCoreTM), sN, nb), kThreads, 0, st>>>(g, t0, w);
